@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of TACO's fused FP8 compression hot path on GB300.
+
+One step is one pass of the whole path over one synthetic tensor (default: the
+GPT-style TP activation, bf16 [8192 x 4096], block 128):
+
+  1. taco_compress      x (bf16)            -> packed records    (Eqs. 5-10)
+  2. taco_reduce_shards P = 8 row-slices of the packed tensor, taken as the P
+                        compressed segments an owner receives in the two-shot
+                        AllReduce, -> one reduced segment          (Section 4.4.2)
+  3. taco_decompress    packed records      -> y (bf16)           (Eqs. 11-13)
+
+Each kernel is timed with CUDA events on the stream it runs on; before each
+kernel a read of a buffer twice the L2 size (untimed) evicts what the
+previous kernel left in L2, so every kernel reads its inputs from HBM.
+
+Metric: GB/s of bf16 data processed = (2N compressed + 2N decompressed + 2N
+logical bf16 bytes of the P reduced segments) per step / step time.  The
+roofline object reports the dominant kernel's algorithmic bytes per launch
+over its average duration against the measured HBM copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl taco|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+seed (weak scaling, no collective on the data path); timings are reduced with
+MAX over ranks and rank 0 prints the JSON line.  `--impl reference` times the
+CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "compress/decompress GB/s of bf16 input; % of GB300 HBM roofline"
+UNIT = "GB/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "compress": "fp8_compression_tensor_gb300/csrc/taco_compress.cu",
+    "decompress": "fp8_compression_tensor_gb300/csrc/taco_decompress.cu",
+    "reduce": "fp8_compression_tensor_gb300/csrc/taco_reduce.cu",
+}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["taco", "reference"], default="taco")
+    ap.add_argument("--workload", default="gpt_activation_8192x4096", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--block", type=int, default=128)
+    ap.add_argument("--shards", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Helpers
+# ---------------------------------------------------------------------------
+
+def source_hash(rel: str) -> str:
+    h = hashlib.sha256()
+    for p in (rel, "fp8_compression_tensor_gb300/csrc/taco_device.cuh"):
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def traffic_for(op: str, workload: str, block: int):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's
+    source has not changed since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        e = t[op][f"{workload}/b{block}"]
+        if e["source_hash"] != source_hash(KERNEL_SOURCES[op]):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks / throttle reasons every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid):
+        self.uuid = device_uuid
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.error = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # nvidia-smi missing
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        if self.error:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": self.error}
+        rows = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not rows:
+            rows = [p for (_, p) in self.samples]
+            window = "whole run"
+        else:
+            window = "timed region"
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        busy = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in busy if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "window": window,
+                "power_w_max": max((num(r[3]) or 0) for r in rows) if rows else None}
+
+
+# ---------------------------------------------------------------------------
+# Oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_step_time(x_bits: np.ndarray, block: int, shards: int, threads: int) -> float:
+    """Wall time of one oracle step (compress, reduce of the P row-slices,
+    decompress) over x_bits, split into block ranges across `threads`."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    x = np.ascontiguousarray(x_bits).reshape(-1)
+    n = x.size
+    nblk = n // block
+    rec = block + 8
+    seg_blk = nblk // shards
+    packed = np.empty(nblk * rec, dtype=np.uint8)
+    y = np.empty(n, dtype=np.uint16)
+    red = np.empty(seg_blk * rec, dtype=np.uint8)
+
+    def ranges(total):
+        c = max(1, -(-total // (4 * threads)))
+        return [(b, min(total, b + c)) for b in range(0, total, c)]
+
+    def comp(r):
+        b0, b1 = r
+        packed[b0 * rec:b1 * rec] = oracle.compress(x[b0 * block:b1 * block], block)
+
+    def reduce_(r):
+        b0, b1 = r
+        segs = [packed[(p * seg_blk + b0) * rec:(p * seg_blk + b1) * rec] for p in range(shards)]
+        red[b0 * rec:b1 * rec] = oracle.reduce_shards(segs, (b1 - b0) * block, block)
+
+    def decomp(r):
+        b0, b1 = r
+        y[b0 * block:b1 * block] = oracle.decompress(packed[b0 * rec:b1 * rec], (b1 - b0) * block, block)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(comp, ranges(nblk)))
+        list(ex.map(reduce_, ranges(seg_blk)))
+        list(ex.map(decomp, ranges(nblk)))
+    return time.perf_counter() - t0
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def sample_rows_for(w, block, shards, threads, budget_s):
+    """Rows of the workload whose oracle step takes about budget_s seconds
+    (a multiple of `shards` rows, at least `shards`)."""
+    probe_rows = max(shards, min(w.rows, 64 * shards))
+    x = w.tensor(row_count=probe_rows)
+    t = oracle_step_time(x, block, shards, threads)
+    rows = int(probe_rows * budget_s / max(t, 1e-6))
+    rows = max(shards, min(w.rows, rows)) // shards * shards
+    return rows
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    block, shards = args.block, args.shards
+    threads = host_threads()
+    # Size each step so that warm-up plus timed steps stay within ~2 minutes.
+    per_step_budget = min(15.0, 120.0 / max(1, args.steps + args.warmup))
+    rows = sample_rows_for(w, block, shards, threads, per_step_budget)
+    x = w.tensor(row_count=rows)
+    for _ in range(args.warmup):
+        oracle_step_time(x, block, shards, threads)
+    times = [oracle_step_time(x, block, shards, threads) for _ in range(args.steps)]
+    n = x.size
+    t = sum(times) / len(times)
+    value = 6.0 * n / t / 1e9
+    sample = (f"rows [0, {rows}) of the {w.rows}x{w.hidden} tensor ({n} elements) per step: "
+              f"compress, reduce of {shards} row-slices, decompress; block ranges split over {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "block": block,
+                   "reduce_shards": shards, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_taco(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    import fp8_compression_tensor_gb300 as taco
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    block, P = args.block, args.shards
+    rows, hidden = w.rows, w.hidden
+    if rows % P:
+        raise SystemExit(f"rows {rows} not divisible by {P} shards")
+    n = rows * hidden
+    seg_rows = rows // P
+    rec = block + 8
+    nbytes = taco.compressed_bytes(rows, hidden, block)
+    seg_bytes = taco.compressed_bytes(seg_rows, hidden, block)
+
+    x_host_bits = w.tensor(seed=w.seeds[0] + rank).reshape(rows, hidden)
+    x_pinned = torch.from_numpy(x_host_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x = x_pinned.to(dev)
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    y = torch.empty((rows, hidden), dtype=torch.bfloat16, device=dev)
+    reduced = torch.empty(seg_bytes, dtype=torch.uint8, device=dev)
+    segments = [packed[p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20)) or (128 << 20)
+    flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush():
+        flush_buf.sum()
+
+    def step(ev=None):
+        flush()
+        if ev: ev[0].record(stream)
+        taco.compress(x, block, out=packed, stream=stream)
+        if ev: ev[1].record(stream)
+        flush()
+        if ev: ev[2].record(stream)
+        taco.reduce_shards(segments, seg_rows, hidden, block, out=reduced, stream=stream)
+        if ev: ev[3].record(stream)
+        flush()
+        if ev: ev[4].record(stream)
+        taco.decompress(packed, rows, hidden, block, out=y, stream=stream)
+        if ev: ev[5].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    if not args.no_clocks:
+        sampler.start()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    taco.device_status()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    barrier()
+    t_wall0 = time.time()
+    for k in range(args.steps):
+        step(events[k])
+    barrier()
+    t_wall1 = time.time()
+    flags = taco.device_status()
+
+    comp = [e[0].elapsed_time(e[1]) for e in events]
+    red = [e[2].elapsed_time(e[3]) for e in events]
+    dec = [e[4].elapsed_time(e[5]) for e in events]
+    local = torch.tensor([sum(comp), sum(red), sum(dec)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(local, op=dist.ReduceOp.MAX)
+    tot_comp, tot_red, tot_dec = (float(v) for v in local.cpu())
+    K = args.steps
+    ms_step = (tot_comp + tot_red + tot_dec) / K
+
+    # End to end through the public API with host buffers: pinned H2D of the
+    # step's input, the three calls, D2H of the decompressed tensor and of
+    # the reduced segment, every step.
+    e2e = None
+    if not args.no_e2e:
+        y_pinned = torch.empty((rows, hidden), dtype=torch.bfloat16).pin_memory()
+        r_pinned = torch.empty(seg_bytes, dtype=torch.uint8).pin_memory()
+        for _ in range(max(1, min(args.warmup, 5))):
+            x.copy_(x_pinned, non_blocking=True)
+            step()
+            y_pinned.copy_(y, non_blocking=True)
+            r_pinned.copy_(reduced, non_blocking=True)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k_e2e = max(1, min(K, 200))
+        e0.record(stream)
+        for _ in range(k_e2e):
+            x.copy_(x_pinned, non_blocking=True)
+            taco.compress(x, block, out=packed, stream=stream)
+            taco.reduce_shards(segments, seg_rows, hidden, block, out=reduced, stream=stream)
+            taco.decompress(packed, rows, hidden, block, out=y, stream=stream)
+            y_pinned.copy_(y, non_blocking=True)
+            r_pinned.copy_(reduced, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        t = torch.tensor([e0.elapsed_time(e1) / k_e2e], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        e2e = {"value": world * 6.0 * n / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+               "steps": k_e2e, "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + seg_bytes}
+
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1) if not args.no_clocks else None
+
+    if rank != 0:
+        return
+
+    peak, peak_src = measured_peak()
+    alg = {
+        "compress": 2 * n + nbytes,
+        "reduce": P * seg_bytes + seg_bytes,
+        "decompress": nbytes + 2 * n,
+    }
+    avg_ms = {"compress": tot_comp / K, "reduce": tot_red / K, "decompress": tot_dec / K}
+    ops = {}
+    for op in ("compress", "reduce", "decompress"):
+        t = avg_ms[op] * 1e-3
+        ops[op] = {"ms": avg_ms[op], "bf16_gbs": 2 * n / t / 1e9,
+                   "hbm_gbs": alg[op] / t / 1e9, "frac_of_measured_hbm": alg[op] / t / 1e9 / peak,
+                   "algorithmic_bytes": alg[op]}
+    dom = max(avg_ms, key=avg_ms.get)
+    achieved = alg[dom] / (avg_ms[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": peak_src,
+                "traffic": traffic_for(dom, w.name, block),
+                "algorithmic_bytes_per_launch": alg[dom]}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        threads = host_threads()
+        srows = sample_rows_for(w, block, P, threads, max(1.0, 25.0 / threads))
+        xs = x_host_bits[:srows]
+        t_cpu = oracle_step_time(xs, block, P, threads)
+        cpu = {"value": 6.0 * xs.size / t_cpu / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"rows [0, {srows}) of the {rows}x{hidden} tensor: one oracle step (compress, "
+                         f"reduce of {P} row-slices, decompress), block ranges split over {threads} threads",
+               "seconds": t_cpu}
+
+    line = {
+        "metric": METRIC,
+        "value": world * 6.0 * n / (ms_step * 1e-3) / 1e9,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "rows": rows, "hidden": hidden, "block": block, "reduce_shards": P,
+                   "step": "compress + reduce_shards(P row-slices of the packed tensor) + decompress",
+                   "bytes_per_step": "6N: 2N compressed + 2N logical bf16 of the reduced segments + 2N decompressed",
+                   "l2": "read of a 2x-L2 buffer before each kernel (untimed); kernels timed with CUDA events",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "ops": ops,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "device_fault_flags": flags,
+        "wall_s_timed": t_wall1 - t_wall0,
+        "gpu": props.name,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_taco(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

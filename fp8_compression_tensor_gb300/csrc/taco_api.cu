@@ -1,0 +1,280 @@
+// taco_api.cu -- the C ABI of libtaco_gb300.so (declared in include/taco.h):
+// argument validation, per-device set-up, grid sizing and kernel launches.
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "taco.h"
+#include "taco_kernels.h"
+
+namespace taco {
+namespace {
+
+// Device-side fault flags (bits kFaultCompress, kFaultDecompress).
+__device__ uint32_t g_fault_flags;
+
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_error = cudaSuccess;
+    int sm_count = 0;
+    uint32_t *fault = nullptr;  // device address of g_fault_flags
+    int compress_ctas_per_sm[3] = {0, 0, 0};
+    int decompress_ctas_per_sm[3] = {0, 0, 0};
+    int reduce_ctas_per_sm[3] = {0, 0, 0};
+};
+
+DeviceState g_devices[kMaxDevices];
+
+int block_index(int block)
+{
+    return block == 64 ? 0 : block == 128 ? 1 : block == 256 ? 2 : -1;
+}
+
+taco_status_t cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = static_cast<int>(e);
+    return TACO_ERR_CUDA;
+}
+
+cudaError_t init_kernel(const KernelInfo &ki, int *ctas_per_sm)
+{
+    cudaError_t e = cudaSuccess;
+    if (ki.smem > 48 * 1024)
+        e = cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ki.smem));
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ki.fn, ki.threads, ki.smem);
+}
+
+void init_device(DeviceState &st)
+{
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.fault), g_fault_flags);
+    int dev = 0;
+    if (e == cudaSuccess)
+        e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    const int blocks[3] = {64, 128, 256};
+    for (int i = 0; i < 3 && e == cudaSuccess; i++) {
+        e = init_kernel(compress_kernel_info(blocks[i]), &st.compress_ctas_per_sm[i]);
+        if (e == cudaSuccess)
+            e = init_kernel(decompress_kernel_info(blocks[i]), &st.decompress_ctas_per_sm[i]);
+        if (e == cudaSuccess)
+            e = init_kernel(reduce_kernel_info(blocks[i]), &st.reduce_ctas_per_sm[i]);
+    }
+    st.init_error = e;
+}
+
+// Set-up of the current device, once per device and process.
+taco_status_t device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices)
+        return cuda_fail(cudaErrorInvalidDevice);
+    DeviceState &st = g_devices[dev];
+    std::call_once(st.once, init_device, std::ref(st));
+    if (st.init_error != cudaSuccess)
+        return cuda_fail(st.init_error);
+    *out = &st;
+    return TACO_OK;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+// Validates block and shape; on success sets the element count and packed bytes.
+taco_status_t check_shape(int64_t rows, int64_t hidden, int block, int64_t *n, int64_t *packed_bytes)
+{
+    if (block_index(block) < 0)
+        return TACO_ERR_UNSUPPORTED_BLOCK;
+    if (rows < 0 || hidden < 0 || hidden % block != 0)
+        return TACO_ERR_BAD_SHAPE;
+    if (rows != 0 && hidden > INT64_MAX / 4 / rows)  // keeps 2*n and the packed size in range
+        return TACO_ERR_BAD_SHAPE;
+    *n = rows * hidden;
+    *packed_bytes = *n / block * (block + 8);
+    return TACO_OK;
+}
+
+// Persistent grid: enough CTAs to fill every SM, no more than the work needs.
+int persistent_grid(int64_t ntiles, int warps_per_cta, int ctas_per_sm, int sm_count)
+{
+    const int64_t needed = (ntiles + warps_per_cta - 1) / warps_per_cta;
+    int64_t full = static_cast<int64_t>(sm_count) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    return static_cast<int>(needed < full ? needed : full);
+}
+
+}  // namespace
+}  // namespace taco
+
+using namespace taco;
+
+extern "C" {
+
+int64_t taco_compressed_bytes(int64_t rows, int64_t hidden, int block)
+{
+    int64_t n = 0, bytes = 0;
+    if (check_shape(rows, hidden, block, &n, &bytes) != TACO_OK)
+        return -1;
+    return bytes;
+}
+
+taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t hidden, int block, void *packed_out,
+                            taco_stream_t stream)
+{
+    int64_t n = 0, bytes = 0;
+    taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
+    if (st != TACO_OK || n == 0)
+        return st;
+    if (!x_bf16 || !packed_out)
+        return TACO_ERR_NULL_POINTER;
+    if (!aligned16(x_bf16) || !aligned16(packed_out))
+        return TACO_ERR_MISALIGNED;
+    if (overlap(x_bf16, 2 * n, packed_out, bytes))
+        return TACO_ERR_OVERLAP;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != TACO_OK)
+        return st;
+    const KernelInfo ki = compress_kernel_info(block);
+    const int64_t nblocks = n / block;
+    const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
+    const int grid = persistent_grid(ntiles, ki.warps, dev->compress_ctas_per_sm[block_index(block)], dev->sm_count);
+    const cudaError_t e = launch_compress(block, x_bf16, packed_out, nblocks, dev->fault, grid,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TACO_OK : cuda_fail(e);
+}
+
+taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidden, int block, void *y_bf16_out,
+                              taco_stream_t stream)
+{
+    int64_t n = 0, bytes = 0;
+    taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
+    if (st != TACO_OK || n == 0)
+        return st;
+    if (!packed_in || !y_bf16_out)
+        return TACO_ERR_NULL_POINTER;
+    if (!aligned16(packed_in) || !aligned16(y_bf16_out))
+        return TACO_ERR_MISALIGNED;
+    if (overlap(packed_in, bytes, y_bf16_out, 2 * n))
+        return TACO_ERR_OVERLAP;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != TACO_OK)
+        return st;
+    const KernelInfo ki = decompress_kernel_info(block);
+    const int64_t nblocks = n / block;
+    const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
+    const int grid =
+        persistent_grid(ntiles, ki.warps, dev->decompress_ctas_per_sm[block_index(block)], dev->sm_count);
+    const cudaError_t e = launch_decompress(block, packed_in, y_bf16_out, nblocks, dev->fault, grid,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TACO_OK : cuda_fail(e);
+}
+
+taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shards, int64_t rows, int64_t hidden,
+                                 int block, void *packed_out, taco_stream_t stream)
+{
+    int64_t n = 0, bytes = 0;
+    taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
+    if (st != TACO_OK)
+        return st;
+    if (num_shards < 1 || num_shards > TACO_MAX_SHARDS)
+        return TACO_ERR_BAD_SHARDS;
+    if (n == 0)
+        return TACO_OK;
+    if (!packed_shards || !packed_out)
+        return TACO_ERR_NULL_POINTER;
+    ReduceArgs args{};
+    for (int p = 0; p < num_shards; p++) {
+        if (!packed_shards[p])
+            return TACO_ERR_NULL_POINTER;
+        if (!aligned16(packed_shards[p]))
+            return TACO_ERR_MISALIGNED;
+        if (overlap(packed_shards[p], bytes, packed_out, bytes))
+            return TACO_ERR_OVERLAP;
+        args.shards[p] = static_cast<const uint8_t *>(packed_shards[p]);
+    }
+    if (!aligned16(packed_out))
+        return TACO_ERR_MISALIGNED;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != TACO_OK)
+        return st;
+    args.out = static_cast<uint8_t *>(packed_out);
+    args.nblocks = n / block;
+    args.num_shards = num_shards;
+    const KernelInfo ki = reduce_kernel_info(block);
+    const int64_t threads_needed = args.nblocks * (block / 8);
+    const int64_t ctas_needed = (threads_needed + ki.threads - 1) / ki.threads;
+    const int per_sm = dev->reduce_ctas_per_sm[block_index(block)];
+    const int64_t full = static_cast<int64_t>(dev->sm_count) * (per_sm > 0 ? per_sm : 1);
+    const int grid = static_cast<int>(ctas_needed < full ? ctas_needed : full);
+    const cudaError_t e = launch_reduce(block, args, grid, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TACO_OK : cuda_fail(e);
+}
+
+taco_status_t taco_device_status(taco_stream_t stream, uint32_t *flags_out)
+{
+    DeviceState *dev = nullptr;
+    taco_status_t st = device_state(&dev);
+    if (st != TACO_OK)
+        return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    uint32_t flags = 0;
+    if (e == cudaSuccess)
+        e = cudaMemcpy(&flags, dev->fault, sizeof flags, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && flags != 0) {
+        const uint32_t zero = 0;
+        e = cudaMemcpy(dev->fault, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    }
+    if (flags_out)
+        *flags_out = flags;
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return flags ? TACO_ERR_DEVICE_FAULT : TACO_OK;
+}
+
+const char *taco_status_string(taco_status_t status)
+{
+    switch (status) {
+    case TACO_OK: return "TACO_OK";
+    case TACO_ERR_NULL_POINTER: return "TACO_ERR_NULL_POINTER: a required pointer is NULL";
+    case TACO_ERR_BAD_SHAPE: return "TACO_ERR_BAD_SHAPE: rows/hidden negative, hidden not a multiple of the block, or too large";
+    case TACO_ERR_UNSUPPORTED_BLOCK: return "TACO_ERR_UNSUPPORTED_BLOCK: block must be 64, 128 or 256";
+    case TACO_ERR_MISALIGNED: return "TACO_ERR_MISALIGNED: device pointers must be 16-byte aligned";
+    case TACO_ERR_BAD_SHARDS: return "TACO_ERR_BAD_SHARDS: num_shards must be in [1, 16]";
+    case TACO_ERR_OVERLAP: return "TACO_ERR_OVERLAP: an output overlaps an input";
+    case TACO_ERR_CUDA: return "TACO_ERR_CUDA: a CUDA call failed (see taco_last_cuda_error)";
+    case TACO_ERR_DEVICE_FAULT: return "TACO_ERR_DEVICE_FAULT: a kernel gave up waiting for a copy";
+    default: return "unknown taco_status_t";
+    }
+}
+
+int taco_last_cuda_error(void)
+{
+    return t_last_cuda_error;
+}
+
+int taco_abi_version(void)
+{
+    return TACO_ABI_VERSION;
+}
+
+}  // extern "C"

@@ -1,0 +1,241 @@
+// taco_device.cuh -- device-side building blocks shared by the TACO kernels:
+// the fixed constants, inline-PTX wrappers for mbarriers and bulk (TMA) copies,
+// E4M3 / bf16 conversions, packed FP32x2 arithmetic and the bounded wait.
+//
+// Method: "TACO: Efficient Communication Compression of Intermediate Tensors
+// for Scalable Tensor-Parallel LLM Training", Algorithm 1, Eqs. (6)-(13).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace taco {
+
+// Constants the paper leaves open (Eqs. 6, 7, 9): target RMS tau, eps inside
+// the root, largest finite E4M3 value.
+constexpr float kTau = 1.0f;
+constexpr float kEps = 1e-30f;
+constexpr float kQmax = 448.0f;
+
+// Fault flag bits written when a kernel gives up waiting.
+constexpr uint32_t kFaultCompress = 1u;
+constexpr uint32_t kFaultDecompress = 2u;
+
+// A wait on the copy engine gives up after this long (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// Shared memory, mbarriers and bulk copies
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses with later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for phase `parity` of the barrier, for at most kWaitLimitNs.  The
+// outcome is the same for every lane of the warp.  On a timeout the fault bit
+// is set and false is returned.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t *fault,
+                                                  uint32_t fault_bit)
+{
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_timer_ns();
+        while (!(ok = mbar_try_wait(bar, parity))) {
+            if (global_timer_ns() - t0 > kWaitLimitNs)
+                break;
+        }
+    }
+    ok = __all_sync(kFullMask, ok);
+    if (!ok && (threadIdx.x & 31) == 0)
+        atomicOr(fault, fault_bit);
+    return ok;
+}
+
+// Bulk copy global -> shared (size a multiple of 16, both addresses 16-byte
+// aligned); completion is counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Bulk copy shared -> global, tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// At most N of this thread's bulk groups may still be reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// At most N of this thread's bulk groups may still be in flight.
+template <int N>
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b)
+{
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Number formats
+// ---------------------------------------------------------------------------
+
+// The two bf16 values packed in a 32-bit word, as floats (exact).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Cvt_FP8 (Eq. 10) of two floats: round to nearest even, saturate to +-448.
+// Returns 16 bits: `lo` in the low byte, `hi` in the high byte.
+__device__ __forceinline__ uint32_t e4m3x2_from_float2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Cvt_FP32 (Eq. 11) of the two E4M3 codes in the low 16 bits of `pair`
+// (exact): low byte -> .x, high byte -> .y.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// Two floats -> two bf16 (round to nearest even) packed in a word, lo first.
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Packed FP32x2 arithmetic (one instruction for two lanes of data)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// In-register Walsh-Hadamard butterflies over the pair index of v[0..NP-1]:
+// pair i and pair i^h are combined as (a + b, a - b) for h = 1, 2, ..., NP/2,
+// i.e. the stages for element-index bits 1 .. log2(NP) when pair i holds
+// elements (2i, 2i+1).  Stage order matches the FWHT of Section 4.2.2.
+template <int NP>
+__device__ __forceinline__ void fwht_pairs(float2 (&v)[NP])
+{
+#pragma unroll
+    for (int h = 1; h < NP; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < NP; i++) {
+            if ((i & h) == 0) {
+                const float2 a = v[i], b = v[i + h];
+                v[i] = add2(a, b);
+                v[i + h] = sub2(a, b);
+            }
+        }
+    }
+}
+
+}  // namespace taco

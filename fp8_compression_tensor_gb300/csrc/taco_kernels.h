@@ -1,0 +1,39 @@
+// taco_kernels.h -- host-side view of the TACO kernels (internal to the library).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace taco {
+
+// Launch facts of one kernel instantiation.
+struct KernelInfo {
+    void *fn = nullptr;     // kernel entry (for attributes and occupancy queries)
+    size_t smem = 0;        // dynamic shared memory per CTA
+    int threads = 0;        // threads per CTA
+    int tile_blocks = 0;    // blocks per warp tile (0 for grid-stride kernels)
+    int warps = 0;          // warps per CTA
+};
+
+KernelInfo compress_kernel_info(int block);
+KernelInfo decompress_kernel_info(int block);
+KernelInfo reduce_kernel_info(int block);
+
+cudaError_t launch_compress(int block, const void *x, void *packed, int64_t nblocks, uint32_t *fault, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_decompress(int block, const void *packed, void *y, int64_t nblocks, uint32_t *fault, int grid,
+                              cudaStream_t stream);
+
+constexpr int kMaxShards = 16;
+
+struct ReduceArgs {
+    const uint8_t *shards[kMaxShards];
+    uint8_t *out;
+    int64_t nblocks;
+    int num_shards;
+};
+
+cudaError_t launch_reduce(int block, const ReduceArgs &args, int grid, cudaStream_t stream);
+
+}  // namespace taco

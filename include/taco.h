@@ -1,0 +1,142 @@
+/*
+ * taco.h -- C ABI of libtaco_gb300.so: TACO's fused FP8 compression of
+ * tensor-parallel intermediate tensors, as CUDA kernels for GB300 (sm_103a).
+ *
+ * Method: "TACO: Efficient Communication Compression of Intermediate Tensors
+ * for Scalable Tensor-Parallel LLM Training", Algorithm 1 and Eqs. (5)-(13),
+ * Sections 4.2-4.4.
+ *
+ * Constants the paper leaves open, fixed here:
+ *   tau = 1 (target RMS of a block after the Adaptive Scale, Eq. 7),
+ *   eps = 1e-30 (inside the square root of Eq. 6),
+ *   Q_max = 448 (largest finite OCP E4M3 value, Eq. 9),
+ *   H_B = Sylvester Hadamard matrix in natural order, (H_B)_ij = (-1)^popcount(i&j),
+ *   Cvt_FP8 = round to nearest even, saturating to +-448 (Eq. 10).
+ *
+ * Tensor layout: a row-major bf16 tensor [rows, hidden] with hidden % block == 0,
+ * seen as M = rows*hidden/block contiguous blocks of `block` elements (Eq. 5).
+ *
+ * Packed layout ("zero-copy metadata layout", Section 4.4.2): one buffer of
+ * M records; record k starts at byte k*(block+8) and holds the block's `block`
+ * E4M3 codes in element order, then alpha_k and s_k as little-endian float32.
+ * taco_compressed_bytes() gives its size.
+ *
+ * Common rules for every call below:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     16-byte aligned (TACO_ERR_MISALIGNED otherwise).  The caller allocates
+ *     and frees every buffer; the library allocates no memory.
+ *   - Inputs and outputs must not overlap (TACO_ERR_OVERLAP).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.  TACO_OK means the
+ *     kernel was launched.  Argument errors are found on the host before any
+ *     launch and leave every output untouched.
+ *   - rows == 0 or hidden == 0 is an empty tensor: TACO_OK, nothing launched,
+ *     pointers may be NULL.
+ *   - Supported blocks: 64, 128, 256 (TACO_ERR_UNSUPPORTED_BLOCK otherwise).
+ *   - Inputs must be finite with |x| < 2^56; beyond that the FP32 block
+ *     energy of Eq. (6) can overflow and the output is unspecified.
+ *   - Kernels that wait on the copy engine give up after about one second,
+ *     set a device-side fault flag and return; taco_device_status() reads it.
+ */
+#ifndef TACO_GB300_H
+#define TACO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TACO_API __attribute__((visibility("default")))
+#else
+#define TACO_API
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *taco_stream_t;
+
+typedef enum taco_status {
+    TACO_OK = 0,
+    TACO_ERR_NULL_POINTER = 1,      /* a required pointer is NULL */
+    TACO_ERR_BAD_SHAPE = 2,         /* rows < 0, hidden < 0, hidden % block != 0, or size overflow */
+    TACO_ERR_UNSUPPORTED_BLOCK = 3, /* block not in {64, 128, 256} */
+    TACO_ERR_MISALIGNED = 4,        /* a device pointer is not 16-byte aligned */
+    TACO_ERR_BAD_SHARDS = 5,        /* num_shards < 1 or > TACO_MAX_SHARDS */
+    TACO_ERR_OVERLAP = 6,           /* an output overlaps an input */
+    TACO_ERR_CUDA = 7,              /* a CUDA runtime call or launch failed; see taco_last_cuda_error() */
+    TACO_ERR_DEVICE_FAULT = 8       /* taco_device_status(): a kernel gave up waiting */
+} taco_status_t;
+
+#define TACO_MAX_SHARDS 16
+#define TACO_ABI_VERSION 1
+
+/* Bytes of the packed buffer for a [rows, hidden] tensor: (rows*hidden/block)*(block+8).
+ * Returns -1 for an unsupported block, a bad shape or an overflow. */
+TACO_API int64_t taco_compressed_bytes(int64_t rows, int64_t hidden, int block);
+
+/*
+ * Sender side, Algorithm 1 lines 4-16 (Eqs. 5-10), one fused kernel: for every
+ * block G_k of x, sigma_k = sqrt(mean(G_k^2) + eps) (Eq. 6), alpha_k = tau/sigma_k
+ * (Eq. 7), Z_k = (1/sqrt B) H_B (alpha_k G_k) (Eq. 8), s_k = max|Z_k| / Q_max
+ * (Eq. 9), q_k = Cvt_FP8(Z_k / s_k) (Eq. 10); writes the record (q_k, alpha_k, s_k).
+ * A block with max|Z_k| = 0 gets s_k = 0 and all codes 0x00.
+ *
+ *   x_bf16      device, in:  rows*hidden bf16 values, row-major
+ *   packed_out  device, out: taco_compressed_bytes(rows, hidden, block) bytes
+ */
+TACO_API taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t hidden, int block,
+                            void *packed_out, taco_stream_t stream);
+
+/*
+ * Receiver side, Algorithm 1 lines 19-24 (Eqs. 11-13), the fused decompress
+ * kernel (Section 4.1, "fused_ash_decompress_kernel"): Zhat_k = Cvt_FP32(q_k) s_k,
+ * Ghat_k = (1/sqrt B) H_B Zhat_k, G'_k = Ghat_k / alpha_k, rounded to bf16
+ * (nearest even).
+ *
+ *   packed_in   device, in:  taco_compressed_bytes(rows, hidden, block) bytes
+ *   y_bf16_out  device, out: rows*hidden bf16 values, row-major
+ */
+TACO_API taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidden, int block,
+                              void *y_bf16_out, taco_stream_t stream);
+
+/*
+ * Receive-side local reduction of the two-shot compressed AllReduce (Section
+ * 4.4.2: "one compressed AlltoAll operation followed by a single local
+ * reduction"): the P packed shards of the same [rows, hidden] tensor are
+ * decoded to FP32 (Eqs. 11-13, no bf16 rounding), summed, and the FP32 sum is
+ * compressed once (Eqs. 6-10) into packed_out.
+ *
+ *   packed_shards  HOST array of num_shards DEVICE pointers, each to
+ *                  taco_compressed_bytes(rows, hidden, block) bytes; the array
+ *                  is read during the call only and may be freed afterwards
+ *   num_shards     P, 1 <= P <= TACO_MAX_SHARDS
+ *   packed_out     device, out: taco_compressed_bytes(rows, hidden, block) bytes,
+ *                  overlapping no shard
+ */
+TACO_API taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shards, int64_t rows,
+                                 int64_t hidden, int block, void *packed_out, taco_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's fault
+ * flags (bit 0: compress, bit 1: decompress gave up waiting for a copy).
+ * *flags_out (may be NULL) receives them.  Returns TACO_ERR_DEVICE_FAULT if any
+ * flag was set, TACO_ERR_CUDA if a CUDA call failed, TACO_OK otherwise.
+ */
+TACO_API taco_status_t taco_device_status(taco_stream_t stream, uint32_t *flags_out);
+
+/* Static, human-readable name of a status. */
+TACO_API const char *taco_status_string(taco_status_t status);
+
+/* The cudaError_t value behind the calling thread's last TACO_ERR_CUDA (0 if none). */
+TACO_API int taco_last_cuda_error(void);
+
+/* TACO_ABI_VERSION of the loaded library. */
+TACO_API int taco_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TACO_GB300_H */

@@ -1,0 +1,117 @@
+"""Parity helpers shared by the GPU tests, the smoke check and the benchmark:
+compare packed records and reconstructions against the CPU oracle.
+
+The tolerances are the ones the compression operator is judged by:
+  - alpha_k and s_k agree to 1e-6 relative (s_k = 0 blocks exactly);
+  - E4M3 codes are identical except in at most 1e-4 of the elements, and
+    those differ by exactly one E4M3 step (+0 / -0 count as equal values and
+    are reported separately);
+  - the reconstruction relative L2 error ||x' - x|| / ||x|| (fp64 over the
+    whole tensor) is within 1e-3 (absolute) of the oracle's.
+Decompressed bf16 values are both nearest-even roundings of FP32 results that
+differ only by rounding order, so they may differ by one bf16 step where the
+exact value sits near a rounding midpoint; the check bounds that difference
+element by element.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+import oracle
+from helpers import bf16_to_f64, code_step_distance, records
+
+SCALE_RTOL = 1e-6
+CODE_MISMATCH_MAX = 1e-4
+RELL2_ATOL = 1e-3
+
+
+def _threads():
+    return min(16, os.cpu_count() or 1)
+
+
+def oracle_compress_parallel(x_bf16: np.ndarray, block: int) -> np.ndarray:
+    """The oracle's compress over disjoint block ranges on several threads
+    (blocks are independent, so this is the same function of the input)."""
+    x = np.ascontiguousarray(x_bf16).reshape(-1)
+    nblk = x.size // block
+    out = np.empty(nblk * (block + 8), dtype=np.uint8)
+    chunk = max(1, -(-nblk // (4 * _threads())))
+
+    def run(b0):
+        b1 = min(nblk, b0 + chunk)
+        out[b0 * (block + 8):b1 * (block + 8)] = oracle.compress(x[b0 * block:b1 * block], block)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(run, range(0, nblk, chunk)))
+    return out
+
+
+def oracle_decompress_parallel(packed: np.ndarray, n: int, block: int) -> np.ndarray:
+    nblk = n // block
+    out = np.empty(n, dtype=np.uint16)
+    chunk = max(1, -(-nblk // (4 * _threads())))
+
+    def run(b0):
+        b1 = min(nblk, b0 + chunk)
+        out[b0 * block:b1 * block] = oracle.decompress(packed[b0 * (block + 8):b1 * (block + 8)],
+                                                       (b1 - b0) * block, block)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(run, range(0, nblk, chunk)))
+    return out
+
+
+def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = True) -> dict:
+    """Compares packed records (uint8 arrays) from two implementations."""
+    cg, ag, sg = records(got, block)
+    cr, ar, sr = records(ref, block)
+    d = code_step_distance(cg, cr)
+    zero_sign = (cg != cr) & (d == 0)
+    n = cg.size
+    nz = sr > 0
+    alpha_rel = float(np.max(np.abs(ag / ar - 1))) if ar.size else 0.0
+    s_rel = float(np.max(np.abs(sg[nz] / sr[nz] - 1))) if nz.any() else 0.0
+    stats = {
+        "blocks": int(cr.shape[0]),
+        "code_mismatch_frac": float((d > 0).sum() / max(n, 1)),
+        "code_max_step": int(d.max()) if n else 0,
+        "signed_zero_diffs": int(zero_sign.sum()),
+        "alpha_max_rel": alpha_rel,
+        "s_max_rel": s_rel,
+        "s_zero_mismatch": int(((sg == 0) != (sr == 0)).sum()),
+    }
+    if check:
+        assert stats["code_mismatch_frac"] <= CODE_MISMATCH_MAX, stats
+        assert stats["code_max_step"] <= 1, stats
+        assert stats["alpha_max_rel"] <= SCALE_RTOL, stats
+        assert stats["s_max_rel"] <= SCALE_RTOL, stats
+        assert stats["s_zero_mismatch"] == 0, stats
+    return stats
+
+
+def compare_decoded(got_bf16: np.ndarray, ref_bf16: np.ndarray, block: int, check: bool = True) -> dict:
+    """Element-wise check of two bf16 reconstructions of the same records: at
+    most one bf16 step apart, and only where FP32 rounding noise of the
+    block's scale (2e-6 of the block's largest value) can reach a midpoint."""
+    g = bf16_to_f64(got_bf16).reshape(-1, block)
+    r = bf16_to_f64(ref_bf16).reshape(-1, block)
+    diff = np.abs(g - r)
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 1e-38))) - 7)
+    bmax = np.abs(r).max(axis=1, keepdims=True)
+    ok = diff <= np.maximum(step, 0) + 2e-6 * bmax
+    stats = {"mismatch_frac": float((diff > 0).mean()) if diff.size else 0.0,
+             "bad": int((~ok).sum())}
+    if check:
+        assert stats["bad"] == 0, stats
+        assert stats["mismatch_frac"] <= 1e-2, stats
+    return stats
+
+
+def rel_l2_bf16(xhat_bf16: np.ndarray, x_bf16: np.ndarray) -> float:
+    x = bf16_to_f64(x_bf16).reshape(-1)
+    xh = bf16_to_f64(xhat_bf16).reshape(-1)
+    nx = np.linalg.norm(x)
+    return float(np.linalg.norm(xh - x) / nx) if nx > 0 else float(np.linalg.norm(xh))

@@ -1,0 +1,62 @@
+"""The C-ABI library loads without a GPU and exports every entry point that
+include/taco.h declares; host-side validation needs no device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"TACO_API\s+[\w\s\*]+?\b(taco_\w+)\s*\(", txt))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_compression_tensor_gb300 import build
+    build.build()
+    import fp8_compression_tensor_gb300 as t
+    return t.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert {"taco_compress", "taco_decompress", "taco_reduce_shards", "taco_compressed_bytes"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_host_side_queries(lib):
+    import fp8_compression_tensor_gb300 as t
+    assert lib.taco_abi_version() == 1
+    assert t.compressed_bytes(8192, 4096, 128) == 8192 * 4096 // 128 * 136
+    assert t.compressed_bytes(0, 4096, 64) == 0
+    assert lib.taco_compressed_bytes(16, 100, 64) == -1
+    assert lib.taco_compressed_bytes(16, 128, 32) == -1
+    assert lib.taco_compressed_bytes(-1, 128, 128) == -1
+    assert lib.taco_compressed_bytes(1 << 40, 1 << 40, 128) == -1
+    for s in range(9):
+        assert lib.taco_status_string(s)
+    # Argument errors are found before any CUDA call.
+    assert lib.taco_compress(None, 4, 100, 64, None, None) == 2
+    assert lib.taco_compress(None, 4, 128, 96, None, None) == 3
+    assert lib.taco_compress(None, 4, 128, 128, None, None) == 1
+    assert lib.taco_compress(16, 4, 128, 128, 2, None) == 4
+    assert lib.taco_compress(0, 0, 128, 128, 0, None) == 0
+    ptrs = (ctypes.c_void_p * 1)(16)
+    assert lib.taco_reduce_shards(ptrs, 0, 4, 128, 128, 32, None) == 5
+    assert lib.taco_reduce_shards(ptrs, 17, 4, 128, 128, 32, None) == 5
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import fp8_compression_tensor_gb300 as t
+    with pytest.raises(TypeError):
+        t.compress(torch.zeros(4, 128, dtype=torch.bfloat16), 128)

@@ -1,0 +1,119 @@
+"""GPU parity at the five workloads' full sizes, in the launch configuration the
+benchmark times (one call over the whole tensor).  The oracle recomputes a
+sample of blocks one by one (plus the first and last blocks, so both ragged
+ends of the grid are covered), and the reconstruction relative L2 error over
+the whole tensor is compared with the oracle's own (the oracle runs over the
+whole tensor on several threads)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import (RELL2_ATOL, compare_records, oracle_compress_parallel, oracle_decompress_parallel,
+                    rel_l2_bf16)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+DEV = "cuda:0"
+N_SAMPLE = 3000
+
+
+@pytest.fixture(scope="module")
+def taco():
+    import fp8_compression_tensor_gb300 as t
+    t.load_library()
+    return t
+
+
+def to_dev(x_bits, rows, hidden):
+    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).reshape(
+        rows, hidden).to(DEV)
+
+
+def sample_blocks(nblocks, seed):
+    rng = np.random.default_rng(seed)
+    s = rng.choice(nblocks, size=min(N_SAMPLE, nblocks), replace=False)
+    return np.unique(np.concatenate([s, [0, 1, nblocks - 2, nblocks - 1]]))
+
+
+def block_rows(packed, ids, block):
+    rec = packed.reshape(-1, block + 8)
+    return rec[ids].reshape(-1)
+
+
+CASES = [("small_4096x1024", 128), ("gpt_activation_8192x4096", 128), ("tp_grad_8192x5120", 128),
+         ("large_16384x8192", 64), ("large_16384x8192", 128), ("large_16384x8192", 256)]
+
+
+@pytest.mark.parametrize("name,block", CASES)
+def test_full_size_compress_decompress(taco, name, block):
+    w = workloads.WORKLOADS[name]
+    x = w.tensor().reshape(-1)
+    nblocks = x.size // block
+    xd = to_dev(x, w.rows, w.hidden)
+    packed = taco.compress(xd, block)
+    y = taco.decompress(packed, w.rows, w.hidden, block)
+    torch.cuda.synchronize()
+    assert taco.device_status() == 0
+    got = packed.cpu().numpy()
+    ids = sample_blocks(nblocks, 1)
+    xs = x.reshape(-1, block)[ids].reshape(-1)
+    compare_records(block_rows(got, ids, block), oracle.compress(xs, block), block)
+    # Whole-tensor reconstruction error against the oracle's.
+    ref = oracle_compress_parallel(x, block)
+    y_ref = oracle_decompress_parallel(ref, x.size, block)
+    y_gpu = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
+    e_gpu, e_ref = rel_l2_bf16(y_gpu, x), rel_l2_bf16(y_ref, x)
+    assert abs(e_gpu - e_ref) <= RELL2_ATOL, (e_gpu, e_ref)
+    del xd, packed, y
+    torch.cuda.empty_cache()
+
+
+def test_full_size_shard_reduce(taco):
+    """Eight shards of the full [8192 x 5120] workload.  (1) Reduce in isolation:
+    the GPU reduces the oracle's packed shards, and the oracle reduces the same
+    shards' sampled records.  (2) The whole pipeline on the GPU (compress each
+    shard, reduce, decompress) against the oracle's pipeline: relative L2 error
+    of the decoded sum against the exact sum of the bf16 shards."""
+    w = workloads.WORKLOADS["shard_reduce_p8_8192x5120"]
+    block = 128
+    xs = [w.tensor(seed=p).reshape(-1) for p in w.seeds]
+    n = xs[0].size
+    ref_shards = [oracle_compress_parallel(x, block) for x in xs]
+    out = taco.reduce_shards([torch.from_numpy(r).to(DEV) for r in ref_shards], w.rows, w.hidden, block)
+    torch.cuda.synchronize()
+    assert taco.device_status() == 0
+    ids = sample_blocks(n // block, 2)
+    ref = oracle.reduce_shards([block_rows(r, ids, block) for r in ref_shards], ids.size * block, block)
+    compare_records(block_rows(out.cpu().numpy(), ids, block), ref, block)
+    del out
+
+    gpu_shards = [taco.compress(to_dev(x, w.rows, w.hidden), block) for x in xs]
+    red = taco.reduce_shards(gpu_shards, w.rows, w.hidden, block)
+    y = taco.decompress(red, w.rows, w.hidden, block)
+    torch.cuda.synchronize()
+    y_gpu = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
+    total = np.zeros(n, dtype=np.float64)
+    for x in xs:
+        total += (x.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    # The oracle's pipeline on the whole tensor, block ranges on several threads.
+    from concurrent.futures import ThreadPoolExecutor
+    nblk = n // block
+    chunk = -(-nblk // 64)
+    y_ref = np.empty(n, dtype=np.uint16)
+
+    def run(b0):
+        b1 = min(nblk, b0 + chunk)
+        sl = [r[b0 * (block + 8):b1 * (block + 8)] for r in ref_shards]
+        rr = oracle.reduce_shards(sl, (b1 - b0) * block, block)
+        y_ref[b0 * block:b1 * block] = oracle.decompress(rr, (b1 - b0) * block, block)
+
+    with ThreadPoolExecutor(16) as ex:
+        list(ex.map(run, range(0, nblk, chunk)))
+    yg = (y_gpu.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    yr = (y_ref.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    nt = np.linalg.norm(total)
+    e_gpu = np.linalg.norm(yg - total) / nt
+    e_ref = np.linalg.norm(yr - total) / nt
+    assert abs(e_gpu - e_ref) <= RELL2_ATOL, (e_gpu, e_ref)
