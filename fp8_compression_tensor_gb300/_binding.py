@@ -103,7 +103,8 @@ def compressed_bytes(rows: int, hidden: int, block: int = 128) -> int:
     """Size in bytes of the packed records of a [rows, hidden] tensor."""
     n = load_library().taco_compressed_bytes(rows, hidden, block)
     if n < 0:
-        raise ValueError(f"unsupported shape/block: rows={rows} hidden={hidden} block={block}")
+        status = 3 if block not in SUPPORTED_BLOCKS else 2
+        raise TacoError(status, "compressed_bytes", f"(rows={rows} hidden={hidden} block={block})")
     return int(n)
 
 

@@ -211,6 +211,15 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
+// w + a * f with the product rounded on its own before the add (scalar
+// __fmul_rn / __fadd_rn are never contracted into a fused multiply-add; the
+// packed FP32x2 forms can be).  Used where a sum of products must behave like a
+// sum of separately rounded terms, e.g. so that x*f + (-x)*f is exactly 0.
+__device__ __forceinline__ float2 add_rounded_product(float2 w, float2 a, float f)
+{
+    return make_float2(__fadd_rn(w.x, __fmul_rn(a.x, f)), __fadd_rn(w.y, __fmul_rn(a.y, f)));
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
     float r;

@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
         for (int i = 0; i < 4; i++)
             w[i] = make_float2(0.f, 0.f);
 
-        // W = sum_p q_p * (s_p / alpha_p), four shards' loads in flight at a time.
+        // W = sum_p q_p * (s_p / alpha_p) in shard order, four shards' loads in flight at a time.
         for (int p0 = 0; p0 < P; p0 += 4) {
             uint2 codes[4], meta[4];
 #pragma unroll
@@ -68,11 +68,13 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
             for (int i = 0; i < 4; i++) {
                 if (p0 + i < P) {
                     const float f = __fdiv_rn(__uint_as_float(meta[i].y), __uint_as_float(meta[i].x));
-                    const float2 f2 = make_float2(f, f);
-                    w[0] = fma2(e4m3x2_to_float2(codes[i].x & 0xffffu), f2, w[0]);
-                    w[1] = fma2(e4m3x2_to_float2(codes[i].x >> 16), f2, w[1]);
-                    w[2] = fma2(e4m3x2_to_float2(codes[i].y & 0xffffu), f2, w[2]);
-                    w[3] = fma2(e4m3x2_to_float2(codes[i].y >> 16), f2, w[3]);
+                    // Each product rounded on its own, then added: a shard and
+                    // its negation cancel exactly, as in an FP32 sum of decoded
+                    // shards.
+                    w[0] = add_rounded_product(w[0], e4m3x2_to_float2(codes[i].x & 0xffffu), f);
+                    w[1] = add_rounded_product(w[1], e4m3x2_to_float2(codes[i].x >> 16), f);
+                    w[2] = add_rounded_product(w[2], e4m3x2_to_float2(codes[i].y & 0xffffu), f);
+                    w[3] = add_rounded_product(w[3], e4m3x2_to_float2(codes[i].y >> 16), f);
                 }
             }
         }

