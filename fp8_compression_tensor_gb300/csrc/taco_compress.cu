@@ -22,6 +22,10 @@
 #include "taco_device.cuh"
 #include "taco_kernels.h"
 
+#ifndef TACO_COMPRESS_MIXED_UNPACK
+#define TACO_COMPRESS_MIXED_UNPACK 1
+#endif
+
 namespace taco {
 namespace {
 
@@ -83,9 +87,16 @@ __device__ __forceinline__ float compress_rotate_whole(uint32_t slot, float2 (&v
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const int i = 4 * c + k;
+#if TACO_COMPRESS_MIXED_UNPACK
+            // Butterfly on element bit 0 straight from the bf16 pair; the
+            // energy comes from its outputs: (a+b)^2 + (a-b)^2 = 2(a^2 + b^2).
+            v[i] = bf16x2_butterfly(w[k]);
+            acc[i % 8] = fma2(v[i], v[i], acc[i % 8]);
+#else
             const float2 g = bf16x2_to_float2(w[k]);
             acc[i % 8] = fma2(g, g, acc[i % 8]);
             v[i] = make_float2(g.x + g.y, g.x - g.y);  // butterfly on element bit 0
+#endif
         }
     }
     fwht_pairs<NP>(v);
@@ -95,7 +106,11 @@ __device__ __forceinline__ float compress_rotate_whole(uint32_t slot, float2 (&v
 #pragma unroll
         for (int i = 0; i < w; i++)
             acc[i] = add2(acc[i], acc[i + w]);
+#if TACO_COMPRESS_MIXED_UNPACK
+    return (acc[0].x + acc[0].y) * 0.5f;
+#else
     return acc[0].x + acc[0].y;
+#endif
 }
 
 // Same for B = 256 with a lane pair per block: lane half h first forms
@@ -161,9 +176,9 @@ __device__ __forceinline__ void encode_pairs(const float2 (&v)[NP], float k, uin
     }
 }
 
-template <int B, int STAGES, int NOUT, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
-    compress_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ packed, int64_t nblocks,
+template <int B, int STAGES, int NOUT, int WARPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+    taco_compress_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ packed, int64_t nblocks,
                     uint32_t *__restrict__ fault)
 {
     using S = CompressShape<B>;
@@ -320,18 +335,28 @@ __global__ void __launch_bounds__(WARPS * 32)
         bulk_wait_all<0>();
 }
 
-template <int B, int STAGES, int NOUT, int WARPS>
+template <int B, int STAGES, int NOUT, int WARPS, int MINB>
 struct CompressConfig {
     static constexpr int kWarps = WARPS;
     static constexpr size_t kSmem = sizeof(CompressWarpSmem<B, STAGES, NOUT>) * WARPS;
     static constexpr int kTileBlocks = CompressShape<B>::kTileBlocks;
-    static void *fn() { return reinterpret_cast<void *>(&compress_kernel<B, STAGES, NOUT, WARPS>); }
+    static void *fn() { return reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, NOUT, WARPS, MINB>); }
 };
 
-// Tuned launch shapes (stages, output buffers, warps per CTA).
-using Compress64 = CompressConfig<64, 4, 2, 2>;
-using Compress128 = CompressConfig<128, 3, 2, 2>;
-using Compress256 = CompressConfig<256, 3, 2, 2>;
+#ifndef TACO_COMPRESS64_CFG
+#define TACO_COMPRESS64_CFG 3110
+#endif
+#ifndef TACO_COMPRESS128_CFG
+#define TACO_COMPRESS128_CFG 2110
+#endif
+#ifndef TACO_COMPRESS256_CFG
+#define TACO_COMPRESS256_CFG 2110
+#endif
+// Launch shapes, as four digits: stages, output buffers, warps per CTA, and
+// the minimum CTAs per SM given to __launch_bounds__ (0: none).
+using Compress64 = CompressConfig<64, TACO_COMPRESS64_CFG / 1000, TACO_COMPRESS64_CFG / 100 % 10, TACO_COMPRESS64_CFG / 10 % 10, TACO_COMPRESS64_CFG % 10>;
+using Compress128 = CompressConfig<128, TACO_COMPRESS128_CFG / 1000, TACO_COMPRESS128_CFG / 100 % 10, TACO_COMPRESS128_CFG / 10 % 10, TACO_COMPRESS128_CFG % 10>;
+using Compress256 = CompressConfig<256, TACO_COMPRESS256_CFG / 1000, TACO_COMPRESS256_CFG / 100 % 10, TACO_COMPRESS256_CFG / 10 % 10, TACO_COMPRESS256_CFG % 10>;
 
 template <class C>
 KernelInfo info()

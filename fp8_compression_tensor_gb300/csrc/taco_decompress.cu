@@ -79,9 +79,9 @@ __device__ __forceinline__ void load_words(const uint8_t *src_gen, uint32_t src_
     }
 }
 
-template <int B, int STAGES, int NOUT, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
-    decompress_kernel(const uint8_t *__restrict__ packed, uint16_t *__restrict__ y, int64_t nblocks,
+template <int B, int STAGES, int NOUT, int WARPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+    taco_decompress_kernel(const uint8_t *__restrict__ packed, uint16_t *__restrict__ y, int64_t nblocks,
                       uint32_t *__restrict__ fault)
 {
     using S = DecompressShape<B>;
@@ -153,10 +153,8 @@ __global__ void __launch_bounds__(WARPS * 32)
                 load_words<B / 4>(rec_g, rec_s, from_global, w);
 #pragma unroll
                 for (int j = 0; j < B / 4; j++) {
-                    const float2 q0 = e4m3x2_to_float2(w[j] & 0xffffu);
-                    const float2 q1 = e4m3x2_to_float2(w[j] >> 16);
-                    v[2 * j] = make_float2(q0.x + q0.y, q0.x - q0.y);
-                    v[2 * j + 1] = make_float2(q1.x + q1.y, q1.x - q1.y);
+                    v[2 * j] = e4m3x2_butterfly(w[j] & 0xffffu);
+                    v[2 * j + 1] = e4m3x2_butterfly(w[j] >> 16);
                 }
             } else {
                 // B = 256: half h forms c_j = q_j + (-1)^h q_{j+128} first.
@@ -227,17 +225,28 @@ __global__ void __launch_bounds__(WARPS * 32)
     bulk_wait_all<0>();
 }
 
-template <int B, int STAGES, int NOUT, int WARPS>
+template <int B, int STAGES, int NOUT, int WARPS, int MINB>
 struct DecompressConfig {
     static constexpr int kWarps = WARPS;
     static constexpr size_t kSmem = sizeof(DecompressWarpSmem<B, STAGES, NOUT>) * WARPS;
     static constexpr int kTileBlocks = DecompressShape<B>::kTileBlocks;
-    static void *fn() { return reinterpret_cast<void *>(&decompress_kernel<B, STAGES, NOUT, WARPS>); }
+    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, STAGES, NOUT, WARPS, MINB>); }
 };
 
-using Decompress64 = DecompressConfig<64, 4, 2, 2>;
-using Decompress128 = DecompressConfig<128, 3, 2, 2>;
-using Decompress256 = DecompressConfig<256, 3, 2, 2>;
+#ifndef TACO_DECOMPRESS64_CFG
+#define TACO_DECOMPRESS64_CFG 4120
+#endif
+#ifndef TACO_DECOMPRESS128_CFG
+#define TACO_DECOMPRESS128_CFG 2120
+#endif
+#ifndef TACO_DECOMPRESS256_CFG
+#define TACO_DECOMPRESS256_CFG 2110
+#endif
+// Launch shapes, as four digits: stages, output buffers, warps per CTA, and
+// the minimum CTAs per SM given to __launch_bounds__ (0: none).
+using Decompress64 = DecompressConfig<64, TACO_DECOMPRESS64_CFG / 1000, TACO_DECOMPRESS64_CFG / 100 % 10, TACO_DECOMPRESS64_CFG / 10 % 10, TACO_DECOMPRESS64_CFG % 10>;
+using Decompress128 = DecompressConfig<128, TACO_DECOMPRESS128_CFG / 1000, TACO_DECOMPRESS128_CFG / 100 % 10, TACO_DECOMPRESS128_CFG / 10 % 10, TACO_DECOMPRESS128_CFG % 10>;
+using Decompress256 = DecompressConfig<256, TACO_DECOMPRESS256_CFG / 1000, TACO_DECOMPRESS256_CFG / 100 % 10, TACO_DECOMPRESS256_CFG / 10 % 10, TACO_DECOMPRESS256_CFG % 10>;
 
 template <class C>
 KernelInfo info()

@@ -206,10 +206,59 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi)
 // Packed FP32x2 arithmetic (one instruction for two lanes of data)
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+// Add and subtract are written as PTX so that a subtraction is one packed
+// instruction (no separate negation of the operand).
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// The first butterfly on a word of two bf16 values (lo, hi): returns
+// (lo + hi, lo - hi), each rounded once.  hi is widened by masking its bits;
+// lo enters the mixed-precision add / sub directly as bf16.
+__device__ __forceinline__ float2 bf16x2_butterfly(uint32_t w)
+{
+    float s, d;
+    asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 hb;\n\tmov.b32 {l, h}, %2;\n\tand.b32 hb, %2, 0xffff0000;\n\t"
+        "add.rn.f32.bf16 %0, l, hb;\n\tsub.rn.f32.bf16 %1, l, hb;\n\t}"
+        : "=f"(s), "=f"(d)
+        : "r"(w));
+    return make_float2(s, d);
+}
+
+// Cvt_FP32 (Eq. 11) of two E4M3 codes fused with the first butterfly: returns
+// (q0 + q1, q0 - q1) for the codes in the low 16 bits of `pair` (low byte q0).
+// The codes go to f16 (exact), q1 to f32, and the mixed-precision add / sub
+// take q0 directly from its f16 half; each result is rounded once.
+__device__ __forceinline__ float2 e4m3x2_butterfly(uint32_t pair)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
+    float s, d;
+    asm("{\n\t.reg .f16 l, h;\n\t.reg .f32 hf;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 hf, h;\n\t"
+        "add.rn.f32.f16 %0, l, hf;\n\tsub.rn.f32.f16 %1, l, hf;\n\t}"
+        : "=f"(s), "=f"(d)
+        : "r"(h2));
+    return make_float2(s, d);
+}
 
 // w + a * f with the product rounded on its own before the add (scalar
 // __fmul_rn / __fadd_rn are never contracted into a fused multiply-add; the

@@ -30,7 +30,7 @@ __device__ __forceinline__ uint2 ldg_nc_u2(const uint8_t *p)
 }
 
 template <int B>
-__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs args)
+__global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const ReduceArgs args)
 {
     constexpr int LPB = B / 8;            // lanes per block
     constexpr int kRec = B + 8;
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
 template <int B>
 KernelInfo info()
 {
-    return KernelInfo{reinterpret_cast<void *>(&reduce_kernel<B>), 0, kReduceThreads, 0, kReduceThreads / 32};
+    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B>), 0, kReduceThreads, 0, kReduceThreads / 32};
 }
 
 }  // namespace
