@@ -218,6 +218,24 @@ def oracle_step_time(x_bits: np.ndarray, block: int, shards: int, threads: int) 
     return time.perf_counter() - t0
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise MAX of a list of floats over all ranks (identity on one
+    process); timings are reduced this way so that the slowest rank sets the
+    whole job's time."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_gbs(world: int, bytes_per_rank_step: float, ms_per_step: float) -> float:
+    """Aggregate GB/s over all ranks: every rank processes its own workload
+    (weak scaling) in at most the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def host_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -348,10 +366,7 @@ def run_taco(args, rank, world):
     comp = [e[0].elapsed_time(e[1]) for e in events]
     red = [e[2].elapsed_time(e[3]) for e in events]
     dec = [e[4].elapsed_time(e[5]) for e in events]
-    local = torch.tensor([sum(comp), sum(red), sum(dec)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(local, op=dist.ReduceOp.MAX)
-    tot_comp, tot_red, tot_dec = (float(v) for v in local.cpu())
+    tot_comp, tot_red, tot_dec = max_over_ranks([sum(comp), sum(red), sum(dec)], device=dev)
     K = args.steps
     ms_step = (tot_comp + tot_red + tot_dec) / K
 
@@ -380,11 +395,8 @@ def run_taco(args, rank, world):
             r_pinned.copy_(reduced, non_blocking=True)
         e1.record(stream)
         barrier()
-        t = torch.tensor([e0.elapsed_time(e1) / k_e2e], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        e2e = {"value": world * 6.0 * n / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+        ms = max_over_ranks([e0.elapsed_time(e1) / k_e2e], device=dev)[0]
+        e2e = {"value": whole_job_gbs(world, 6.0 * n, ms), "unit": UNIT, "ms_per_step": ms,
                "steps": k_e2e, "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + seg_bytes}
 
     sampler.stop()
@@ -426,7 +438,7 @@ def run_taco(args, rank, world):
 
     line = {
         "metric": METRIC,
-        "value": world * 6.0 * n / (ms_step * 1e-3) / 1e9,
+        "value": whole_job_gbs(world, 6.0 * n, ms_step),
         "unit": UNIT,
         "n_gpus": world,
         "steps": K,

@@ -221,7 +221,7 @@ taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shard
     args.nblocks = n / block;
     args.num_shards = num_shards;
     const KernelInfo ki = reduce_kernel_info(block);
-    const int64_t threads_needed = args.nblocks * (block / 8);
+    const int64_t threads_needed = args.nblocks * ki.tile_blocks;
     const int64_t ctas_needed = (threads_needed + ki.threads - 1) / ki.threads;
     const int per_sm = dev->reduce_ctas_per_sm[block_index(block)];
     const int64_t full = static_cast<int64_t>(dev->sm_count) * (per_sm > 0 ? per_sm : 1);

@@ -12,7 +12,7 @@ struct KernelInfo {
     void *fn = nullptr;     // kernel entry (for attributes and occupancy queries)
     size_t smem = 0;        // dynamic shared memory per CTA
     int threads = 0;        // threads per CTA
-    int tile_blocks = 0;    // blocks per warp tile (0 for grid-stride kernels)
+    int tile_blocks = 0;    // blocks per warp tile; for the shard reduce: threads per block
     int warps = 0;          // warps per CTA
 };
 

@@ -10,9 +10,9 @@
 // codes Cvt_FP8(Q_max W / max|W|).  The kernel computes exactly these, which
 // differ from decode-sum-encode with explicit rotations only by FP32 rounding.
 //
-// Layout.  B/8 consecutive lanes share a block; each lane owns 8 elements,
-// i.e. 8 bytes of codes per shard, read with coalesced 8-byte loads (a warp
-// reads whole records).  Energy and maximum are reduced across the block's
+// Layout.  B/16 consecutive lanes share a block; each lane owns 16 elements,
+// i.e. 16 bytes of codes per shard (two 8-byte loads: records are 8-byte
+// aligned), so a warp reads whole records.  Energy and maximum are reduced across the block's
 // lanes with xor-shuffles (every lane ends with the same bits).
 #include "taco_device.cuh"
 #include "taco_kernels.h"
@@ -21,6 +21,18 @@ namespace taco {
 namespace {
 
 constexpr int kReduceThreads = 256;
+constexpr int kLaneCodes = 16;  // codes (elements) per lane per shard
+constexpr int kBatch = 4;       // shards whose loads are issued together
+
+// 16 code bytes of a record.  Records start at multiples of B + 8 bytes,
+// which are only 8-byte aligned, so the bytes come in two 8-byte loads.
+__device__ __forceinline__ uint4 ldg_codes16(const uint8_t *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.z), "=r"(v.w) : "l"(p + 8));
+    return v;
+}
 
 __device__ __forceinline__ uint2 ldg_nc_u2(const uint8_t *p)
 {
@@ -29,10 +41,27 @@ __device__ __forceinline__ uint2 ldg_nc_u2(const uint8_t *p)
     return v;
 }
 
+// w[0..15] += q[0..15] * f for the 16 codes in `c`, each product rounded on its
+// own before the add (so that a shard and its negation cancel exactly, as in
+// an FP32 sum of decoded shards).
+__device__ __forceinline__ void accumulate_shard(float (&w)[kLaneCodes], uint4 c, float f)
+{
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const float2 q0 = e4m3x2_to_float2(words[k] & 0xffffu);
+        const float2 q1 = e4m3x2_to_float2(words[k] >> 16);
+        w[4 * k + 0] = __fadd_rn(w[4 * k + 0], __fmul_rn(q0.x, f));
+        w[4 * k + 1] = __fadd_rn(w[4 * k + 1], __fmul_rn(q0.y, f));
+        w[4 * k + 2] = __fadd_rn(w[4 * k + 2], __fmul_rn(q1.x, f));
+        w[4 * k + 3] = __fadd_rn(w[4 * k + 3], __fmul_rn(q1.y, f));
+    }
+}
+
 template <int B>
 __global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const ReduceArgs args)
 {
-    constexpr int LPB = B / 8;            // lanes per block
+    constexpr int LPB = B / kLaneCodes;   // lanes per block
     constexpr int kRec = B + 8;
     const int64_t total = args.nblocks * LPB;
     const int P = args.num_shards;
@@ -45,50 +74,48 @@ __global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const
         const int part = static_cast<int>(g % LPB);
         const int64_t off = k * kRec;
 
-        float2 w[4];
+        float w[kLaneCodes];
 #pragma unroll
-        for (int i = 0; i < 4; i++)
-            w[i] = make_float2(0.f, 0.f);
+        for (int i = 0; i < kLaneCodes; i++)
+            w[i] = 0.f;
 
-        // W = sum_p q_p * (s_p / alpha_p) in shard order, four shards' loads in flight at a time.
-        for (int p0 = 0; p0 < P; p0 += 4) {
-            uint2 codes[4], meta[4];
+        // W = sum_p q_p * (s_p / alpha_p) in shard order, the loads of up to
+        // kBatch shards in flight at a time.
+        for (int p0 = 0; p0 < P; p0 += kBatch) {
+            uint4 codes[kBatch];
+            uint2 meta[kBatch];
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
+            for (int i = 0; i < kBatch; i++) {
                 if (p0 + i < P && active) {
                     const uint8_t *rec = args.shards[p0 + i] + off;
-                    codes[i] = ldg_nc_u2(rec + 8 * part);
+                    codes[i] = ldg_codes16(rec + kLaneCodes * part);
                     meta[i] = ldg_nc_u2(rec + B);
                 } else {
-                    codes[i] = make_uint2(0u, 0u);
+                    codes[i] = make_uint4(0u, 0u, 0u, 0u);
                     meta[i] = make_uint2(0x3f800000u, 0u);  // alpha = 1, s = 0
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
+            for (int i = 0; i < kBatch; i++) {
                 if (p0 + i < P) {
-                    const float f = __fdiv_rn(__uint_as_float(meta[i].y), __uint_as_float(meta[i].x));
-                    // Each product rounded on its own, then added: a shard and
-                    // its negation cancel exactly, as in an FP32 sum of decoded
-                    // shards.
-                    w[0] = add_rounded_product(w[0], e4m3x2_to_float2(codes[i].x & 0xffffu), f);
-                    w[1] = add_rounded_product(w[1], e4m3x2_to_float2(codes[i].x >> 16), f);
-                    w[2] = add_rounded_product(w[2], e4m3x2_to_float2(codes[i].y & 0xffffu), f);
-                    w[3] = add_rounded_product(w[3], e4m3x2_to_float2(codes[i].y >> 16), f);
+                    // s_p / alpha_p (within 2 ulp; alpha_p <= 1e15 is far from
+                    // the range where the fast quotient underflows).
+                    const float f = __fdividef(__uint_as_float(meta[i].y), __uint_as_float(meta[i].x));
+                    accumulate_shard(w, codes[i], f);
                 }
             }
         }
 
         // Energy |W|^2 and max|W| over the block's lanes.
-        float2 e2 = mul2(w[0], w[0]);
-        e2 = fma2(w[1], w[1], e2);
-        e2 = fma2(w[2], w[2], e2);
-        e2 = fma2(w[3], w[3], e2);
+        float2 e2 = make_float2(0.f, 0.f);
+        float wmax = 0.f;
+#pragma unroll
+        for (int i = 0; i < kLaneCodes; i += 2) {
+            const float2 wi = make_float2(w[i], w[i + 1]);
+            e2 = fma2(wi, wi, e2);
+            wmax = max3(wmax, fabsf(w[i]), fabsf(w[i + 1]));
+        }
         float e = e2.x + e2.y;
-        float wmax = max3(fabsf(w[0].x), fabsf(w[0].y), fabsf(w[1].x));
-        wmax = max3(wmax, fabsf(w[1].y), fabsf(w[2].x));
-        wmax = max3(wmax, fabsf(w[2].y), fabsf(w[3].x));
-        wmax = fmaxf(wmax, fabsf(w[3].y));
 #pragma unroll
         for (int d = 1; d < LPB; d <<= 1) {
             e = e + __shfl_xor_sync(kFullMask, e, d);
@@ -98,19 +125,25 @@ __global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const
         const float m = e * (1.0f / B);
         const float alpha = __fdiv_rn(kTau, __fsqrt_rn(m + kEps));
         float s = 0.f;
-        uint32_t c0 = 0u, c1 = 0u;
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
         if (wmax > 0.f) {
             s = __fdiv_rn(__fmul_rn(alpha, wmax), kQmax);
             const float kq = __fdiv_rn(kQmax, wmax);
             const float2 k2 = make_float2(kq, kq);
-            const float2 u0 = mul2(w[0], k2), u1 = mul2(w[1], k2);
-            const float2 u2 = mul2(w[2], k2), u3 = mul2(w[3], k2);
-            c0 = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
-            c1 = e4m3x2_from_float2(u2.x, u2.y) | (e4m3x2_from_float2(u3.x, u3.y) << 16);
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const float2 u0 = mul2(make_float2(w[4 * j], w[4 * j + 1]), k2);
+                const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
+                o[j] = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
+            }
+            out = make_uint4(o[0], o[1], o[2], o[3]);
         }
         if (active) {
             uint8_t *rec = args.out + off;
-            *reinterpret_cast<uint2 *>(rec + 8 * part) = make_uint2(c0, c1);
+            // Records are 8-byte aligned: two 8-byte stores per lane.
+            *reinterpret_cast<uint2 *>(rec + kLaneCodes * part) = make_uint2(out.x, out.y);
+            *reinterpret_cast<uint2 *>(rec + kLaneCodes * part + 8) = make_uint2(out.z, out.w);
             if (part == 0)
                 *reinterpret_cast<uint2 *>(rec + B) = make_uint2(__float_as_uint(alpha), __float_as_uint(s));
         }
@@ -120,7 +153,8 @@ __global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const
 template <int B>
 KernelInfo info()
 {
-    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B>), 0, kReduceThreads, 0, kReduceThreads / 32};
+    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B>), 0, kReduceThreads, B / kLaneCodes,
+                      kReduceThreads / 32};
 }
 
 }  // namespace
