@@ -48,7 +48,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        p = path or LIBRARY_PATH
+        p = path or os.environ.get("TACO_GB300_LIBRARY") or LIBRARY_PATH
         if not os.path.exists(p):
             raise RuntimeError(f"{p} is missing: build it with `python -m fp8_compression_tensor_gb300.build`")
         lib = ctypes.CDLL(p)

@@ -6,7 +6,9 @@
 #include <functional>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "taco.h"
 #include "taco_kernels.h"
@@ -90,6 +92,43 @@ taco_status_t device_state(DeviceState **out)
     return TACO_OK;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_error = cudaSuccess;
+
+cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        g_encode_error = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (g_encode_error == cudaSuccess && (q != cudaDriverEntryPointSuccess || !fn))
+            g_encode_error = cudaErrorSymbolNotFound;
+        g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    *out = g_encode_tiled;
+    return g_encode_error;
+}
+
+// Tensor map of x as [nblocks, block] bf16 rows, box {64 elements, 128 rows},
+// 128-byte swizzle; rows past the end read as zeros.
+cudaError_t encode_block_rows_map(CUtensorMap *map, const void *x, int64_t nblocks, int block)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    cudaError_t e = tensor_map_encoder(&encode);
+    if (e != cudaSuccess)
+        return e;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(block), static_cast<cuuint64_t>(nblocks)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(block) * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box,
+                              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool aligned16(const void *p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -154,12 +193,18 @@ taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t hidden, in
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != TACO_OK)
         return st;
-    const KernelInfo ki = compress_kernel_info(block);
+    // Tensor-core kernel: one persistent CTA per SM over tiles of 128 blocks.
     const int64_t nblocks = n / block;
+    const KernelInfo ki = compress_kernel_info(block);
+    alignas(64) CUtensorMap map;
+    cudaError_t e = encode_block_rows_map(&map, x_bf16, nblocks, block);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
-    const int grid = persistent_grid(ntiles, ki.warps, dev->compress_ctas_per_sm[block_index(block)], dev->sm_count);
-    const cudaError_t e = launch_compress(block, x_bf16, packed_out, nblocks, dev->fault, grid,
-                                          reinterpret_cast<cudaStream_t>(stream));
+    const int per_sm = dev->compress_ctas_per_sm[block_index(block)];
+    const int64_t full = static_cast<int64_t>(dev->sm_count) * (per_sm > 0 ? per_sm : 1);
+    const int grid = static_cast<int>(ntiles < full ? ntiles : full);
+    e = launch_compress(block, &map, packed_out, nblocks, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }
 

@@ -1,390 +1,400 @@
-// taco_compress.cu -- the fused sender-side kernel of TACO (Algorithm 1, lines
-// 4-16; Eqs. 5-10) for GB300 (sm_103a): one HBM pass per tensor.
+// taco_compress.cu -- TACO's fused sender-side kernel (Algorithm 1, lines
+// 4-16; Eqs. 5-10) with the Hadamard rotation on the 5th-generation tensor
+// cores (tcgen05), for GB300 (sm_103a).
 //
-// Work decomposition.  Each warp is an independent pipeline over "tiles" of
-// 32 consecutive blocks (16 for B = 256).  For B <= 128 one lane owns one
-// whole block; for B = 256 a lane pair owns a block.  Tiles are staged in
-// shared memory by bulk (TMA) copies that complete on a per-stage mbarrier,
-// STAGES tiles ahead of the one being computed.  A lane reads its block from
-// its own padded slot (padding keeps the 16-byte reads free of bank
-// conflicts), keeps it in registers, and computes everything there:
-//   energy (Eq. 6)   sum of squares with packed FP32x2 FMAs,
-//   rotation (Eq. 8) in-register Walsh-Hadamard butterflies on FP32x2 pairs,
-//   scales (Eqs. 7, 9) and the E4M3 conversion (Eq. 10), two codes per cvt.
-// Records are written to a shared-memory staging buffer in the packed layout
-// (Section 4.4.2) and leave with one bulk store per tile.
+// The rotation of a whole tile of blocks is a dense product: with the tile's
+// 128 blocks as the rows of G (128 x B, bf16), Y = G H_B^T = G H_B (H_B is
+// symmetric) holds y_k = H_B G_k in row k.  The products G_kj * (+-1) are exact
+// and the tensor core accumulates in FP32, so Y is the unnormalised rotation
+// of Eq. (8) up to FP32 summation order.
 //
-// Arithmetic order.  The rotation is applied to the unscaled block: with
-// y = H_B G, Z = alpha y / sqrt(B) and Z / s = Q_max y / max|y| in real
-// arithmetic, so the kernel takes u = y * (Q_max / max|y|) and
-// s = alpha * max|y| * (1/sqrt B) / Q_max.  This differs from the literal
-// order only by FP32 rounding.
+// Roles in a persistent CTA (one per SM), one tile of 128 blocks at a time:
+//   warp 0  TMA producer: 2-D tiled loads (128-byte swizzle) of the tile into a
+//           ring of STAGES shared-memory stages;
+//   warp 1  allocates tensor memory and issues the B/16 tcgen05.mma of a tile
+//           (M = 128, N = B, K = B, BF16 in, FP32 out) into one of two
+//           accumulators, then commits to the stage's "empty" and the
+//           accumulator's "full" barriers;
+//   warps 2.. epilogue, one or two groups of 4 warps (group g takes every
+//           EPG-th tile, so two tiles' epilogues can overlap): each thread
+//           owns one row (one block) of the
+//           accumulator in its TMEM lane: pass 1 reads it for the energy (by
+//           Parseval, sum_j y_j^2 = B sum_j G_j^2) and the maximum, pass 2
+//           reads it again and converts y * (Q_max / max|y|) to E4M3 two
+//           codes at a time into a shared-memory record tile, which one
+//           thread writes out with a bulk store.
+// H_B is written once per CTA into shared memory in the same swizzled layout.
+//
+// Scales: m = sum y^2 / B^2 (Eq. 6), alpha = tau / sqrt(m + eps) (Eq. 7),
+// s = alpha * max|y| * (1/sqrt B) / Q_max (Eq. 9), codes of y * (Q_max / max|y|)
+// (Eq. 10, alpha cancels); equal to the literal order up to FP32 rounding.
+#include <cstring>
+
+#include <cuda.h>
+
 #include "taco_device.cuh"
 #include "taco_kernels.h"
-
-#ifndef TACO_COMPRESS_MIXED_UNPACK
-#define TACO_COMPRESS_MIXED_UNPACK 1
-#endif
+#include "taco_tcgen05.cuh"
 
 namespace taco {
 namespace {
 
-template <int B>
-struct CompressShape {
-    static constexpr int kLanesPerBlock = (B <= 128) ? 1 : 2;
-    static constexpr int kTileBlocks = 32 / kLanesPerBlock;        // blocks per warp tile
-    static constexpr int kLaneElems = B / kLanesPerBlock;          // elements a lane owns
-    static constexpr int kPairs = kLaneElems / 2;                  // FP32x2 registers a lane owns
-    static constexpr int kSlotBytes = 2 * B + 16;                  // padded input slot per block
-    static constexpr int kRecBytes = B + 8;                        // packed record
-    static constexpr int kInTileBytes = kTileBlocks * kSlotBytes;
-    static constexpr int kOutTileBytes = kTileBlocks * kRecBytes;  // multiple of 16
+constexpr uint32_t kMmaNegateA = 1u << 13;   // instruction-descriptor bit: negate A
+
+constexpr int kTcRows = 128;       // blocks per tile = MMA M = TMEM lanes
+constexpr int kEpiThreads = 128;   // threads of one epilogue group (4 warps, one per TMEM lane quarter)
+
+__host__ __device__ constexpr int tc_threads(int groups) { return 64 + kEpiThreads * groups; }
+
+// B: block size; STAGES: A tiles in flight; EPG: epilogue groups (group g
+// takes the tiles i with i % EPG == g, so EPG = 2 overlaps two tiles'
+// epilogues); NBG: record-tile buffers per group.
+template <int B, int STAGES, int EPG, int NBG>
+struct TcCompressLayout {
+    static constexpr int NOUT = EPG * NBG;                         // record-tile buffers
+    static constexpr int kN = B <= 128 ? B : 128;                  // MMA N = order of the Hadamard matrix used
+    static constexpr int kHalves = B / kN;                         // 2 for B = 256 (Kronecker split)
+    static constexpr int kKSteps = kN / 16;                        // MMAs (K = 16) per product with H_N
+    static constexpr int kChunks = B / 64;                         // 128-byte K chunks of a row
+    static constexpr int kChunkBytesA = kTcRows * 128;             // one chunk of the A tile
+    static constexpr int kStageBytes = kTcRows * B * 2;            // one A tile
+    static constexpr int kChunkBytesH = kN * 128;                  // one chunk of H_N
+    static constexpr int kHBytes = kN * kN * 2;
+    static constexpr int kRec = B + 8;
+    static constexpr int kOutBytes = kTcRows * kRec;               // one record tile (multiple of 16)
+    static constexpr int kTmemCols = 2 * B;                        // two accumulators of B columns
+    // Offsets from the 1024-byte aligned base.
+    static constexpr int kOffA = 0;
+    static constexpr int kOffH = kOffA + STAGES * kStageBytes;
+    static constexpr int kOffOut = kOffH + kHBytes;
+    static constexpr int kOffBar = kOffOut + NOUT * kOutBytes;     // 8-byte aligned
+    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * NOUT;
+    static constexpr int kOffTmem = kOffBar + 8 * kNumBars;
+    static constexpr int kBytes = kOffTmem + 16;
+    static constexpr int kSmem = kBytes + 1024;                    // slack for 1024-byte alignment
 };
 
-template <int B, int STAGES, int NOUT>
-struct CompressWarpSmem {
-    using S = CompressShape<B>;
-    alignas(16) uint8_t in[STAGES][S::kInTileBytes];
-    alignas(16) uint8_t out[NOUT][S::kOutTileBytes];
-    alignas(8) uint64_t bar[STAGES];
-};
-
-// Issues the bulk loads of one tile into stage `stage` (every lane calls it).
+// Writes H_B (+-1 in bf16, Sylvester order) into shared memory as the K-major
+// B operand in the 128-byte swizzled layout: chunk c holds columns
+// [64c, 64c+64); row n of a chunk is 128 bytes whose 16-byte unit u sits at
+// unit u ^ (n % 8).
 template <int B>
-__device__ __forceinline__ void compress_issue_tile(const uint16_t *__restrict__ x, int64_t nblocks, int64_t tile,
-                                                    uint32_t in_stage, uint32_t bar, int lane)
+__device__ void write_hadamard_sw128(uint8_t *h)
 {
-    using S = CompressShape<B>;
-    const int64_t blk0 = tile * S::kTileBlocks;
-    const int nvalid = static_cast<int>(nblocks - blk0 < S::kTileBlocks ? nblocks - blk0 : S::kTileBlocks);
-    if (lane == 0)
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvalid) * 2u * B);
-    __syncwarp();
-    // Lane `lane` copies bytes [part*2B/L, (part+1)*2B/L) of block lane/L.
-    const int blk = lane / S::kLanesPerBlock;
-    const int part = lane % S::kLanesPerBlock;
-    if (blk < nvalid) {
-        constexpr uint32_t kPartBytes = 2u * B / S::kLanesPerBlock;
-        const uint16_t *src = x + (blk0 + blk) * B + part * (B / S::kLanesPerBlock);
-        bulk_load(in_stage + blk * S::kSlotBytes + part * kPartBytes, src, kPartBytes, bar);
-    }
-}
-
-// Energy partial sums and FWHT of a lane's data for B <= 128: the lane holds
-// the whole block.  v[i] ends as (y[2i], y[2i+1]).
-template <int B>
-__device__ __forceinline__ float compress_rotate_whole(uint32_t slot, float2 (&v)[B / 2])
-{
-    constexpr int NP = B / 2;
-    float2 acc[8];
+    constexpr int kUnits = B * (B / 8);    // 16-byte units of H
+    for (int idx = threadIdx.x; idx < kUnits; idx += blockDim.x) {
+        const int n = idx / (B / 8);
+        const int u_all = idx % (B / 8);   // unit index along K over the whole row
+        const int c = u_all / 8, u = u_all % 8;
+        uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 8; i++)
-        acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < B / 8; c++) {
-        const uint4 raw = lds128(slot + 16 * c);
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int i = 4 * c + k;
-#if TACO_COMPRESS_MIXED_UNPACK
-            // Butterfly on element bit 0 straight from the bf16 pair; the
-            // energy comes from its outputs: (a+b)^2 + (a-b)^2 = 2(a^2 + b^2).
-            v[i] = bf16x2_butterfly(w[k]);
-            acc[i % 8] = fma2(v[i], v[i], acc[i % 8]);
-#else
-            const float2 g = bf16x2_to_float2(w[k]);
-            acc[i % 8] = fma2(g, g, acc[i % 8]);
-            v[i] = make_float2(g.x + g.y, g.x - g.y);  // butterfly on element bit 0
-#endif
+        for (int q = 0; q < 4; q++) {
+            const int k0 = 8 * u_all + 2 * q;
+            const uint32_t lo = (__popc(n & k0) & 1) ? 0xBF80u : 0x3F80u;
+            const uint32_t hi = (__popc(n & (k0 + 1)) & 1) ? 0xBF80u : 0x3F80u;
+            w[q] = lo | (hi << 16);
         }
-    }
-    fwht_pairs<NP>(v);
-    // Tree-sum the 16 partial sums.
-#pragma unroll
-    for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; i++)
-            acc[i] = add2(acc[i], acc[i + w]);
-#if TACO_COMPRESS_MIXED_UNPACK
-    return (acc[0].x + acc[0].y) * 0.5f;
-#else
-    return acc[0].x + acc[0].y;
-#endif
-}
-
-// Same for B = 256 with a lane pair per block: lane half h first forms
-// c_j = G_j + (-1)^h G_{j+128} (the butterfly on element bit 7), then runs the
-// remaining seven stages on its 128 values, which become y[128h .. 128h+127].
-// Returns the sum of squares of the lane's own half of G.
-__device__ __forceinline__ float compress_rotate_half256(uint32_t slot, int h, float2 (&v)[64])
-{
-    float2 acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++)
-        acc[i] = make_float2(0.f, 0.f);
-    const float sg = h ? -1.f : 1.f;
-    const float2 sgn = make_float2(sg, sg);
-#pragma unroll
-    for (int c = 0; c < 16; c++) {
-        const uint4 ra = lds128(slot + 16 * c);        // elements 8c .. 8c+7
-        const uint4 rb = lds128(slot + 256 + 16 * c);  // elements 128+8c .. 128+8c+7
-        const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
-        const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int i = 4 * c + k;
-            const float2 a = bf16x2_to_float2(wa[k]);
-            const float2 b = bf16x2_to_float2(wb[k]);
-            const float2 own = h ? b : a;
-            acc[i % 8] = fma2(own, own, acc[i % 8]);
-            const float2 cc = fma2(b, sgn, a);          // a + b or a - b, one rounding
-            v[i] = make_float2(cc.x + cc.y, cc.x - cc.y);
-        }
-    }
-    fwht_pairs<64>(v);
-#pragma unroll
-    for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; i++)
-            acc[i] = add2(acc[i], acc[i + w]);
-    return acc[0].x + acc[0].y;
-}
-
-template <int NP>
-__device__ __forceinline__ float abs_max(const float2 (&v)[NP])
-{
-    float m0 = 0.f, m1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < NP; i += 2) {
-        m0 = max3(m0, fabsf(v[i].x), fabsf(v[i].y));
-        m1 = max3(m1, fabsf(v[i + 1].x), fabsf(v[i + 1].y));
-    }
-    return fmaxf(m0, m1);
-}
-
-// Encodes a lane's NP pairs to E4M3 (u = y * k) into NP/2 words.
-template <int NP>
-__device__ __forceinline__ void encode_pairs(const float2 (&v)[NP], float k, uint32_t (&cw)[NP / 2])
-{
-    const float2 k2 = make_float2(k, k);
-#pragma unroll
-    for (int i = 0; i < NP; i += 2) {
-        const float2 u0 = mul2(v[i], k2);
-        const float2 u1 = mul2(v[i + 1], k2);
-        cw[i / 2] = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
+        uint8_t *dst = h + c * (B * 128) + n * 128 + ((u ^ (n & 7)) * 16);
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-template <int B, int STAGES, int NOUT, int WARPS, int MINB>
-__global__ void __launch_bounds__(WARPS * 32, MINB)
-    taco_compress_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ packed, int64_t nblocks,
-                    uint32_t *__restrict__ fault)
+template <int B, int STAGES, int EPG, int NBG>
+__global__ void __launch_bounds__(tc_threads(EPG), 1)
+    taco_compress_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, uint8_t *__restrict__ packed,
+                            int64_t nblocks, uint32_t *__restrict__ fault)
 {
-    using S = CompressShape<B>;
-    using Smem = CompressWarpSmem<B, STAGES, NOUT>;
-    constexpr int L = S::kLanesPerBlock;
-    constexpr int NP = S::kPairs;
+    using Lay = TcCompressLayout<B, STAGES, EPG, NBG>;
+    constexpr int NOUT = Lay::NOUT;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(base);
+    const uint32_t bar0 = sbase + Lay::kOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto acc_full_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto acc_empty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    auto out_free_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
+    auto rec_done_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + NOUT + b); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
-    extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    Smem &sm = reinterpret_cast<Smem *>(smem_raw)[warp];
+    const int64_t ntiles = (nblocks + kTcRows - 1) / kTcRows;
 
-    const int64_t ntiles = (nblocks + S::kTileBlocks - 1) / S::kTileBlocks;
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * WARPS;
-    if (first >= ntiles)
-        return;
-
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < STAGES; s++)
-            mbar_init(smem_addr(&sm.bar[s]), 1);
+    // ---- set-up ----------------------------------------------------------
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(acc_full_bar(a), 1);
+            mbar_init(acc_empty_bar(a), kEpiThreads / 32);   // the 4 warps of the group reading it
+        }
+        for (int b = 0; b < NOUT; b++) {
+            mbar_init(out_free_bar(b), 1);
+            mbar_init(rec_done_bar(b), kEpiThreads);
+        }
         fence_mbar_init();
+        prefetch_tmap(&tmap_x);
     }
-    __syncwarp();
+    if (warp == 1)
+        tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
+    write_hadamard_sw128<Lay::kN>(base + Lay::kOffH);
+    fence_proxy_async_smem();   // H is read by the tensor core (async proxy)
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
 
+    if (warp == 0) {
+        // ---- TMA producer ------------------------------------------------
+        if (lane == 0) {
+            int i = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+                const int s = i % STAGES;
+                if (i >= STAGES &&
+                    !mbar_wait_bounded_thread(empty_bar(s), ((i / STAGES) - 1) & 1, fault, kFaultCompress))
+                    break;
+                mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
+                const uint32_t dst = sbase + Lay::kOffA + s * Lay::kStageBytes;
 #pragma unroll
-    for (int s = 0; s < STAGES; s++) {
-        const int64_t t = first + s * stride;
-        if (t < ntiles)
-            compress_issue_tile<B>(x, nblocks, t, smem_addr(sm.in[s]), smem_addr(&sm.bar[s]), lane);
-    }
-
-    const int blk = lane / L;   // block of the tile this lane works on
-    const int h = lane % L;     // which half (B = 256)
-    const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
-
-    int iter = 0;
-    bool healthy = true;
-    for (int64_t t = first; t < ntiles; t += stride, iter++) {
-        const int stage = iter % STAGES;
-        const uint32_t bar = smem_addr(&sm.bar[stage]);
-        if (!mbar_wait_bounded(bar, (iter / STAGES) & 1, fault, kFaultCompress)) {
-            healthy = false;
-            break;
+                for (int c = 0; c < Lay::kChunks; c++)
+                    tma_load_2d(dst + c * Lay::kChunkBytesA, &tmap_x, 64 * c, static_cast<int32_t>(t * kTcRows),
+                                full_bar(s));
+            }
+            // Copies this thread issued must land before the CTA can exit:
+            // the consumer waited on every full barrier unless it stopped early.
+            const int issued = i;
+            for (int j = issued - STAGES > 0 ? issued - STAGES : 0; j < issued; j++)
+                mbar_wait_bounded_thread(full_bar(j % STAGES), (j / STAGES) & 1, fault, kFaultCompress);
         }
-        const int64_t blk0 = t * S::kTileBlocks;
-        const int nvalid = static_cast<int>(nblocks - blk0 < S::kTileBlocks ? nblocks - blk0 : S::kTileBlocks);
-        const bool active = blk < nvalid;
-
-        // Load the block into registers, rotate it, and take its energy.
-        float2 v[NP];
-        float sumsq = 0.f;
-        const uint32_t slot = smem_addr(sm.in[stage]) + blk * S::kSlotBytes;
-        if (active) {
-            if constexpr (L == 1)
-                sumsq = compress_rotate_whole<B>(slot, v);
-            else
-                sumsq = compress_rotate_half256(slot, h, v);
-        }
-
-        // The stage's slots are consumed: refill them with tile t + STAGES*stride.
-        fence_proxy_async_smem();
-        __syncwarp();
-        {
-            const int64_t tn = t + STAGES * stride;
-            if (tn < ntiles)
-                compress_issue_tile<B>(x, nblocks, tn, smem_addr(sm.in[stage]), bar, lane);
-        }
-
-        // Scales (Eqs. 6, 7, 9) and codes (Eq. 10).
-        float ymax = active ? abs_max<NP>(v) : 0.f;
-        if constexpr (L == 2) {
-            sumsq = sumsq + __shfl_xor_sync(kFullMask, sumsq, 1);
-            ymax = fmaxf(ymax, __shfl_xor_sync(kFullMask, ymax, 1));
-        }
-        const float m = sumsq * (1.0f / B);
-        const float sigma = __fsqrt_rn(m + kEps);
-        const float alpha = __fdiv_rn(kTau, sigma);
-        float s = 0.f, k = 0.f;
-        if (ymax > 0.f) {
-            s = __fdiv_rn(__fmul_rn(__fmul_rn(alpha, ymax), rB), kQmax);
-            k = __fdiv_rn(kQmax, ymax);
-        }
-        uint32_t cw[NP / 2];
-        if (ymax > 0.f) {
-            encode_pairs<NP>(v, k, cw);
-        } else {
+    } else if (warp == 1) {
+        // ---- MMA issuer --------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = mma_idesc_bf16_f32(kTcRows, Lay::kN);
+            const uint32_t a0 = sbase + Lay::kOffA, h0 = sbase + Lay::kOffH;
+            int i = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+                const int s = i % STAGES, acc = i & 1;
+                if (i >= 2 && !mbar_wait_bounded_thread(acc_empty_bar(acc), ((i >> 1) - 1) & 1, fault,
+                                                        kFaultCompress))
+                    break;
+                if (!mbar_wait_bounded_thread(full_bar(s), (i / STAGES) & 1, fault, kFaultCompress))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * B);
+                const uint32_t a_stage = a0 + s * Lay::kStageBytes;
+                if constexpr (Lay::kHalves == 1) {
 #pragma unroll
-            for (int i = 0; i < NP / 2; i++)
-                cw[i] = 0u;
+                    for (int kk = 0; kk < Lay::kKSteps; kk++) {
+                        const uint32_t koff = (kk & 3) * 32;   // 16 bf16 = 32 bytes along K
+                        const uint64_t ad = sw128_kmajor_desc(a_stage + (kk >> 2) * Lay::kChunkBytesA + koff);
+                        const uint64_t bd = sw128_kmajor_desc(h0 + (kk >> 2) * Lay::kChunkBytesH + koff);
+                        tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    }
+                } else {
+                    // B = 256 with H_256 = [[H, H], [H, -H]] (H = H_128): the
+                    // columns [0, 128) get H g0 + H g1 and [128, 256) get
+                    // H g0 - H g1, where g0 / g1 are the block's two halves
+                    // (A chunks 0-1 / 2-3); the minus is the negate-A bit.
+#pragma unroll
+                    for (int out_half = 0; out_half < 2; out_half++) {
+#pragma unroll
+                        for (int in_half = 0; in_half < 2; in_half++) {
+                            const uint32_t id = (out_half == 1 && in_half == 1) ? (idesc | kMmaNegateA) : idesc;
+#pragma unroll
+                            for (int kk = 0; kk < Lay::kKSteps; kk++) {
+                                const uint32_t koff = (kk & 3) * 32;
+                                const uint64_t ad = sw128_kmajor_desc(
+                                    a_stage + (2 * in_half + (kk >> 2)) * Lay::kChunkBytesA + koff);
+                                const uint64_t bd = sw128_kmajor_desc(h0 + (kk >> 2) * Lay::kChunkBytesH + koff);
+                                tc_mma_bf16(d + out_half * 128, ad, bd, id, (in_half == 0 && kk == 0) ? 0u : 1u);
+                            }
+                        }
+                    }
+                }
+                tc_commit(empty_bar(s));
+                tc_commit(acc_full_bar(acc));
+            }
+            // All MMAs issued must finish before tensor memory is freed.
+            if (i > 0)
+                mbar_wait_bounded_thread(acc_full_bar((i - 1) & 1), ((i - 1) >> 1) & 1, fault, kFaultCompress);
         }
+    } else {
+        // ---- epilogue (warps 2 .. 2+4*EPG-1) --------------------------------
+        const int grp = (warp - 2) / 4;                 // epilogue group
+        const int et = threadIdx.x - 64 - kEpiThreads * grp;   // 0..127 within the group
+        const int q = warp & 3;                         // TMEM lane quarter of this warp
+        const int row = 32 * q + lane;                  // accumulator row = block within the tile
+        const bool store_warp = ((warp - 2) & 3) == 0;  // first warp of the group issues the stores
+        const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
+        int kt = 0;   // tiles this group has handled
+        for (int64_t t = blockIdx.x + static_cast<int64_t>(grp) * gridDim.x; t < ntiles;
+             t += static_cast<int64_t>(EPG) * gridDim.x, kt++) {
+            const int i = EPG * kt + grp;               // the CTA's tile counter
+            const int acc = i & 1;
+            if (!mbar_wait_bounded(acc_full_bar(acc), (i >> 1) & 1, fault, kFaultCompress))
+                break;
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * B);
 
-        // Stage the record in shared memory (the previous store from this
-        // buffer must have finished reading it).
-        const int ob = iter % NOUT;
-        if (lane == 0)
-            bulk_wait_read<NOUT - 1>();
-        __syncwarp();
-        const uint32_t rec = smem_addr(sm.out[ob]) + blk * S::kRecBytes;
-        if (active) {
-            if constexpr (L == 1) {
+            // Pass 1: energy (Parseval) and max|y|.
+            float2 e2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+            float ymax = 0.f;
 #pragma unroll
-                for (int j = 0; j < NP / 4; j++)
-                    sts64(rec + 8 * j, cw[2 * j], cw[2 * j + 1]);
-            } else {
-                // Half h writes codes [128h, 128h+128); the second half of the
-                // pair writes its chunks in a rotated order (chunk j+8 at step
-                // j) so that the two halves hit different banks.
+            for (int c = 0; c < B / 32; c++) {
+                uint32_t r[32];
+                tmem_ld32(taddr + 32 * c, r);
+                tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const int jr = (j + 8) & 15;
-                    const uint32_t a = h ? cw[2 * jr] : cw[2 * j];
-                    const uint32_t b = h ? cw[2 * jr + 1] : cw[2 * j + 1];
-                    sts64(rec + (h ? 128 + 8 * jr : 8 * j), a, b);
+                for (int j = 0; j < 32; j += 2) {
+                    const float2 y = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                    e2[(j >> 1) & 3] = fma2(y, y, e2[(j >> 1) & 3]);
+                    ymax = max3(ymax, fabsf(y.x), fabsf(y.y));
                 }
             }
-            if (h == 0)
-                sts64(rec + B, __float_as_uint(alpha), __float_as_uint(s));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
+            const float2 e01 = add2(e2[0], e2[1]), e23 = add2(e2[2], e2[3]);
+            const float2 ee = add2(e01, e23);
+            const float m = (ee.x + ee.y) * (1.0f / (static_cast<float>(B) * B));
+            const float alpha = __fdiv_rn(kTau, __fsqrt_rn(m + kEps));
+            float s = 0.f, k = 0.f;
+            if (ymax > 0.f) {
+                s = __fdiv_rn(__fmul_rn(__fmul_rn(alpha, ymax), rB), kQmax);
+                k = __fdiv_rn(kQmax, ymax);
+            }
 
-        // Write the tile's records: one bulk store for an even count; an odd
-        // last record goes out with plain stores.
-        const int neven = nvalid & ~1;
-        if (lane == 0 && neven > 0) {
-            bulk_store(packed + blk0 * S::kRecBytes, smem_addr(sm.out[ob]), neven * S::kRecBytes);
-            bulk_commit();
+            // The group's record tile buffer used NBG tiles ago must have been read
+            // by its bulk store before it is overwritten: thread 0 (which
+            // issued that store) confirms it on out_free, the others wait.
+            const int ob = grp * NBG + (kt % NBG);
+            if (kt >= NBG) {
+                if (et == 0) {
+                    bulk_wait_read<NBG - 1>();
+                    mbar_arrive(out_free_bar(ob));
+                }
+                if (!mbar_wait_bounded(out_free_bar(ob), ((kt / NBG) - 1) & 1, fault, kFaultCompress))
+                    break;
+            }
+            const uint32_t rec = sbase + Lay::kOffOut + ob * Lay::kOutBytes + row * Lay::kRec;
+
+            // Pass 2: codes (Eq. 10) two per cvt, 32 per chunk.
+            const float2 k2 = make_float2(k, k);
+#pragma unroll
+            for (int c = 0; c < B / 32; c++) {
+                uint32_t r[32];
+                tmem_ld32(taddr + 32 * c, r);
+                tmem_ld_wait();
+                uint32_t cw[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float2 u0 = mul2(make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), k2);
+                    const float2 u1 =
+                        mul2(make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), k2);
+                    cw[j] = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
+                }
+                if (!(ymax > 0.f)) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        cw[j] = 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    sts64(rec + 32 * c + 8 * j, cw[2 * j], cw[2 * j + 1]);
+            }
+            // The accumulator is read: hand it back to the MMA warp.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acc_empty_bar(acc));
+
+            sts64(rec + B, __float_as_uint(alpha), __float_as_uint(s));
+            fence_proxy_async_smem();
+            mbar_arrive(rec_done_bar(ob));
+
+            // The group's first warp (lane 0) stores the tile's records once all 128 are written.
+            const int64_t blk0 = t * kTcRows;
+            const int nvalid = static_cast<int>(nblocks - blk0 < kTcRows ? nblocks - blk0 : kTcRows);
+            const int neven = nvalid & ~1;
+            if (store_warp) {
+                if (!mbar_wait_bounded(rec_done_bar(ob), (kt / NBG) & 1, fault, kFaultCompress))
+                    break;
+                if (lane == 0 && neven > 0) {
+                    bulk_store(packed + blk0 * Lay::kRec, sbase + Lay::kOffOut + ob * Lay::kOutBytes,
+                               static_cast<uint32_t>(neven * Lay::kRec));
+                    bulk_commit();
+                }
+            }
+            if ((nvalid & 1) && row == nvalid - 1) {
+                uint8_t *dst = packed + (blk0 + row) * Lay::kRec;
+                const uint8_t *src = base + Lay::kOffOut + ob * Lay::kOutBytes + row * Lay::kRec;
+                for (int o = 0; o < Lay::kRec; o += 8)
+                    *reinterpret_cast<uint2 *>(dst + o) = *reinterpret_cast<const uint2 *>(src + o);
+            }
         }
-        if ((nvalid & 1) && blk == nvalid - 1) {
-            uint8_t *dst = packed + (blk0 + blk) * S::kRecBytes;
-            const uint8_t *src = sm.out[ob] + blk * S::kRecBytes;
-            for (int o = h * 8; o < S::kRecBytes; o += 8 * L)
-                *reinterpret_cast<uint2 *>(dst + o) = *reinterpret_cast<const uint2 *>(src + o);
-        }
+        if (et == 0)
+            bulk_wait_all<0>();
     }
 
-    if (!healthy) {
-        // Let copies still in flight land before the CTA's shared memory is
-        // released: for each stage, wait (bounded) for the last tile issued
-        // into it.  Tile i of this warp went to stage i % STAGES as phase
-        // i / STAGES; tiles i < iter + STAGES were issued.
-        for (int s = 0; s < STAGES; s++) {
-            int64_t i = s + static_cast<int64_t>((iter + STAGES - 1 - s) / STAGES) * STAGES;
-            while (i >= 0 && first + i * stride >= ntiles)
-                i -= STAGES;
-            if (i >= 0)
-                mbar_wait_bounded(smem_addr(&sm.bar[s]), static_cast<uint32_t>(i / STAGES) & 1u, fault,
-                                  kFaultCompress);
-        }
+    // ---- tear-down -------------------------------------------------------
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Lay::kTmemCols);
     }
-    if (lane == 0)
-        bulk_wait_all<0>();
 }
 
-template <int B, int STAGES, int NOUT, int WARPS, int MINB>
-struct CompressConfig {
-    static constexpr int kWarps = WARPS;
-    static constexpr size_t kSmem = sizeof(CompressWarpSmem<B, STAGES, NOUT>) * WARPS;
-    static constexpr int kTileBlocks = CompressShape<B>::kTileBlocks;
-    static void *fn() { return reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, NOUT, WARPS, MINB>); }
+template <int B, int STAGES, int EPG, int NBG>
+struct TcCompressConfig {
+    using Lay = TcCompressLayout<B, STAGES, EPG, NBG>;
+    static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
+    static void *fn() { return reinterpret_cast<void *>(&taco_compress_tc_kernel<B, STAGES, EPG, NBG>); }
+    static KernelInfo info()
+    {
+        return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), kTcRows, 0};
+    }
 };
 
-#ifndef TACO_COMPRESS64_CFG
-#define TACO_COMPRESS64_CFG 3110
+#ifndef TACO_TC64_CFG
+#define TACO_TC64_CFG 821
 #endif
-#ifndef TACO_COMPRESS128_CFG
-#define TACO_COMPRESS128_CFG 2110
+#ifndef TACO_TC128_CFG
+#define TACO_TC128_CFG 421
 #endif
-#ifndef TACO_COMPRESS256_CFG
-#define TACO_COMPRESS256_CFG 2110
+#ifndef TACO_TC256_CFG
+#define TACO_TC256_CFG 211
 #endif
-// Launch shapes, as four digits: stages, output buffers, warps per CTA, and
-// the minimum CTAs per SM given to __launch_bounds__ (0: none).
-using Compress64 = CompressConfig<64, TACO_COMPRESS64_CFG / 1000, TACO_COMPRESS64_CFG / 100 % 10, TACO_COMPRESS64_CFG / 10 % 10, TACO_COMPRESS64_CFG % 10>;
-using Compress128 = CompressConfig<128, TACO_COMPRESS128_CFG / 1000, TACO_COMPRESS128_CFG / 100 % 10, TACO_COMPRESS128_CFG / 10 % 10, TACO_COMPRESS128_CFG % 10>;
-using Compress256 = CompressConfig<256, TACO_COMPRESS256_CFG / 1000, TACO_COMPRESS256_CFG / 100 % 10, TACO_COMPRESS256_CFG / 10 % 10, TACO_COMPRESS256_CFG % 10>;
-
-template <class C>
-KernelInfo info()
-{
-    return KernelInfo{C::fn(), C::kSmem, C::kWarps * 32, C::kTileBlocks, C::kWarps};
-}
+// Per block size, three digits: A stages, epilogue groups, buffers per group.
+using CompressTc64 = TcCompressConfig<64, TACO_TC64_CFG / 100, TACO_TC64_CFG / 10 % 10, TACO_TC64_CFG % 10>;
+using CompressTc128 = TcCompressConfig<128, TACO_TC128_CFG / 100, TACO_TC128_CFG / 10 % 10, TACO_TC128_CFG % 10>;
+using CompressTc256 = TcCompressConfig<256, TACO_TC256_CFG / 100, TACO_TC256_CFG / 10 % 10, TACO_TC256_CFG % 10>;
 
 }  // namespace
 
 KernelInfo compress_kernel_info(int block)
 {
     switch (block) {
-    case 64: return info<Compress64>();
-    case 128: return info<Compress128>();
-    case 256: return info<Compress256>();
+    case 64: return CompressTc64::info();
+    case 128: return CompressTc128::info();
+    case 256: return CompressTc256::info();
     default: return KernelInfo{};
     }
 }
 
-cudaError_t launch_compress(int block, const void *x, void *packed, int64_t nblocks, uint32_t *fault, int grid,
+cudaError_t launch_compress(int block, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault, int grid,
                             cudaStream_t stream)
 {
     const KernelInfo ki = compress_kernel_info(block);
     if (!ki.fn)
         return cudaErrorInvalidValue;
-    const uint16_t *xp = static_cast<const uint16_t *>(x);
+    CUtensorMap map;
+    memcpy(&map, tmap, sizeof map);
     uint8_t *pp = static_cast<uint8_t *>(packed);
-    void *args[] = {&xp, &pp, &nblocks, &fault};
+    void *args[] = {&map, &pp, &nblocks, &fault};
     return cudaLaunchKernel(ki.fn, dim3(grid), dim3(ki.threads), args, ki.smem, stream);
 }
 

@@ -134,15 +134,6 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
 __device__ __forceinline__ uint2 lds64(uint32_t addr)
 {
     uint2 v;
@@ -165,12 +156,6 @@ __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b)
 // ---------------------------------------------------------------------------
 // Number formats
 // ---------------------------------------------------------------------------
-
-// The two bf16 values packed in a 32-bit word, as floats (exact).
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
-{
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
 
 // Cvt_FP8 (Eq. 10) of two floats: round to nearest even, saturate to +-448.
 // Returns 16 bits: `lo` in the low byte, `hi` in the high byte.
@@ -231,19 +216,6 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b)
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// The first butterfly on a word of two bf16 values (lo, hi): returns
-// (lo + hi, lo - hi), each rounded once.  hi is widened by masking its bits;
-// lo enters the mixed-precision add / sub directly as bf16.
-__device__ __forceinline__ float2 bf16x2_butterfly(uint32_t w)
-{
-    float s, d;
-    asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 hb;\n\tmov.b32 {l, h}, %2;\n\tand.b32 hb, %2, 0xffff0000;\n\t"
-        "add.rn.f32.bf16 %0, l, hb;\n\tsub.rn.f32.bf16 %1, l, hb;\n\t}"
-        : "=f"(s), "=f"(d)
-        : "r"(w));
-    return make_float2(s, d);
-}
-
 // Cvt_FP32 (Eq. 11) of two E4M3 codes fused with the first butterfly: returns
 // (q0 + q1, q0 - q1) for the codes in the low 16 bits of `pair` (low byte q0).
 // The codes go to f16 (exact), q1 to f32, and the mixed-precision add / sub
@@ -258,15 +230,6 @@ __device__ __forceinline__ float2 e4m3x2_butterfly(uint32_t pair)
         : "=f"(s), "=f"(d)
         : "r"(h2));
     return make_float2(s, d);
-}
-
-// w + a * f with the product rounded on its own before the add (scalar
-// __fmul_rn / __fadd_rn are never contracted into a fused multiply-add; the
-// packed FP32x2 forms can be).  Used where a sum of products must behave like a
-// sum of separately rounded terms, e.g. so that x*f + (-x)*f is exactly 0.
-__device__ __forceinline__ float2 add_rounded_product(float2 w, float2 a, float f)
-{
-    return make_float2(__fadd_rn(w.x, __fmul_rn(a.x, f)), __fadd_rn(w.y, __fmul_rn(a.y, f)));
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c)

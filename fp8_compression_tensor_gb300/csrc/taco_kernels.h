@@ -20,7 +20,9 @@ KernelInfo compress_kernel_info(int block);
 KernelInfo decompress_kernel_info(int block);
 KernelInfo reduce_kernel_info(int block);
 
-cudaError_t launch_compress(int block, const void *x, void *packed, int64_t nblocks, uint32_t *fault, int grid,
+// `tmap` points to a CUtensorMap of x viewed as [nblocks, block] bf16, box
+// {64, 128}, 128-byte swizzle.
+cudaError_t launch_compress(int block, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault, int grid,
                             cudaStream_t stream);
 cudaError_t launch_decompress(int block, const void *packed, void *y, int64_t nblocks, uint32_t *fault, int grid,
                               cudaStream_t stream);
