@@ -111,9 +111,10 @@ cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
     return g_encode_error;
 }
 
-// Tensor map of x as [nblocks, block] bf16 rows, box {64 elements, 128 rows},
-// 128-byte swizzle; rows past the end read as zeros.
-cudaError_t encode_block_rows_map(CUtensorMap *map, const void *x, int64_t nblocks, int block)
+// Tensor map of a bf16 tensor as [nblocks, block] rows, box {64 elements,
+// box_rows rows}, 128-byte swizzle; loads past the end read zeros, stores past
+// the end are dropped.
+cudaError_t encode_block_rows_map(CUtensorMap *map, const void *x, int64_t nblocks, int block, int box_rows = 128)
 {
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     cudaError_t e = tensor_map_encoder(&encode);
@@ -121,7 +122,7 @@ cudaError_t encode_block_rows_map(CUtensorMap *map, const void *x, int64_t nbloc
         return e;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(block), static_cast<cuuint64_t>(nblocks)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(block) * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t elem_strides[2] = {1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box,
                               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -152,14 +153,6 @@ taco_status_t check_shape(int64_t rows, int64_t hidden, int block, int64_t *n, i
     *n = rows * hidden;
     *packed_bytes = *n / block * (block + 8);
     return TACO_OK;
-}
-
-// Persistent grid: enough CTAs to fill every SM, no more than the work needs.
-int persistent_grid(int64_t ntiles, int warps_per_cta, int ctas_per_sm, int sm_count)
-{
-    const int64_t needed = (ntiles + warps_per_cta - 1) / warps_per_cta;
-    int64_t full = static_cast<int64_t>(sm_count) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
-    return static_cast<int>(needed < full ? needed : full);
 }
 
 }  // namespace
@@ -224,13 +217,18 @@ taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidde
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != TACO_OK)
         return st;
-    const KernelInfo ki = decompress_kernel_info(block);
+    // Tensor-core kernel: one persistent CTA per SM over tiles of 128 (B = 64: 256) blocks.
     const int64_t nblocks = n / block;
+    const KernelInfo ki = decompress_kernel_info(block);
+    alignas(64) CUtensorMap map;
+    cudaError_t e = encode_block_rows_map(&map, y_bf16_out, nblocks, block, ki.tile_blocks);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
-    const int grid =
-        persistent_grid(ntiles, ki.warps, dev->decompress_ctas_per_sm[block_index(block)], dev->sm_count);
-    const cudaError_t e = launch_decompress(block, packed_in, y_bf16_out, nblocks, dev->fault, grid,
-                                            reinterpret_cast<cudaStream_t>(stream));
+    const int per_sm = dev->decompress_ctas_per_sm[block_index(block)];
+    const int64_t full = static_cast<int64_t>(dev->sm_count) * (per_sm > 0 ? per_sm : 1);
+    const int grid = static_cast<int>(ntiles < full ? ntiles : full);
+    e = launch_decompress(block, &map, packed_in, nblocks, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }
 

@@ -39,7 +39,6 @@
 namespace taco {
 namespace {
 
-constexpr uint32_t kMmaNegateA = 1u << 13;   // instruction-descriptor bit: negate A
 
 constexpr int kTcRows = 128;       // blocks per tile = MMA M = TMEM lanes
 constexpr int kEpiThreads = 128;   // threads of one epilogue group (4 warps, one per TMEM lane quarter)
@@ -101,7 +100,7 @@ __device__ void write_hadamard_sw128(uint8_t *h)
 
 template <int B, int STAGES, int EPG, int NBG>
 __global__ void __launch_bounds__(tc_threads(EPG), 1)
-    taco_compress_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, uint8_t *__restrict__ packed,
+    taco_compress_kernel(const __grid_constant__ CUtensorMap tmap_x, uint8_t *__restrict__ packed,
                             int64_t nblocks, uint32_t *__restrict__ fault)
 {
     using Lay = TcCompressLayout<B, STAGES, EPG, NBG>;
@@ -352,7 +351,7 @@ template <int B, int STAGES, int EPG, int NBG>
 struct TcCompressConfig {
     using Lay = TcCompressLayout<B, STAGES, EPG, NBG>;
     static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
-    static void *fn() { return reinterpret_cast<void *>(&taco_compress_tc_kernel<B, STAGES, EPG, NBG>); }
+    static void *fn() { return reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG>); }
     static KernelInfo info()
     {
         return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), kTcRows, 0};

@@ -1,280 +1,405 @@
-// taco_decompress.cu -- the fused receiver-side kernel of TACO (Algorithm 1,
-// lines 19-24; Eqs. 11-13; the paper's fused_ash_decompress_kernel) for GB300
-// (sm_103a): one HBM pass, no intermediate writes.
+// taco_decompress.cu -- TACO's fused receiver-side kernel (Algorithm 1,
+// lines 19-24; Eqs. 11-13; the paper's fused_ash_decompress_kernel) with the
+// inverse rotation on the tensor cores (tcgen05), for GB300 (sm_103a).
 //
-// Work decomposition mirrors the compress kernel: each warp pipelines tiles
-// of 32 consecutive records (16 for B = 256) through shared memory with bulk
-// (TMA) copies on per-stage mbarriers.  A tile of records is contiguous, so
-// one bulk copy fetches it; the record stride (B + 8 bytes) already keeps a
-// lane's 8-byte reads free of bank conflicts.  Each lane decodes its block's
-// codes two at a time (E4M3x2 -> F16x2 -> FP32, exact), runs the
-// Walsh-Hadamard butterflies in registers on FP32x2 pairs, applies one
-// per-block factor and converts to bf16 two at a time.  Output blocks are
-// staged in padded shared-memory slots and leave by per-lane bulk stores.
+// For a tile of blocks, the E4M3 codes of each block form one row of A and
+// Y = A H^T (H symmetric) gives H q for every block at once: the codes are
+// the MMA's 8-bit operand (.kind::f8f6f4), H holds +-1 in E4M3, products are
+// exact and accumulate in FP32 in tensor memory.  G' = Y * (s / sqrt(B) / alpha)
+// per block is Eqs. (11)-(13) up to FP32 summation order.
 //
-// Arithmetic order.  (1/sqrt B) H_B (q s) / alpha = (H_B q) * (s / sqrt B / alpha)
-// in real arithmetic; the kernel rotates the decoded codes (whose sums are
-// exact in FP32 for all but extreme code mixes) and applies the factor
-// c = (s * (1/sqrt B)) / alpha once, which differs from the literal order only
-// by FP32 rounding.
+// Roles in a persistent CTA (one per SM):
+//   warp 0    bulk-copies each tile of records (contiguous, B + 8 bytes each)
+//             into a ring of raw stages;
+//   warp 1    allocates tensor memory and issues the MMAs of a tile into one
+//             of two accumulators (M = 128 rows, N = 128, K = 32 per MMA);
+//   warps 2-5 "transposers": each thread takes one MMA row, copies its codes
+//             from the record into the 128-byte swizzled K-major A layout,
+//             and writes the block's factor s / sqrt(B) / alpha;
+//   warps 6-9 epilogue: each thread reads its row of the accumulator from
+//             TMEM, scales it by the factor, converts two values per cvt to
+//             bf16 into a swizzled output tile, which one thread writes with
+//             2-D TMA stores (rows past the tensor's end are not written).
+// Block sizes: 128 (one block per row, H_128), 256 (one block per row, two
+// 128-code halves; H_256 = [[H, H], [H, -H]] with the negate-A bit), and 64
+// (two blocks per row, H = diag(H_64, H_64)).
+#include <cstring>
+
+#include <cuda.h>
+
 #include "taco_device.cuh"
 #include "taco_kernels.h"
+#include "taco_tcgen05.cuh"
 
 namespace taco {
 namespace {
 
-template <int B>
-struct DecompressShape {
-    static constexpr int kLanesPerBlock = (B <= 128) ? 1 : 2;
-    static constexpr int kTileBlocks = 32 / kLanesPerBlock;
-    static constexpr int kLaneElems = B / kLanesPerBlock;
-    static constexpr int kPairs = kLaneElems / 2;
-    static constexpr int kRecBytes = B + 8;
-    // Each lane stages its 2B/L output bytes in its own slot, padded by 16
-    // bytes so that the lanes' 16-byte writes fall in distinct banks.
-    static constexpr int kLaneOutBytes = 2 * B / kLanesPerBlock;
-    static constexpr int kOutSlotBytes = kLaneOutBytes + 16;
-    static constexpr int kInTileBytes = kTileBlocks * kRecBytes;
-    static constexpr int kOutTileBytes = 32 * kOutSlotBytes;
+constexpr int kDRows = 128;        // MMA rows per tile
+constexpr int kDThreads = 320;     // 10 warps
+constexpr int kGroup = 128;        // threads of the transposer / epilogue groups
+
+template <int B, int RS, int AS, int NOUT>
+struct TcDecompressLayout {
+    static constexpr int kBlocksPerRow = B == 64 ? 2 : 1;
+    static constexpr int kTileBlocks = kDRows * kBlocksPerRow;
+    static constexpr int kRowCodes = B * kBlocksPerRow;            // 128 or 256
+    static constexpr int kAChunks = kRowCodes / 128;               // 128-byte chunks of an A row
+    static constexpr int kHalves = B == 256 ? 2 : 1;
+    static constexpr int kAccCols = 128 * kHalves;                 // TMEM columns per tile
+    static constexpr int kRec = B + 8;
+    static constexpr int kRawBytes = kTileBlocks * kRec;
+    static constexpr int kAStageBytes = kDRows * kRowCodes;
+    static constexpr int kAChunkBytes = kDRows * 128;
+    static constexpr int kHBytes = 128 * 128;
+    static constexpr int kOutRows = kTileBlocks;                   // rows of y per tile
+    static constexpr int kOutChunks = B == 64 ? 1 : B / 64;        // 64-element chunks of a y row
+    static constexpr int kOutChunkBytes = kOutRows * 128;
+    static constexpr int kOutBytes = kOutChunks * kOutChunkBytes;
+    static constexpr int FS = AS + 2;                              // factor slots
+    // Offsets from the 1024-byte aligned base.
+    static constexpr int kOffA = 0;
+    static constexpr int kOffH = kOffA + AS * kAStageBytes;
+    static constexpr int kOffOut = kOffH + kHBytes;
+    static constexpr int kOffRaw = kOffOut + NOUT * kOutBytes;
+    static constexpr int kOffFac = kOffRaw + RS * kRawBytes;      // 16-byte aligned (kRawBytes % 16 == 0)
+    static constexpr int kOffBar = kOffFac + FS * kTileBlocks * 4;
+    static constexpr int kNumBars = 2 * RS + 2 * AS + 4 + 2 * NOUT + FS;
+    static constexpr int kOffTmem = kOffBar + 8 * kNumBars;
+    static constexpr int kBytes = kOffTmem + 16;
+    static constexpr int kSmem = kBytes + 1024;
+    static constexpr int kTmemCols = 2 * kAccCols;
 };
 
-template <int B, int STAGES, int NOUT>
-struct DecompressWarpSmem {
-    using S = DecompressShape<B>;
-    alignas(16) uint8_t in[STAGES][S::kInTileBytes];
-    alignas(16) uint8_t out[NOUT][S::kOutTileBytes];
-    alignas(8) uint64_t bar[STAGES];
-};
-
-// Issues the bulk load of one tile's records (an even number of them; an odd
-// last record of the tensor is read from global memory by its lane instead).
+// The MMA's B operand, K-major, 128-byte swizzle, E4M3 (+1 = 0x38, -1 = 0xB8):
+// H_128 for B = 128 / 256, diag(H_64, H_64) for B = 64.
 template <int B>
-__device__ __forceinline__ void decompress_issue_tile(const uint8_t *__restrict__ packed, int64_t nblocks,
-                                                      int64_t tile, uint32_t in_stage, uint32_t bar, int lane)
+__device__ void write_hadamard_e4m3_sw128(uint8_t *h)
 {
-    using S = DecompressShape<B>;
-    const int64_t blk0 = tile * S::kTileBlocks;
-    const int nvalid = static_cast<int>(nblocks - blk0 < S::kTileBlocks ? nblocks - blk0 : S::kTileBlocks);
-    const int neven = nvalid & ~1;
-    if (lane == 0) {
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(neven) * S::kRecBytes);
-        if (neven > 0)
-            bulk_load(in_stage, packed + blk0 * S::kRecBytes, static_cast<uint32_t>(neven) * S::kRecBytes, bar);
-    }
-}
-
-template <int N>
-__device__ __forceinline__ void load_words(const uint8_t *src_gen, uint32_t src_smem, bool from_global,
-                                           uint32_t (&w)[N])
-{
+    for (int idx = threadIdx.x; idx < 128 * 8; idx += blockDim.x) {
+        const int n = idx / 8, u = idx % 8;
+        uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < N / 2; j++) {
-        uint2 v;
-        if (from_global)
-            v = *reinterpret_cast<const uint2 *>(src_gen + 8 * j);
-        else
-            v = lds64(src_smem + 8 * j);
-        w[2 * j] = v.x;
-        w[2 * j + 1] = v.y;
+        for (int q = 0; q < 4; q++) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int b = 0; b < 4; b++) {
+                const int k = 16 * u + 4 * q + b;
+                uint32_t code;
+                if (B == 64)
+                    code = (n / 64 != k / 64) ? 0x00u : ((__popc((n & 63) & (k & 63)) & 1) ? 0xB8u : 0x38u);
+                else
+                    code = (__popc(n & k) & 1) ? 0xB8u : 0x38u;
+                word |= code << (8 * b);
+            }
+            w[q] = word;
+        }
+        *reinterpret_cast<uint4 *>(h + n * 128 + ((u ^ (n & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-template <int B, int STAGES, int NOUT, int WARPS, int MINB>
-__global__ void __launch_bounds__(WARPS * 32, MINB)
-    taco_decompress_kernel(const uint8_t *__restrict__ packed, uint16_t *__restrict__ y, int64_t nblocks,
-                      uint32_t *__restrict__ fault)
+template <int B, int RS, int AS, int NOUT>
+__global__ void __launch_bounds__(kDThreads, 1)
+    taco_decompress_kernel(const __grid_constant__ CUtensorMap tmap_y, const uint8_t *__restrict__ packed,
+                              int64_t nblocks, uint32_t *__restrict__ fault)
 {
-    using S = DecompressShape<B>;
-    using Smem = DecompressWarpSmem<B, STAGES, NOUT>;
-    constexpr int L = S::kLanesPerBlock;
-    constexpr int NP = S::kPairs;
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT>;
+    constexpr int FS = Lay::FS;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(base);
+    const uint32_t bar0 = sbase + Lay::kOffBar;
+    auto raw_full = [&](int s) { return bar0 + 8u * s; };
+    auto raw_empty = [&](int s) { return bar0 + 8u * (RS + s); };
+    auto a_full = [&](int j) { return bar0 + 8u * (2 * RS + j); };
+    auto a_empty = [&](int j) { return bar0 + 8u * (2 * RS + AS + j); };
+    auto acc_full = [&](int a) { return bar0 + 8u * (2 * RS + 2 * AS + a); };
+    auto acc_empty = [&](int a) { return bar0 + 8u * (2 * RS + 2 * AS + 2 + a); };
+    auto out_free = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + b); };
+    auto out_done = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + NOUT + b); };
+    auto fac_full = [&](int f) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + 2 * NOUT + f); };
+    float *factors = reinterpret_cast<float *>(base + Lay::kOffFac);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
-    extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    Smem &sm = reinterpret_cast<Smem *>(smem_raw)[warp];
+    const int64_t ntiles = (nblocks + Lay::kTileBlocks - 1) / Lay::kTileBlocks;
 
-    const int64_t ntiles = (nblocks + S::kTileBlocks - 1) / S::kTileBlocks;
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * WARPS;
-    if (first >= ntiles)
-        return;
-
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < STAGES; s++)
-            mbar_init(smem_addr(&sm.bar[s]), 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-#pragma unroll
-    for (int s = 0; s < STAGES; s++) {
-        const int64_t t = first + s * stride;
-        if (t < ntiles)
-            decompress_issue_tile<B>(packed, nblocks, t, smem_addr(sm.in[s]), smem_addr(&sm.bar[s]), lane);
-    }
-
-    const int blk = lane / L;
-    const int h = lane % L;
-    const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
-
-    int iter = 0;
-    bool healthy = true;
-    for (int64_t t = first; t < ntiles; t += stride, iter++) {
-        const int stage = iter % STAGES;
-        const uint32_t bar = smem_addr(&sm.bar[stage]);
-        if (!mbar_wait_bounded(bar, (iter / STAGES) & 1, fault, kFaultDecompress)) {
-            healthy = false;
-            break;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RS; s++) {
+            mbar_init(raw_full(s), 1);
+            mbar_init(raw_empty(s), kGroup / 32);
         }
-        const int64_t blk0 = t * S::kTileBlocks;
-        const int nvalid = static_cast<int>(nblocks - blk0 < S::kTileBlocks ? nblocks - blk0 : S::kTileBlocks);
-        const bool active = blk < nvalid;
-        const bool from_global = (nvalid & 1) && blk == nvalid - 1;  // odd last record: not in the tile copy
+        for (int j = 0; j < AS; j++) {
+            mbar_init(a_full(j), kGroup / 32);
+            mbar_init(a_empty(j), 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), kGroup / 32);
+        }
+        for (int b = 0; b < NOUT; b++) {
+            mbar_init(out_free(b), 1);
+            mbar_init(out_done(b), kGroup);
+        }
+        for (int f = 0; f < FS; f++)
+            mbar_init(fac_full(f), kGroup / 32);
+        fence_mbar_init();
+        prefetch_tmap(&tmap_y);
+    }
+    if (warp == 1)
+        tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
+    write_hadamard_e4m3_sw128<B>(base + Lay::kOffH);
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
 
-        float2 v[NP];
-        float factor = 0.f;
-        if (active) {
-            const uint8_t *rec_g = packed + (blk0 + blk) * S::kRecBytes;
-            const uint32_t rec_s = smem_addr(sm.in[stage]) + blk * S::kRecBytes;
-            uint2 meta;
-            if (from_global)
-                meta = *reinterpret_cast<const uint2 *>(rec_g + B);
-            else
-                meta = lds64(rec_s + B);
-            const float alpha = __uint_as_float(meta.x);
-            const float s = __uint_as_float(meta.y);
-            factor = __fdiv_rn(__fmul_rn(s, rB), alpha);
-            if constexpr (L == 1) {
-                // Codes 4j..4j+3 sit in word j.  Pair i = (code 2i, code 2i+1)
-                // after the butterfly on element bit 0.
-                uint32_t w[B / 4];
-                load_words<B / 4>(rec_g, rec_s, from_global, w);
+    if (warp == 0) {
+        // ---- record loader ----------------------------------------------
+        if (lane == 0) {
+            int i = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+                const int s = i % RS;
+                if (i >= RS && !mbar_wait_bounded_thread(raw_empty(s), ((i / RS) - 1) & 1, fault, kFaultDecompress))
+                    break;
+                const int64_t blk0 = t * Lay::kTileBlocks;
+                const int nvalid = static_cast<int>(nblocks - blk0 < Lay::kTileBlocks ? nblocks - blk0
+                                                                                      : Lay::kTileBlocks);
+                const uint32_t bytes = static_cast<uint32_t>(nvalid & ~1) * Lay::kRec;   // multiple of 16
+                mbar_arrive_expect_tx(raw_full(s), bytes);
+                if (bytes > 0)
+                    bulk_load(sbase + Lay::kOffRaw + s * Lay::kRawBytes, packed + blk0 * Lay::kRec, bytes, raw_full(s));
+            }
+            const int issued = i;
+            for (int j = issued - RS > 0 ? issued - RS : 0; j < issued; j++)
+                mbar_wait_bounded_thread(raw_full(j % RS), (j / RS) & 1, fault, kFaultDecompress);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ----------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = mma_idesc_e4m3_f32(kDRows, 128);
+            const uint32_t h0 = sbase + Lay::kOffH;
+            int i = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+                const int j = i % AS, acc = i & 1;
+                if (i >= 2 &&
+                    !mbar_wait_bounded_thread(acc_empty(acc), ((i >> 1) - 1) & 1, fault, kFaultDecompress))
+                    break;
+                if (!mbar_wait_bounded_thread(a_full(j), (i / AS) & 1, fault, kFaultDecompress))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * Lay::kAccCols);
+                const uint32_t a_st = sbase + Lay::kOffA + j * Lay::kAStageBytes;
 #pragma unroll
-                for (int j = 0; j < B / 4; j++) {
-                    v[2 * j] = e4m3x2_butterfly(w[j] & 0xffffu);
-                    v[2 * j + 1] = e4m3x2_butterfly(w[j] >> 16);
-                }
-            } else {
-                // B = 256: half h forms c_j = q_j + (-1)^h q_{j+128} first.
-                uint32_t wa[32], wb[32];
-                load_words<32>(rec_g, rec_s, from_global, wa);
-                load_words<32>(rec_g + 128, rec_s + 128, from_global, wb);
-                const float sg = h ? -1.f : 1.f;
-                const float2 sgn = make_float2(sg, sg);
+                for (int oh = 0; oh < Lay::kHalves; oh++) {
 #pragma unroll
-                for (int j = 0; j < 32; j++) {
+                    for (int ih = 0; ih < Lay::kAChunks; ih++) {
+                        const uint32_t id = (oh == 1 && ih == 1) ? (idesc | kMmaNegateA) : idesc;
 #pragma unroll
-                    for (int half = 0; half < 2; half++) {
-                        const uint32_t pa = half ? (wa[j] >> 16) : (wa[j] & 0xffffu);
-                        const uint32_t pb = half ? (wb[j] >> 16) : (wb[j] & 0xffffu);
-                        const float2 c = fma2(e4m3x2_to_float2(pb), sgn, e4m3x2_to_float2(pa));
-                        v[2 * j + half] = make_float2(c.x + c.y, c.x - c.y);
+                        for (int kk = 0; kk < 4; kk++) {   // 32 codes = 32 bytes per MMA
+                            const uint64_t ad = sw128_kmajor_desc(a_st + ih * Lay::kAChunkBytes + 32 * kk);
+                            const uint64_t bd = sw128_kmajor_desc(h0 + 32 * kk);
+                            tc_mma_f8(d + 128 * oh, ad, bd, id, (ih == 0 && kk == 0) ? 0u : 1u);
+                        }
                     }
                 }
+                tc_commit(a_empty(j));
+                tc_commit(acc_full(acc));
             }
-            fwht_pairs<NP>(v);
+            if (i > 0)
+                mbar_wait_bounded_thread(acc_full((i - 1) & 1), ((i - 1) >> 1) & 1, fault, kFaultDecompress);
         }
-
-        // This stage's tile is consumed: refill it.
-        fence_proxy_async_smem();
-        __syncwarp();
-        {
-            const int64_t tn = t + STAGES * stride;
-            if (tn < ntiles)
-                decompress_issue_tile<B>(packed, nblocks, tn, smem_addr(sm.in[stage]), bar, lane);
-        }
-
-        // Scale, convert to bf16, stage and store.  Each lane's previous store
-        // from this output buffer must have finished reading it.
-        const int ob = iter % NOUT;
-        bulk_wait_read<NOUT - 1>();
-        if (active) {
-            const float2 f2 = make_float2(factor, factor);
-            const uint32_t slot = smem_addr(sm.out[ob]) + lane * S::kOutSlotBytes;
+    } else if (warp < 6) {
+        // ---- transposers (warps 2..5): one MMA row per thread ---------------
+        const int m = threadIdx.x - 64;    // 0..127
+        const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
+        int i = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+            const int s = i % RS, j = i % AS, fs = i % FS;
+            if (!mbar_wait_bounded(raw_full(s), (i / RS) & 1, fault, kFaultDecompress))
+                break;
+            if (i >= AS && !mbar_wait_bounded(a_empty(j), ((i / AS) - 1) & 1, fault, kFaultDecompress))
+                break;
+            const int64_t blk0 = t * Lay::kTileBlocks;
+            const int nvalid = static_cast<int>(nblocks - blk0 < Lay::kTileBlocks ? nblocks - blk0 : Lay::kTileBlocks);
+            const uint32_t raw = sbase + Lay::kOffRaw + s * Lay::kRawBytes;
+            const uint32_t a_row = sbase + Lay::kOffA + j * Lay::kAStageBytes + m * 128;
 #pragma unroll
-            for (int c = 0; c < NP / 4; c++) {
-                uint32_t o[4];
+            for (int b = 0; b < Lay::kBlocksPerRow; b++) {
+                const int bl = m * Lay::kBlocksPerRow + b;    // block within the tile
+                uint32_t w[B / 4];
+                float f = 0.f;
+                if (bl < nvalid) {
+                    const bool from_global = (nvalid & 1) && bl == nvalid - 1;   // not in the bulk copy
+                    const uint8_t *rg = packed + (blk0 + bl) * Lay::kRec;
+                    const uint32_t rs = raw + bl * Lay::kRec;
 #pragma unroll
-                for (int k = 0; k < 2; k++) {
-                    const float2 a = mul2(v[4 * c + 2 * k], f2);
-                    const float2 b = mul2(v[4 * c + 2 * k + 1], f2);
-                    o[2 * k] = float2_to_bf16x2(a.x, a.y);
-                    o[2 * k + 1] = float2_to_bf16x2(b.x, b.y);
+                    for (int q = 0; q < B / 8; q++) {
+                        const uint2 v = from_global ? *reinterpret_cast<const uint2 *>(rg + 8 * q) : lds64(rs + 8 * q);
+                        w[2 * q] = v.x;
+                        w[2 * q + 1] = v.y;
+                    }
+                    const uint2 meta = from_global ? *reinterpret_cast<const uint2 *>(rg + B) : lds64(rs + B);
+                    f = __fdiv_rn(__fmul_rn(__uint_as_float(meta.y), rB), __uint_as_float(meta.x));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < B / 4; q++)
+                        w[q] = 0u;
                 }
-                sts128(slot + 16 * c, make_uint4(o[0], o[1], o[2], o[3]));
+                factors[fs * Lay::kTileBlocks + bl] = f;
+                // Codes to the swizzled A row: 16 codes per 16-byte unit.
+#pragma unroll
+                for (int u = 0; u < B / 16; u++) {
+                    const int ua = b * (B / 16) + u;          // unit index along the A row
+                    const int chunk = ua / 8, uc = ua % 8;
+                    sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
+                           make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]));
+                }
             }
             fence_proxy_async_smem();
-            // One bulk store per lane: its block, or its half of a B = 256 block.
-            bulk_store(y + (blk0 + blk) * B + h * (B / L), slot, S::kLaneOutBytes);
-            bulk_commit();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(raw_empty(s));
+                mbar_arrive(a_full(j));
+                mbar_arrive(fac_full(fs));
+            }
         }
+    } else {
+        // ---- epilogue (warps 6..9): one MMA row per thread ------------------
+        const int et = threadIdx.x - 192;          // 0..127
+        const int q = warp & 3;
+        const int m = 32 * q + lane;               // accumulator row
+        int i = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+            const int acc = i & 1, fs = i % FS, ob = i % NOUT;
+            if (!mbar_wait_bounded(acc_full(acc), (i >> 1) & 1, fault, kFaultDecompress))
+                break;
+            if (!mbar_wait_bounded(fac_full(fs), (i / FS) & 1, fault, kFaultDecompress))
+                break;
+            tc_fence_after_sync();
+            float fb[Lay::kBlocksPerRow];
+#pragma unroll
+            for (int b = 0; b < Lay::kBlocksPerRow; b++)
+                fb[b] = factors[fs * Lay::kTileBlocks + m * Lay::kBlocksPerRow + b];
+            if (i >= NOUT) {
+                if (et == 0) {
+                    bulk_wait_read<NOUT - 1>();
+                    mbar_arrive(out_free(ob));
+                }
+                if (!mbar_wait_bounded(out_free(ob), ((i / NOUT) - 1) & 1, fault, kFaultDecompress))
+                    break;
+            }
+            const uint32_t out = sbase + Lay::kOffOut + ob * Lay::kOutBytes;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                   static_cast<uint32_t>(acc * Lay::kAccCols);
+#pragma unroll
+            for (int c = 0; c < Lay::kAccCols / 32; c++) {
+                uint32_t r[32];
+                tmem_ld32(taddr + 32 * c, r);
+                tmem_ld_wait();
+                const int e0 = 32 * c;                     // first element (column) of the chunk
+                const int b = (B == 64) ? e0 / 64 : 0;     // block within the row (B = 64)
+                const float f = fb[b];
+                const float2 f2 = make_float2(f, f);
+                const int row = (B == 64) ? 2 * m + b : m; // y row within the tile
+                const int el = (B == 64) ? e0 % 64 : e0;   // element within the block row
+#pragma unroll
+                for (int uu = 0; uu < 4; uu++) {           // four 8-element units
+                    uint32_t o[4];
+#pragma unroll
+                    for (int h = 0; h < 4; h++) {
+                        const float2 v = mul2(make_float2(__uint_as_float(r[8 * uu + 2 * h]),
+                                                          __uint_as_float(r[8 * uu + 2 * h + 1])), f2);
+                        o[h] = float2_to_bf16x2(v.x, v.y);
+                    }
+                    const int e = el + 8 * uu;
+                    const int oc = e / 64, u = (e % 64) / 8;
+                    sts128(out + oc * Lay::kOutChunkBytes + row * 128 + ((u ^ (row & 7)) * 16),
+                           make_uint4(o[0], o[1], o[2], o[3]));
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acc_empty(acc));
+            fence_proxy_async_smem();
+            mbar_arrive(out_done(ob));
+            if (warp == 6) {
+                if (!mbar_wait_bounded(out_done(ob), (i / NOUT) & 1, fault, kFaultDecompress))
+                    break;
+                if (lane == 0) {
+                    const int32_t y0 = static_cast<int32_t>(t * Lay::kOutRows);
+#pragma unroll
+                    for (int oc = 0; oc < Lay::kOutChunks; oc++)
+                        tma_store_2d(&tmap_y, 64 * oc, y0, out + oc * Lay::kOutChunkBytes);
+                    bulk_commit();
+                }
+            }
+        }
+        if (et == 0)
+            bulk_wait_all<0>();
     }
 
-    if (!healthy) {
-        for (int s = 0; s < STAGES; s++) {
-            int64_t i = s + static_cast<int64_t>((iter + STAGES - 1 - s) / STAGES) * STAGES;
-            while (i >= 0 && first + i * stride >= ntiles)
-                i -= STAGES;
-            if (i >= 0)
-                mbar_wait_bounded(smem_addr(&sm.bar[s]), static_cast<uint32_t>(i / STAGES) & 1u, fault,
-                                  kFaultDecompress);
-        }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Lay::kTmemCols);
     }
-    bulk_wait_all<0>();
 }
 
-template <int B, int STAGES, int NOUT, int WARPS, int MINB>
-struct DecompressConfig {
-    static constexpr int kWarps = WARPS;
-    static constexpr size_t kSmem = sizeof(DecompressWarpSmem<B, STAGES, NOUT>) * WARPS;
-    static constexpr int kTileBlocks = DecompressShape<B>::kTileBlocks;
-    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, STAGES, NOUT, WARPS, MINB>); }
+template <int B, int RS, int AS, int NOUT>
+struct TcDecompressConfig {
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT>;
+    static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(Lay::kRawBytes % 16 == 0, "raw stage alignment");
+    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, RS, AS, NOUT>); }
+    static KernelInfo info()
+    {
+        return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), kDThreads, Lay::kTileBlocks, 0};
+    }
 };
 
-#ifndef TACO_DECOMPRESS64_CFG
-#define TACO_DECOMPRESS64_CFG 4120
+#ifndef TACO_DTC64_CFG
+#define TACO_DTC64_CFG 322
 #endif
-#ifndef TACO_DECOMPRESS128_CFG
-#define TACO_DECOMPRESS128_CFG 2120
+#ifndef TACO_DTC128_CFG
+#define TACO_DTC128_CFG 322
 #endif
-#ifndef TACO_DECOMPRESS256_CFG
-#define TACO_DECOMPRESS256_CFG 2110
+#ifndef TACO_DTC256_CFG
+#define TACO_DTC256_CFG 221
 #endif
-// Launch shapes, as four digits: stages, output buffers, warps per CTA, and
-// the minimum CTAs per SM given to __launch_bounds__ (0: none).
-using Decompress64 = DecompressConfig<64, TACO_DECOMPRESS64_CFG / 1000, TACO_DECOMPRESS64_CFG / 100 % 10, TACO_DECOMPRESS64_CFG / 10 % 10, TACO_DECOMPRESS64_CFG % 10>;
-using Decompress128 = DecompressConfig<128, TACO_DECOMPRESS128_CFG / 1000, TACO_DECOMPRESS128_CFG / 100 % 10, TACO_DECOMPRESS128_CFG / 10 % 10, TACO_DECOMPRESS128_CFG % 10>;
-using Decompress256 = DecompressConfig<256, TACO_DECOMPRESS256_CFG / 1000, TACO_DECOMPRESS256_CFG / 100 % 10, TACO_DECOMPRESS256_CFG / 10 % 10, TACO_DECOMPRESS256_CFG % 10>;
-
-template <class C>
-KernelInfo info()
-{
-    return KernelInfo{C::fn(), C::kSmem, C::kWarps * 32, C::kTileBlocks, C::kWarps};
-}
+// Per block size, three digits: raw stages, A stages, output tiles.
+using DecompressTc64 = TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10>;
+using DecompressTc128 =
+    TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10>;
+using DecompressTc256 =
+    TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10>;
 
 }  // namespace
 
 KernelInfo decompress_kernel_info(int block)
 {
     switch (block) {
-    case 64: return info<Decompress64>();
-    case 128: return info<Decompress128>();
-    case 256: return info<Decompress256>();
+    case 64: return DecompressTc64::info();
+    case 128: return DecompressTc128::info();
+    case 256: return DecompressTc256::info();
     default: return KernelInfo{};
     }
 }
 
-cudaError_t launch_decompress(int block, const void *packed, void *y, int64_t nblocks, uint32_t *fault, int grid,
-                              cudaStream_t stream)
+cudaError_t launch_decompress(int block, const void *tmap_y, const void *packed, int64_t nblocks, uint32_t *fault,
+                              int grid, cudaStream_t stream)
 {
     const KernelInfo ki = decompress_kernel_info(block);
     if (!ki.fn)
         return cudaErrorInvalidValue;
+    CUtensorMap map;
+    memcpy(&map, tmap_y, sizeof map);
     const uint8_t *pp = static_cast<const uint8_t *>(packed);
-    uint16_t *yp = static_cast<uint16_t *>(y);
-    void *args[] = {&pp, &yp, &nblocks, &fault};
+    void *args[] = {&map, &pp, &nblocks, &fault};
     return cudaLaunchKernel(ki.fn, dim3(grid), dim3(ki.threads), args, ki.smem, stream);
 }
 

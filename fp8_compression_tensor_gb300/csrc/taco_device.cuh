@@ -1,5 +1,5 @@
 // taco_device.cuh -- device-side building blocks shared by the TACO kernels:
-// the fixed constants, inline-PTX wrappers for mbarriers and bulk (TMA) copies,
+// the fixed constants, inline-PTX wrappers for mbarriers and bulk copies,
 // E4M3 / bf16 conversions, packed FP32x2 arithmetic and the bounded wait.
 //
 // Method: "TACO: Efficient Communication Compression of Intermediate Tensors
@@ -191,8 +191,7 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi)
 // Packed FP32x2 arithmetic (one instruction for two lanes of data)
 // ---------------------------------------------------------------------------
 
-// Add and subtract are written as PTX so that a subtraction is one packed
-// instruction (no separate negation of the operand).
+// Packed add written as PTX (one instruction for two lanes of data).
 __device__ __forceinline__ float2 add2(float2 a, float2 b)
 {
     float2 d;
@@ -203,60 +202,14 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b)
     return d;
 }
 
-__device__ __forceinline__ float2 sub2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-
-// Cvt_FP32 (Eq. 11) of two E4M3 codes fused with the first butterfly: returns
-// (q0 + q1, q0 - q1) for the codes in the low 16 bits of `pair` (low byte q0).
-// The codes go to f16 (exact), q1 to f32, and the mixed-precision add / sub
-// take q0 directly from its f16 half; each result is rounded once.
-__device__ __forceinline__ float2 e4m3x2_butterfly(uint32_t pair)
-{
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
-    float s, d;
-    asm("{\n\t.reg .f16 l, h;\n\t.reg .f32 hf;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 hf, h;\n\t"
-        "add.rn.f32.f16 %0, l, hf;\n\tsub.rn.f32.f16 %1, l, hf;\n\t}"
-        : "=f"(s), "=f"(d)
-        : "r"(h2));
-    return make_float2(s, d);
-}
 
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
-}
-
-// In-register Walsh-Hadamard butterflies over the pair index of v[0..NP-1]:
-// pair i and pair i^h are combined as (a + b, a - b) for h = 1, 2, ..., NP/2,
-// i.e. the stages for element-index bits 1 .. log2(NP) when pair i holds
-// elements (2i, 2i+1).  Stage order matches the FWHT of Section 4.2.2.
-template <int NP>
-__device__ __forceinline__ void fwht_pairs(float2 (&v)[NP])
-{
-#pragma unroll
-    for (int h = 1; h < NP; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < NP; i++) {
-            if ((i & h) == 0) {
-                const float2 a = v[i], b = v[i + h];
-                v[i] = add2(a, b);
-                v[i + h] = sub2(a, b);
-            }
-        }
-    }
 }
 
 }  // namespace taco

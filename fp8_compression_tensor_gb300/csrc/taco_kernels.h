@@ -12,7 +12,7 @@ struct KernelInfo {
     void *fn = nullptr;     // kernel entry (for attributes and occupancy queries)
     size_t smem = 0;        // dynamic shared memory per CTA
     int threads = 0;        // threads per CTA
-    int tile_blocks = 0;    // blocks per warp tile; for the shard reduce: threads per block
+    int tile_blocks = 0;    // blocks per CTA tile; for the shard reduce: threads per block
     int warps = 0;          // warps per CTA
 };
 
@@ -24,8 +24,10 @@ KernelInfo reduce_kernel_info(int block);
 // {64, 128}, 128-byte swizzle.
 cudaError_t launch_compress(int block, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault, int grid,
                             cudaStream_t stream);
-cudaError_t launch_decompress(int block, const void *packed, void *y, int64_t nblocks, uint32_t *fault, int grid,
-                              cudaStream_t stream);
+// `tmap_y` points to a CUtensorMap of y viewed as [nblocks, block] bf16, box
+// {64, tile_blocks}, 128-byte swizzle.
+cudaError_t launch_decompress(int block, const void *tmap_y, const void *packed, int64_t nblocks, uint32_t *fault,
+                              int grid, cudaStream_t stream);
 
 constexpr int kMaxShards = 16;
 

@@ -95,6 +95,19 @@ __host__ __device__ constexpr uint32_t mma_idesc_bf16_f32(int M, int N)
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4 with E4M3 A and B (both
+// K-major), FP32 accumulation, shape M x N.
+__host__ __device__ constexpr uint32_t mma_idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4)                                   // D format: F32
+           | (0u << 7)                                 // A format: E4M3
+           | (0u << 10)                                // B format: E4M3
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+constexpr uint32_t kMmaNegateA = 1u << 13;   // instruction-descriptor bit: negate A
+
 // D[tmem] = A * B^T (+ D if accumulate): A is M x K, B is N x K, both from
 // shared-memory descriptors.  Issued by one thread.
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -103,6 +116,17 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Same with 8-bit operands (.kind::f8f6f4): K = 32 per instruction.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -129,6 +153,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         "[%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// 2-D tiled bulk tensor store of a shared-memory box to (x, y); elements
+// outside the tensor are not written.  Tracked by bulk async-groups.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t x, int32_t y, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
