@@ -20,9 +20,18 @@
 namespace taco {
 namespace {
 
-constexpr int kReduceThreads = 256;
-constexpr int kLaneCodes = 16;  // codes (elements) per lane per shard
-constexpr int kBatch = 4;       // shards whose loads are issued together
+#ifndef TACO_REDUCE_PACKED_ADD
+#define TACO_REDUCE_PACKED_ADD 1
+#endif
+#ifndef TACO_REDUCE_THREADS
+#define TACO_REDUCE_THREADS 128
+#endif
+#ifndef TACO_REDUCE_BATCH
+#define TACO_REDUCE_BATCH 4
+#endif
+constexpr int kReduceThreads = TACO_REDUCE_THREADS;
+constexpr int kLaneCodes = 16;                  // codes (elements) per lane per shard
+constexpr int kBatch = TACO_REDUCE_BATCH;       // shards whose loads are issued together
 
 // 16 code bytes of a record.  Records start at multiples of B + 8 bytes,
 // which are only 8-byte aligned, so the bytes come in two 8-byte loads.
@@ -51,10 +60,22 @@ __device__ __forceinline__ void accumulate_shard(float (&w)[kLaneCodes], uint4 c
     for (int k = 0; k < 4; k++) {
         const float2 q0 = e4m3x2_to_float2(words[k] & 0xffffu);
         const float2 q1 = e4m3x2_to_float2(words[k] >> 16);
+#if TACO_REDUCE_PACKED_ADD
+        // Scalar products (never contracted), packed sums.
+        const float2 t0 = make_float2(__fmul_rn(q0.x, f), __fmul_rn(q0.y, f));
+        const float2 t1 = make_float2(__fmul_rn(q1.x, f), __fmul_rn(q1.y, f));
+        const float2 s0 = add2(make_float2(w[4 * k + 0], w[4 * k + 1]), t0);
+        const float2 s1 = add2(make_float2(w[4 * k + 2], w[4 * k + 3]), t1);
+        w[4 * k + 0] = s0.x;
+        w[4 * k + 1] = s0.y;
+        w[4 * k + 2] = s1.x;
+        w[4 * k + 3] = s1.y;
+#else
         w[4 * k + 0] = __fadd_rn(w[4 * k + 0], __fmul_rn(q0.x, f));
         w[4 * k + 1] = __fadd_rn(w[4 * k + 1], __fmul_rn(q0.y, f));
         w[4 * k + 2] = __fadd_rn(w[4 * k + 2], __fmul_rn(q1.x, f));
         w[4 * k + 3] = __fadd_rn(w[4 * k + 3], __fmul_rn(q1.y, f));
+#endif
     }
 }
 
@@ -80,28 +101,33 @@ __global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const
             w[i] = 0.f;
 
         // W = sum_p q_p * (s_p / alpha_p) in shard order, the loads of up to
-        // kBatch shards in flight at a time.
-        for (int p0 = 0; p0 < P; p0 += kBatch) {
-            uint4 codes[kBatch];
-            uint2 meta[kBatch];
+        // kBatch shards in flight at a time.  The shard loop is unrolled to
+        // the maximum shard count so every shard pointer is a fixed kernel
+        // parameter (no indexed parameter access).
 #pragma unroll
-            for (int i = 0; i < kBatch; i++) {
-                if (p0 + i < P && active) {
-                    const uint8_t *rec = args.shards[p0 + i] + off;
-                    codes[i] = ldg_codes16(rec + kLaneCodes * part);
-                    meta[i] = ldg_nc_u2(rec + B);
-                } else {
-                    codes[i] = make_uint4(0u, 0u, 0u, 0u);
-                    meta[i] = make_uint2(0x3f800000u, 0u);  // alpha = 1, s = 0
+        for (int p0 = 0; p0 < kMaxShards; p0 += kBatch) {
+            if (p0 < P) {
+                uint4 codes[kBatch];
+                uint2 meta[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; i++) {
+                    if (p0 + i < P && active) {
+                        const uint8_t *rec = args.shards[p0 + i] + off;
+                        codes[i] = ldg_codes16(rec + kLaneCodes * part);
+                        meta[i] = ldg_nc_u2(rec + B);
+                    } else {
+                        codes[i] = make_uint4(0u, 0u, 0u, 0u);
+                        meta[i] = make_uint2(0x3f800000u, 0u);  // alpha = 1, s = 0
+                    }
                 }
-            }
 #pragma unroll
-            for (int i = 0; i < kBatch; i++) {
-                if (p0 + i < P) {
-                    // s_p / alpha_p (within 2 ulp; alpha_p <= 1e15 is far from
-                    // the range where the fast quotient underflows).
-                    const float f = __fdividef(__uint_as_float(meta[i].y), __uint_as_float(meta[i].x));
-                    accumulate_shard(w, codes[i], f);
+                for (int i = 0; i < kBatch; i++) {
+                    if (p0 + i < P) {
+                        // s_p / alpha_p (within 2 ulp; alpha_p <= 1e15 is far from
+                        // the range where the fast quotient underflows).
+                        const float f = __fdividef(__uint_as_float(meta[i].y), __uint_as_float(meta[i].x));
+                        accumulate_shard(w, codes[i], f);
+                    }
                 }
             }
         }
