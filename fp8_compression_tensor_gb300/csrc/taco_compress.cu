@@ -139,6 +139,23 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
         fence_mbar_init();
         prefetch_tmap(&tmap_x);
     }
+    // The producer (thread 0) fills the first STAGES stages before the rest of
+    // the set-up, so the first loads are in flight while H is written.
+    auto issue_tile = [&](int i, int64_t t) {
+        const int s = i % STAGES;
+        mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
+        const uint32_t dst = sbase + Lay::kOffA + s * Lay::kStageBytes;
+#pragma unroll
+        for (int c = 0; c < Lay::kChunks; c++)
+            tma_load_2d(dst + c * Lay::kChunkBytesA, &tmap_x, 64 * c, static_cast<int32_t>(t * kTcRows), full_bar(s));
+    };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; i++) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+            if (t < ntiles)
+                issue_tile(i, t);
+        }
+    }
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
     write_hadamard_sw128<Lay::kN>(base + Lay::kOffH);
@@ -151,18 +168,18 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     if (warp == 0) {
         // ---- TMA producer ------------------------------------------------
         if (lane == 0) {
-            int i = 0;
-            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+            int i = STAGES;
+            for (int64_t t = blockIdx.x + static_cast<int64_t>(STAGES) * gridDim.x; t < ntiles;
+                 t += gridDim.x, i++) {
                 const int s = i % STAGES;
-                if (i >= STAGES &&
-                    !mbar_wait_bounded_thread(empty_bar(s), ((i / STAGES) - 1) & 1, fault, kFaultCompress))
+                if (!mbar_wait_bounded_thread(empty_bar(s), ((i / STAGES) - 1) & 1, fault, kFaultCompress))
                     break;
-                mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
-                const uint32_t dst = sbase + Lay::kOffA + s * Lay::kStageBytes;
-#pragma unroll
-                for (int c = 0; c < Lay::kChunks; c++)
-                    tma_load_2d(dst + c * Lay::kChunkBytesA, &tmap_x, 64 * c, static_cast<int32_t>(t * kTcRows),
-                                full_bar(s));
+                issue_tile(i, t);
+            }
+            if (i == STAGES) {   // fewer tiles than stages: count what the set-up issued
+                const int64_t left = ntiles - blockIdx.x;
+                const int64_t n = left <= 0 ? 0 : (left + gridDim.x - 1) / gridDim.x;
+                i = static_cast<int>(n < STAGES ? n : STAGES);
             }
             // Copies this thread issued must land before the CTA can exit:
             // the consumer waited on every full barrier unless it stopped early.

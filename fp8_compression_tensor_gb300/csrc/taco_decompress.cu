@@ -147,6 +147,24 @@ __global__ void __launch_bounds__(kDThreads, 1)
         fence_mbar_init();
         prefetch_tmap(&tmap_y);
     }
+    // The loader (thread 0) starts the first RS record copies before the rest
+    // of the set-up, so they are in flight while H is written.
+    auto issue_tile = [&](int i, int64_t t) {
+        const int s = i % RS;
+        const int64_t blk0 = t * Lay::kTileBlocks;
+        const int nvalid = static_cast<int>(nblocks - blk0 < Lay::kTileBlocks ? nblocks - blk0 : Lay::kTileBlocks);
+        const uint32_t bytes = static_cast<uint32_t>(nvalid & ~1) * Lay::kRec;   // multiple of 16
+        mbar_arrive_expect_tx(raw_full(s), bytes);
+        if (bytes > 0)
+            bulk_load(sbase + Lay::kOffRaw + s * Lay::kRawBytes, packed + blk0 * Lay::kRec, bytes, raw_full(s));
+    };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RS; i++) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+            if (t < ntiles)
+                issue_tile(i, t);
+        }
+    }
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
     write_hadamard_e4m3_sw128<B>(base + Lay::kOffH);
@@ -159,18 +177,17 @@ __global__ void __launch_bounds__(kDThreads, 1)
     if (warp == 0) {
         // ---- record loader ----------------------------------------------
         if (lane == 0) {
-            int i = 0;
-            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+            int i = RS;
+            for (int64_t t = blockIdx.x + static_cast<int64_t>(RS) * gridDim.x; t < ntiles; t += gridDim.x, i++) {
                 const int s = i % RS;
-                if (i >= RS && !mbar_wait_bounded_thread(raw_empty(s), ((i / RS) - 1) & 1, fault, kFaultDecompress))
+                if (!mbar_wait_bounded_thread(raw_empty(s), ((i / RS) - 1) & 1, fault, kFaultDecompress))
                     break;
-                const int64_t blk0 = t * Lay::kTileBlocks;
-                const int nvalid = static_cast<int>(nblocks - blk0 < Lay::kTileBlocks ? nblocks - blk0
-                                                                                      : Lay::kTileBlocks);
-                const uint32_t bytes = static_cast<uint32_t>(nvalid & ~1) * Lay::kRec;   // multiple of 16
-                mbar_arrive_expect_tx(raw_full(s), bytes);
-                if (bytes > 0)
-                    bulk_load(sbase + Lay::kOffRaw + s * Lay::kRawBytes, packed + blk0 * Lay::kRec, bytes, raw_full(s));
+                issue_tile(i, t);
+            }
+            if (i == RS) {   // fewer tiles than stages: count what the set-up issued
+                const int64_t left = ntiles - blockIdx.x;
+                const int64_t n = left <= 0 ? 0 : (left + gridDim.x - 1) / gridDim.x;
+                i = static_cast<int>(n < RS ? n : RS);
             }
             const int issued = i;
             for (int j = issued - RS > 0 ? issued - RS : 0; j < issued; j++)
