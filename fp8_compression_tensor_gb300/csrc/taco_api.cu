@@ -266,8 +266,9 @@ taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shard
     const KernelInfo ki = reduce_kernel_info(block);
     const int64_t threads_needed = args.nblocks * ki.tile_blocks;
     const int64_t ctas_needed = (threads_needed + ki.threads - 1) / ki.threads;
-    const int per_sm = dev->reduce_ctas_per_sm[block_index(block)];
-    const int64_t full = static_cast<int64_t>(dev->sm_count) * (per_sm > 0 ? per_sm : 1);
+    // One pass over the blocks: every thread takes one part of one block.  A
+    // persistent grid (SM count x resident CTAs, looping) measured slower.
+    const int64_t full = INT32_MAX;
     const int grid = static_cast<int>(ctas_needed < full ? ctas_needed : full);
     const cudaError_t e = launch_reduce(block, args, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
