@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     write_hadamard_sw128<Lay::kN>(base + Lay::kOffH);
     fence_proxy_async_smem();   // H is read by the tensor core (async proxy)
     tc_fence_before_sync();
-    __syncthreads();
+    cta_barrier();   // lanes of warps 0 and 1 took different paths above
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
 
     // ---- tear-down -------------------------------------------------------
     tc_fence_before_sync();
-    __syncthreads();
+    cta_barrier();   // every role ran lane-divergent code
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Lay::kTmemCols);

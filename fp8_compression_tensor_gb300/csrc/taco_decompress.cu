@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     write_hadamard_e4m3_sw128<B>(base + Lay::kOffH);
     fence_proxy_async_smem();
     tc_fence_before_sync();
-    __syncthreads();
+    cta_barrier();   // lanes of warps 0 and 1 took different paths above
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    cta_barrier();   // every role ran lane-divergent code
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Lay::kTmemCols);

@@ -134,6 +134,16 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// CTA-wide barrier over all threads, counted thread by thread (the
+// non-aligned form): lanes of one warp that took different paths (a
+// single-lane producer or issuer) may arrive separately.  The aligned form
+// behind __syncthreads() expects whole converged warps and may release early
+// when a warp arrives in pieces.
+__device__ __forceinline__ void cta_barrier()
+{
+    asm volatile("barrier.sync 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint2 lds64(uint32_t addr)
 {
     uint2 v;
