@@ -10,9 +10,15 @@ GPT-style TP activation, bf16 [8192 x 4096], block 128):
                         AllReduce, -> one reduced segment          (Section 4.4.2)
   3. taco_decompress    packed records      -> y (bf16)           (Eqs. 11-13)
 
-Each kernel is timed with CUDA events on the stream it runs on; before each
-kernel a read of a buffer twice the L2 size (untimed) evicts what the
-previous kernel left in L2, so every kernel reads its inputs from HBM.
+Steady state.  The step runs as a CUDA graph of the three launches, replayed
+K times back to back.  Inputs rotate over R buffer sets (R x the bytes of one
+set >= 3 x L2) and the three kernels of step k work on different sets: compress
+on set k, the reduce on the packed records of set k-2 and decompress on those
+of set k-3 (k mod R), so every kernel reads data last written at least two
+kernels and some hundreds of MB of traffic earlier, from HBM, and the deferred
+write-back of every kernel's output is paid inside the timed region.  Each
+kernel's own average launch duration is timed the same way: graphs of R
+back-to-back launches of that kernel alone, replayed, over the rotating sets.
 
 Metric: GB/s of bf16 data processed = (2N compressed + 2N decompressed + 2N
 logical bf16 bytes of the P reduced segments) per step / step time.  The
@@ -60,7 +66,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["taco", "reference"], default="taco")
     ap.add_argument("--workload", default="gpt_activation_8192x4096", choices=sorted(workloads.WORKLOADS))
@@ -309,37 +315,53 @@ def run_taco(args, rank, world):
 
     x_host_bits = w.tensor(seed=w.seeds[0] + rank).reshape(rows, hidden)
     x_pinned = torch.from_numpy(x_host_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    x = x_pinned.to(dev)
-    packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    y = torch.empty((rows, hidden), dtype=torch.bfloat16, device=dev)
-    reduced = torch.empty(seg_bytes, dtype=torch.uint8, device=dev)
-    segments = [packed[p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)]
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20)) or (128 << 20)
-    flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    set_bytes = 2 * n + nbytes + seg_bytes + 2 * n
+    R = max(4, -(-3 * l2 // set_bytes))
+    xs = [x_pinned.to(dev) for _ in range(R)]
+    packs = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(R)]
+    reds = [torch.empty(seg_bytes, dtype=torch.uint8, device=dev) for _ in range(R)]
+    ys = [torch.empty((rows, hidden), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    segs = [[packs[r][p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)] for r in range(R)]
+    stream = torch.cuda.Stream(dev)
 
-    def flush():
-        flush_buf.sum()
+    def op_compress(r):
+        taco.compress(xs[r], block, out=packs[r], stream=stream)
 
-    def step(ev=None):
-        flush()
-        if ev: ev[0].record(stream)
-        taco.compress(x, block, out=packed, stream=stream)
-        if ev: ev[1].record(stream)
-        flush()
-        if ev: ev[2].record(stream)
-        taco.reduce_shards(segments, seg_rows, hidden, block, out=reduced, stream=stream)
-        if ev: ev[3].record(stream)
-        flush()
-        if ev: ev[4].record(stream)
-        taco.decompress(packed, rows, hidden, block, out=y, stream=stream)
-        if ev: ev[5].record(stream)
+    def op_reduce(r):
+        taco.reduce_shards(segs[r], seg_rows, hidden, block, out=reds[r], stream=stream)
+
+    def op_decompress(r):
+        taco.decompress(packs[r], rows, hidden, block, out=ys[r], stream=stream)
+
+    def step(k):
+        op_compress(k % R)
+        op_reduce((k - 2) % R)
+        op_decompress((k - 3) % R)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for r in range(R):          # every set holds valid records before the skewed steps read them
+            op_compress(r)
+        for k in range(R):
+            step(k)
+        stream.synchronize()
+        step_graphs = [capture(lambda k=k: step(k)) for k in range(R)]
+        cycle_graph = capture(lambda: [step(k) for k in range(R)])   # R steps, sets 0..R-1 once each
+        solo_graphs = {name: capture(lambda fn=fn: [fn(r) for r in range(R)])
+                       for name, fn in (("compress", op_compress), ("reduce", op_reduce),
+                                        ("decompress", op_decompress))}
 
     uuid = None
     try:
@@ -350,26 +372,46 @@ def run_taco(args, rank, world):
     if not args.no_clocks:
         sampler.start()
 
-    for _ in range(args.warmup):
-        step()
+    K = args.steps
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            step_graphs[k % R].replay()
     barrier()
-    taco.device_status()
+    taco.device_status(stream=stream)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     t_wall0 = time.time()
-    for k in range(args.steps):
-        step(events[k])
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(K // R):
+            cycle_graph.replay()
+        for k in range(K - K % R, K):
+            step_graphs[k % R].replay()
+        ev1.record(stream)
     barrier()
     t_wall1 = time.time()
-    flags = taco.device_status()
+    flags = taco.device_status(stream=stream)
+    ms_step = max_over_ranks([ev0.elapsed_time(ev1) / K], device=dev)[0]
 
-    comp = [e[0].elapsed_time(e[1]) for e in events]
-    red = [e[2].elapsed_time(e[3]) for e in events]
-    dec = [e[4].elapsed_time(e[5]) for e in events]
-    tot_comp, tot_red, tot_dec = max_over_ranks([sum(comp), sum(red), sum(dec)], device=dev)
-    K = args.steps
-    ms_step = (tot_comp + tot_red + tot_dec) / K
+    # Each kernel alone: back-to-back launches over the rotating sets.
+    reps = max(4, min(250, (20 * K) // (R * 10)))
+    solo_ms = {}
+    with torch.cuda.stream(stream):
+        for name, g in solo_graphs.items():
+            for _ in range(2):
+                g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            stream.synchronize()
+            solo_ms[name] = a.elapsed_time(b) / (reps * R)
+    tot = max_over_ranks([solo_ms["compress"], solo_ms["reduce"], solo_ms["decompress"]], device=dev)
+    solo_ms = dict(zip(("compress", "reduce", "decompress"), tot))
+    x, packed, reduced, y = xs[0], packs[0], reds[0], ys[0]
+    segments = segs[0]
 
     # End to end through the public API with host buffers: pinned H2D of the
     # step's input, the three calls, D2H of the decompressed tensor and of
@@ -378,23 +420,25 @@ def run_taco(args, rank, world):
     if not args.no_e2e:
         y_pinned = torch.empty((rows, hidden), dtype=torch.bfloat16).pin_memory()
         r_pinned = torch.empty(seg_bytes, dtype=torch.uint8).pin_memory()
-        for _ in range(max(1, min(args.warmup, 5))):
-            x.copy_(x_pinned, non_blocking=True)
-            step()
-            y_pinned.copy_(y, non_blocking=True)
-            r_pinned.copy_(reduced, non_blocking=True)
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k_e2e = max(1, min(K, 200))
-        e0.record(stream)
-        for _ in range(k_e2e):
+
+        def e2e_step():
             x.copy_(x_pinned, non_blocking=True)
             taco.compress(x, block, out=packed, stream=stream)
             taco.reduce_shards(segments, seg_rows, hidden, block, out=reduced, stream=stream)
             taco.decompress(packed, rows, hidden, block, out=y, stream=stream)
             y_pinned.copy_(y, non_blocking=True)
             r_pinned.copy_(reduced, non_blocking=True)
-        e1.record(stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, min(args.warmup, 5))):
+                e2e_step()
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k_e2e = max(1, min(K, 200))
+            e0.record(stream)
+            for _ in range(k_e2e):
+                e2e_step()
+            e1.record(stream)
         barrier()
         ms = max_over_ranks([e0.elapsed_time(e1) / k_e2e], device=dev)[0]
         e2e = {"value": whole_job_gbs(world, 6.0 * n, ms), "unit": UNIT, "ms_per_step": ms,
@@ -412,19 +456,21 @@ def run_taco(args, rank, world):
         "reduce": P * seg_bytes + seg_bytes,
         "decompress": nbytes + 2 * n,
     }
-    avg_ms = {"compress": tot_comp / K, "reduce": tot_red / K, "decompress": tot_dec / K}
+    avg_ms = solo_ms
     ops = {}
     for op in ("compress", "reduce", "decompress"):
         t = avg_ms[op] * 1e-3
         ops[op] = {"ms": avg_ms[op], "bf16_gbs": 2 * n / t / 1e9,
                    "hbm_gbs": alg[op] / t / 1e9, "frac_of_measured_hbm": alg[op] / t / 1e9 / peak,
-                   "algorithmic_bytes": alg[op]}
+                   "algorithmic_bytes": alg[op], "launches_timed": reps * R}
     dom = max(avg_ms, key=avg_ms.get)
     achieved = alg[dom] / (avg_ms[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_src,
                 "traffic": traffic_for(dom, w.name, block),
-                "algorithmic_bytes_per_launch": alg[dom]}
+                "algorithmic_bytes_per_launch": alg[dom],
+                "duration": (f"mean of {reps * R} back-to-back launches of the kernel alone (graph replays over "
+                             f"the {R} rotating sets), CUDA events on its stream")}
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -461,9 +507,13 @@ def run_taco(args, rank, world):
         "config": {"workload": w.name, "rows": rows, "hidden": hidden, "block": block, "reduce_shards": P,
                    "step": "compress + reduce_shards(P row-slices of the packed tensor) + decompress",
                    "bytes_per_step": "6N: 2N compressed + 2N logical bf16 of the reduced segments + 2N decompressed",
-                   "l2": "read of a 2x-L2 buffer before each kernel (untimed); kernels timed with CUDA events",
+                   "l2": (f"no flush; inputs larger than L2: {R} rotating buffer sets of {set_bytes / 1e6:.1f} MB "
+                          f"(L2 {l2 / 1e6:.0f} MB); step k compresses set k, reduces set k-2, decompresses "
+                          f"set k-3; graph replays (one graph per R steps), one CUDA-event pair around the K steps"),
+                   "buffer_sets": R,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops,
+        "ops_sum_ms": sum(avg_ms.values()),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

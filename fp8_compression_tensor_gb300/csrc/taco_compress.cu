@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     auto rec_done_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + NOUT + b); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
+    grid_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t ntiles = (nblocks + kTcRows - 1) / kTcRows;
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             tma_load_2d(dst + c * Lay::kChunkBytesA, &tmap_x, 64 * c, static_cast<int32_t>(t * kTcRows), full_bar(s));
     };
     if (threadIdx.x == 0) {
+        grid_dependency_wait();   // the input may come from the previous kernel
         for (int i = 0; i < STAGES; i++) {
             const int64_t t = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
             if (t < ntiles)
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     write_hadamard_sw128<Lay::kN>(base + Lay::kOffH);
     fence_proxy_async_smem();   // H is read by the tensor core (async proxy)
     tc_fence_before_sync();
+    grid_dependency_wait();   // before any global access of this thread
     cta_barrier();   // lanes of warps 0 and 1 took different paths above
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
@@ -411,7 +414,7 @@ cudaError_t launch_compress(int block, const void *tmap, void *packed, int64_t n
     memcpy(&map, tmap, sizeof map);
     uint8_t *pp = static_cast<uint8_t *>(packed);
     void *args[] = {&map, &pp, &nblocks, &fault};
-    return cudaLaunchKernel(ki.fn, dim3(grid), dim3(ki.threads), args, ki.smem, stream);
+    return launch_kernel(ki.fn, grid, ki.threads, ki.smem, stream, args);
 }
 
 }  // namespace taco

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     float *factors = reinterpret_cast<float *>(base + Lay::kOffFac);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
+    grid_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t ntiles = (nblocks + Lay::kTileBlocks - 1) / Lay::kTileBlocks;
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
             bulk_load(sbase + Lay::kOffRaw + s * Lay::kRawBytes, packed + blk0 * Lay::kRec, bytes, raw_full(s));
     };
     if (threadIdx.x == 0) {
+        grid_dependency_wait();   // the input may come from the previous kernel
         for (int i = 0; i < RS; i++) {
             const int64_t t = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
             if (t < ntiles)
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     write_hadamard_e4m3_sw128<B>(base + Lay::kOffH);
     fence_proxy_async_smem();
     tc_fence_before_sync();
+    grid_dependency_wait();   // before any global access of this thread
     cta_barrier();   // lanes of warps 0 and 1 took different paths above
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
@@ -417,7 +420,7 @@ cudaError_t launch_decompress(int block, const void *tmap_y, const void *packed,
     memcpy(&map, tmap_y, sizeof map);
     const uint8_t *pp = static_cast<const uint8_t *>(packed);
     void *args[] = {&map, &pp, &nblocks, &fault};
-    return cudaLaunchKernel(ki.fn, dim3(grid), dim3(ki.threads), args, ki.smem, stream);
+    return launch_kernel(ki.fn, grid, ki.threads, ki.smem, stream, args);
 }
 
 }  // namespace taco

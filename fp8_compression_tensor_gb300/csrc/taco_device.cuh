@@ -134,6 +134,23 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream is still
+// running; grid_dependency_wait() returns once that kernel has completed and
+// its memory operations are visible (at once for an ordinary launch), so every
+// thread calls it before its first global-memory access.
+// grid_launch_dependents() lets the next kernel in the stream be scheduled
+// (on the SM resources this grid frees) before this one has finished.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // CTA-wide barrier over all threads, counted thread by thread (the
 // non-aligned form): lanes of one warp that took different paths (a
 // single-lane producer or issuer) may arrive separately.  The aligned form

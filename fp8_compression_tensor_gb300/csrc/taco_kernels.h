@@ -16,6 +16,28 @@ struct KernelInfo {
     int warps = 0;          // warps per CTA
 };
 
+#ifndef TACO_PDL
+#define TACO_PDL 1
+#endif
+
+// Launches `fn` with programmatic stream serialisation (when TACO_PDL): the
+// kernel may be scheduled while the previous kernel in the stream finishes;
+// the kernels order their memory accesses with griddepcontrol.wait.
+inline cudaError_t launch_kernel(const void *fn, int grid, int threads, size_t smem, cudaStream_t stream, void **args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = TACO_PDL ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 KernelInfo compress_kernel_info(int block);
 KernelInfo decompress_kernel_info(int block);
 KernelInfo reduce_kernel_info(int block);

@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const
     constexpr int kRec = B + 8;
     const int64_t total = args.nblocks * LPB;
     const int P = args.num_shards;
+    grid_launch_dependents();
+    grid_dependency_wait();   // the shards may come from the previous kernel
 
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
          g - (threadIdx.x & 31) < total;  // whole warps iterate together
@@ -202,7 +204,7 @@ cudaError_t launch_reduce(int block, const ReduceArgs &args, int grid, cudaStrea
         return cudaErrorInvalidValue;
     ReduceArgs a = args;
     void *params[] = {&a};
-    return cudaLaunchKernel(ki.fn, dim3(grid), dim3(ki.threads), params, 0, stream);
+    return launch_kernel(ki.fn, grid, ki.threads, 0, stream, params);
 }
 
 }  // namespace taco
