@@ -186,17 +186,18 @@ taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t hidden, in
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != TACO_OK)
         return st;
-    // Tensor-core kernel: one persistent CTA per SM over tiles of 128 blocks.
+    // Tensor-core kernel over tiles of 128 blocks: one CTA per tile, of which
+    // one per SM runs and takes the tiles of CTAs it cancels before they start.
     const int64_t nblocks = n / block;
     const KernelInfo ki = compress_kernel_info(block);
+    const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
+    if (ntiles > INT32_MAX)
+        return TACO_ERR_BAD_SHAPE;
     alignas(64) CUtensorMap map;
     cudaError_t e = encode_block_rows_map(&map, x_bf16, nblocks, block);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
-    const int per_sm = dev->compress_ctas_per_sm[block_index(block)];
-    const int64_t full = static_cast<int64_t>(dev->sm_count) * (per_sm > 0 ? per_sm : 1);
-    const int grid = static_cast<int>(ntiles < full ? ntiles : full);
+    const int grid = static_cast<int>(ntiles);
     e = launch_compress(block, &map, packed_out, nblocks, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }
@@ -217,17 +218,18 @@ taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidde
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != TACO_OK)
         return st;
-    // Tensor-core kernel: one persistent CTA per SM over tiles of 128 (B = 64: 256) blocks.
+    // Tensor-core kernel over tiles of 128 (B = 64: 256) blocks: one CTA per
+    // tile, of which one per SM runs and takes the tiles of CTAs it cancels.
     const int64_t nblocks = n / block;
     const KernelInfo ki = decompress_kernel_info(block);
+    const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
+    if (ntiles > INT32_MAX)
+        return TACO_ERR_BAD_SHAPE;
     alignas(64) CUtensorMap map;
     cudaError_t e = encode_block_rows_map(&map, y_bf16_out, nblocks, block, ki.tile_blocks);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
-    const int per_sm = dev->decompress_ctas_per_sm[block_index(block)];
-    const int64_t full = static_cast<int64_t>(dev->sm_count) * (per_sm > 0 ? per_sm : 1);
-    const int grid = static_cast<int>(ntiles < full ? ntiles : full);
+    const int grid = static_cast<int>(ntiles);
     e = launch_decompress(block, &map, packed_in, nblocks, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }

@@ -8,7 +8,13 @@
 // and the tensor core accumulates in FP32, so Y is the unnormalised rotation
 // of Eq. (8) up to FP32 summation order.
 //
-// Roles in a persistent CTA (one per SM), one tile of 128 blocks at a time:
+// Scheduling: the grid has one CTA per tile of 128 blocks, and shared memory
+// admits one CTA per SM.  A running CTA takes its own tile, then claims the
+// tiles of CTAs that have not started yet by cancelling them (cluster launch
+// control), so CTAs that get more memory bandwidth take more tiles and all
+// SMs finish together.
+//
+// Roles in a CTA, one tile at a time:
 //   warp 0  TMA producer: 2-D tiled loads (128-byte swizzle) of the tile into a
 //           ring of STAGES shared-memory stages;
 //   warp 1  allocates tensor memory and issues the B/16 tcgen05.mma of a tile
@@ -66,8 +72,17 @@ struct TcCompressLayout {
     static constexpr int kOffA = 0;
     static constexpr int kOffH = kOffA + STAGES * kStageBytes;
     static constexpr int kOffOut = kOffH + kHBytes;
-    static constexpr int kOffBar = kOffOut + NOUT * kOutBytes;     // 8-byte aligned
-    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * NOUT;
+    // Tile scheduling: ring of kSched 16-byte cluster-launch-control
+    // responses, kSchedAhead requests in flight.  A slot is reused only after
+    // the producer has passed the empty barrier kSchedAhead + STAGES + 3
+    // tiles later, when the MMA issuer and both epilogue groups have read it.
+    static constexpr int kSched = 16;
+    static constexpr int kSchedAhead = 4;
+    static_assert(kSched >= kSchedAhead + STAGES + 3, "response slot reused too early");
+    static_assert(kSchedAhead >= EPG, "every epilogue group must find the failed response");
+    static constexpr int kOffResp = kOffOut + NOUT * kOutBytes;    // 16-byte aligned
+    static constexpr int kOffBar = kOffResp + 16 * kSched;         // 8-byte aligned
+    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * NOUT + kSched;
     static constexpr int kOffTmem = kOffBar + 8 * kNumBars;
     static constexpr int kBytes = kOffTmem + 16;
     static constexpr int kSmem = kBytes + 1024;                    // slack for 1024-byte alignment
@@ -116,12 +131,40 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     auto acc_empty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     auto out_free_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
     auto rec_done_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + NOUT + b); };
+    auto sched_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 4 + 2 * NOUT + q); };
+    const uint32_t resp0 = sbase + Lay::kOffResp;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
     grid_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t ntiles = (nblocks + kTcRows - 1) / kTcRows;
+
+    // Work items.  The grid has one CTA per tile; a running CTA takes item 0
+    // = its own tile, then cancels CTAs that have not started and takes their
+    // tiles (request j answers item j, in slot (j - 1) % kSched), until a
+    // request fails because none is left.  Faster CTAs so take more tiles.
+    auto request_item = [&](int j) {   // producer thread
+        const int q = (j - 1) % Lay::kSched;
+        mbar_arrive_expect_tx(sched_bar(q), 16);
+        clc_try_cancel(resp0 + 16u * q, sched_bar(q));
+    };
+    // Tile of item j, or -1 when none was left (or the wait timed out).
+    auto item_tile_thread = [&](int j) -> int64_t {
+        if (j == 0)
+            return blockIdx.x;
+        const int q = (j - 1) % Lay::kSched;
+        if (!mbar_wait_bounded_thread(sched_bar(q), ((j - 1) / Lay::kSched) & 1, fault, kFaultCompress))
+            return -1;
+        return clc_response_ctaid_x(resp0 + 16u * q);
+    };
+    auto item_tile_warp = [&](int j) -> int64_t {
+        if (j == 0)
+            return blockIdx.x;
+        const int q = (j - 1) % Lay::kSched;
+        if (!mbar_wait_bounded(sched_bar(q), ((j - 1) / Lay::kSched) & 1, fault, kFaultCompress))
+            return -1;
+        return clc_response_ctaid_x(resp0 + 16u * q);
+    };
 
     // ---- set-up ----------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -137,11 +180,13 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             mbar_init(out_free_bar(b), 1);
             mbar_init(rec_done_bar(b), kEpiThreads);
         }
+        for (int q = 0; q < Lay::kSched; q++)
+            mbar_init(sched_bar(q), 1);
         fence_mbar_init();
         prefetch_tmap(&tmap_x);
     }
-    // The producer (thread 0) fills the first STAGES stages before the rest of
-    // the set-up, so the first loads are in flight while H is written.
+    // The producer (thread 0) starts its own tile's load and the first
+    // kSchedAhead tile requests before the rest of the set-up.
     auto issue_tile = [&](int i, int64_t t) {
         const int s = i % STAGES;
         mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
@@ -151,12 +196,10 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             tma_load_2d(dst + c * Lay::kChunkBytesA, &tmap_x, 64 * c, static_cast<int32_t>(t * kTcRows), full_bar(s));
     };
     if (threadIdx.x == 0) {
+        for (int j = 1; j <= Lay::kSchedAhead; j++)
+            request_item(j);
         grid_dependency_wait();   // the input may come from the previous kernel
-        for (int i = 0; i < STAGES; i++) {
-            const int64_t t = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
-            if (t < ntiles)
-                issue_tile(i, t);
-        }
+        issue_tile(0, blockIdx.x);
     }
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
@@ -171,21 +214,24 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     if (warp == 0) {
         // ---- TMA producer ------------------------------------------------
         if (lane == 0) {
-            int i = STAGES;
-            for (int64_t t = blockIdx.x + static_cast<int64_t>(STAGES) * gridDim.x; t < ntiles;
-                 t += gridDim.x, i++) {
+            int i = 1;                           // items 0 .. i-1 have been loaded
+            int requested = Lay::kSchedAhead;    // requests 1 .. requested issued
+            for (;; i++) {
+                const int64_t t = item_tile_thread(i);
+                if (t < 0)
+                    break;
+                request_item(++requested);       // no failure seen yet: keep kSchedAhead in flight
                 const int s = i % STAGES;
-                if (!mbar_wait_bounded_thread(empty_bar(s), ((i / STAGES) - 1) & 1, fault, kFaultCompress))
+                if (i >= STAGES &&
+                    !mbar_wait_bounded_thread(empty_bar(s), ((i / STAGES) - 1) & 1, fault, kFaultCompress))
                     break;
                 issue_tile(i, t);
             }
-            if (i == STAGES) {   // fewer tiles than stages: count what the set-up issued
-                const int64_t left = ntiles - blockIdx.x;
-                const int64_t n = left <= 0 ? 0 : (left + gridDim.x - 1) / gridDim.x;
-                i = static_cast<int>(n < STAGES ? n : STAGES);
-            }
-            // Copies this thread issued must land before the CTA can exit:
-            // the consumer waited on every full barrier unless it stopped early.
+            // Responses still in flight and copies this thread issued must
+            // land before the CTA can exit.
+            for (int j = i; j <= requested; j++)
+                mbar_wait_bounded_thread(sched_bar((j - 1) % Lay::kSched), ((j - 1) / Lay::kSched) & 1, fault,
+                                         kFaultCompress);
             const int issued = i;
             for (int j = issued - STAGES > 0 ? issued - STAGES : 0; j < issued; j++)
                 mbar_wait_bounded_thread(full_bar(j % STAGES), (j / STAGES) & 1, fault, kFaultCompress);
@@ -196,7 +242,9 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             constexpr uint32_t idesc = mma_idesc_bf16_f32(kTcRows, Lay::kN);
             const uint32_t a0 = sbase + Lay::kOffA, h0 = sbase + Lay::kOffH;
             int i = 0;
-            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, i++) {
+            for (;; i++) {
+                if (item_tile_thread(i) < 0)
+                    break;
                 const int s = i % STAGES, acc = i & 1;
                 if (i >= 2 && !mbar_wait_bounded_thread(acc_empty_bar(acc), ((i >> 1) - 1) & 1, fault,
                                                         kFaultCompress))
@@ -250,10 +298,11 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
         const int row = 32 * q + lane;                  // accumulator row = block within the tile
         const bool store_warp = ((warp - 2) & 3) == 0;  // first warp of the group issues the stores
         const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
-        int kt = 0;   // tiles this group has handled
-        for (int64_t t = blockIdx.x + static_cast<int64_t>(grp) * gridDim.x; t < ntiles;
-             t += static_cast<int64_t>(EPG) * gridDim.x, kt++) {
-            const int i = EPG * kt + grp;               // the CTA's tile counter
+        for (int kt = 0;; kt++) {                   // kt: tiles this group has handled
+            const int i = EPG * kt + grp;               // the CTA's item counter
+            const int64_t t = item_tile_warp(i);
+            if (t < 0)
+                break;
             const int acc = i & 1;
             if (!mbar_wait_bounded(acc_full_bar(acc), (i >> 1) & 1, fault, kFaultCompress))
                 break;

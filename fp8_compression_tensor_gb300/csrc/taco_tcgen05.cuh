@@ -140,6 +140,39 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
 }
 
 // ---------------------------------------------------------------------------
+// Cluster launch control (dynamic tile scheduling)
+// ---------------------------------------------------------------------------
+
+// Asks the hardware to cancel one CTA of this grid that has not started yet;
+// the 16-byte response lands at `result_addr` (16-byte aligned shared memory)
+// and completes 16 transaction bytes on `bar` (the caller arrives on `bar`
+// with expect_tx(16) first).  No request may be issued once a failed
+// response has been observed.
+__device__ __forceinline__ void clc_try_cancel(uint32_t result_addr, uint32_t bar)
+{
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+                 ::"r"(result_addr), "r"(bar)
+                 : "memory");
+}
+
+// Reads a response: the x index of the cancelled CTA (whose work the caller
+// now does), or -1 if no CTA was left to cancel.
+__device__ __forceinline__ int64_t clc_response_ctaid_x(uint32_t result_addr)
+{
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "r"(result_addr)
+        : "memory");
+    return ok ? static_cast<int64_t>(x) : -1;
+}
+
+// ---------------------------------------------------------------------------
 // TMA, barriers
 // ---------------------------------------------------------------------------
 
