@@ -76,7 +76,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str |
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = lib + f".tmp{os.getpid()}"
-    cmd = [cc, *GENCODE, "-shared", "-o", tmp, *objs, "-lrt", "-ldl", "-lpthread"]
+    cmd = [cc, *GENCODE, "-shared", "-o", tmp, *objs, "-lrt", "-ldl", "-lpthread", "-Xlinker", "--no-undefined"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

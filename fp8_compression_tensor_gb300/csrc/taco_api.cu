@@ -265,14 +265,14 @@ taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shard
     args.out = static_cast<uint8_t *>(packed_out);
     args.nblocks = n / block;
     args.num_shards = num_shards;
+    // One CTA per tile of blocks; one per SM runs and takes the tiles of CTAs
+    // it cancels before they start.
     const KernelInfo ki = reduce_kernel_info(block);
-    const int64_t threads_needed = args.nblocks * ki.tile_blocks;
-    const int64_t ctas_needed = (threads_needed + ki.threads - 1) / ki.threads;
-    // One pass over the blocks: every thread takes one part of one block.  A
-    // persistent grid (SM count x resident CTAs, looping) measured slower.
-    const int64_t full = INT32_MAX;
-    const int grid = static_cast<int>(ctas_needed < full ? ctas_needed : full);
-    const cudaError_t e = launch_reduce(block, args, grid, reinterpret_cast<cudaStream_t>(stream));
+    const int64_t ntiles = (args.nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
+    if (ntiles > INT32_MAX)
+        return TACO_ERR_BAD_SHAPE;
+    const int grid = static_cast<int>(ntiles);
+    const cudaError_t e = launch_reduce(block, args, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }
 

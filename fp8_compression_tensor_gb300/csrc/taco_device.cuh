@@ -20,6 +20,7 @@ constexpr float kQmax = 448.0f;
 // Fault flag bits written when a kernel gives up waiting.
 constexpr uint32_t kFaultCompress = 1u;
 constexpr uint32_t kFaultDecompress = 2u;
+constexpr uint32_t kFaultReduce = 4u;
 
 // A wait on the copy engine gives up after this long (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

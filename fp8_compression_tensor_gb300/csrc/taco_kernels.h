@@ -12,7 +12,7 @@ struct KernelInfo {
     void *fn = nullptr;     // kernel entry (for attributes and occupancy queries)
     size_t smem = 0;        // dynamic shared memory per CTA
     int threads = 0;        // threads per CTA
-    int tile_blocks = 0;    // blocks per CTA tile; for the shard reduce: threads per block
+    int tile_blocks = 0;    // blocks per CTA tile
     int warps = 0;          // warps per CTA
 };
 
@@ -60,6 +60,8 @@ struct ReduceArgs {
     int num_shards;
 };
 
-cudaError_t launch_reduce(int block, const ReduceArgs &args, int grid, cudaStream_t stream);
+// One CTA per tile of KernelInfo::tile_blocks blocks (tiles of CTAs that have
+// not started are taken over by running ones).
+cudaError_t launch_reduce(int block, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream);
 
 }  // namespace taco

@@ -10,45 +10,62 @@
 // codes Cvt_FP8(Q_max W / max|W|).  The kernel computes exactly these, which
 // differ from decode-sum-encode with explicit rotations only by FP32 rounding.
 //
-// Layout.  B/16 consecutive lanes share a block; each lane owns 16 elements,
-// i.e. 16 bytes of codes per shard (two 8-byte loads: records are 8-byte
-// aligned), so a warp reads whole records.  Energy and maximum are reduced across the block's
-// lanes with xor-shuffles (every lane ends with the same bits).
+// Data movement.  A tile is T consecutive blocks (T = 4096 / B); its records
+// are contiguous in every shard, T * (B + 8) bytes (a multiple of 16: T is
+// even).  A loader thread bulk-copies the tile's P record runs into one stage
+// of a shared-memory ring (as many stages of P runs as fit in kRingBytes) and
+// a group of 8 consumer warps decodes them from shared memory (three groups
+// take turns, so three tiles are decoded at once): B/16 consecutive threads of
+// a group share a block, each owns 16 elements.  Energy and maximum are reduced across
+// the block's threads with xor-shuffles (every thread ends with the same bits),
+// and every thread stores its 16 codes directly (8-byte stores).
+//
+// Scheduling: one CTA per tile, one CTA per SM resident (shared memory); the
+// resident CTA takes its own tile, then the tiles of CTAs it cancels before
+// they start (cluster launch control).
 #include "taco_device.cuh"
 #include "taco_kernels.h"
+#include "taco_tcgen05.cuh"
 
 namespace taco {
 namespace {
 
-#ifndef TACO_REDUCE_PACKED_ADD
-#define TACO_REDUCE_PACKED_ADD 1
+#ifndef TACO_REDUCE_RING_KB
+#define TACO_REDUCE_RING_KB 192
 #endif
-#ifndef TACO_REDUCE_THREADS
-#define TACO_REDUCE_THREADS 128
+#ifndef TACO_REDUCE_GROUPS
+#define TACO_REDUCE_GROUPS 3
 #endif
-#ifndef TACO_REDUCE_BATCH
-#define TACO_REDUCE_BATCH 4
-#endif
-constexpr int kReduceThreads = TACO_REDUCE_THREADS;
-constexpr int kLaneCodes = 16;                  // codes (elements) per lane per shard
-constexpr int kBatch = TACO_REDUCE_BATCH;       // shards whose loads are issued together
+constexpr int kConsumers = 256;                 // threads of a consumer group: 8 warps, 16 elements each
+constexpr int kGroups = TACO_REDUCE_GROUPS;     // consumer groups; group g takes items i % kGroups == g
+constexpr int kRThreads = kGroups * kConsumers + 32;   // + the loader warp
+constexpr int kLaneCodes = 16;                  // codes (elements) per thread per shard
+constexpr int kRingBytes = TACO_REDUCE_RING_KB * 1024;
+constexpr int kMaxStages = 8;
+constexpr int kSched = 16;                      // cluster-launch-control response slots
+constexpr int kSchedAhead = 4;                  // requests kept in flight
+// A response slot is reused kSchedAhead requests after the loader passed the
+// empty barrier of a stage the consumers released up to kMaxStages items earlier.
+static_assert(kSched >= kSchedAhead + kMaxStages + 1, "response slot reused too early");
+static_assert(kSchedAhead >= kGroups, "every consumer group must find the failed response");
 
-// 16 code bytes of a record.  Records start at multiples of B + 8 bytes,
-// which are only 8-byte aligned, so the bytes come in two 8-byte loads.
-__device__ __forceinline__ uint4 ldg_codes16(const uint8_t *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.z), "=r"(v.w) : "l"(p + 8));
-    return v;
-}
-
-__device__ __forceinline__ uint2 ldg_nc_u2(const uint8_t *p)
-{
-    uint2 v;
-    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
+template <int B>
+struct ReduceLayout {
+    static constexpr int kT = kConsumers * kLaneCodes / B;   // blocks per tile
+    static constexpr int kLpb = B / kLaneCodes;             // threads per block
+    static constexpr int kRec = B + 8;
+    static constexpr int kRunBytes = kT * kRec;             // one shard's records of a tile
+    static_assert(kT % 2 == 0 && kRunBytes % 16 == 0, "bulk copies need 16-byte multiples");
+    static_assert(kRingBytes >= 2 * kMaxShards * kRunBytes, "at least two stages at P = 16");
+    // Offsets from the 128-byte aligned base.
+    static constexpr int kOffRing = 0;
+    static constexpr int kOffResp = kOffRing + kRingBytes;            // 16-byte aligned
+    static constexpr int kOffPtrs = kOffResp + 16 * kSched;
+    static constexpr int kOffBar = kOffPtrs + 8 * kMaxShards;
+    static constexpr int kNumBars = 2 * kMaxStages + kSched;
+    static constexpr int kBytes = kOffBar + 8 * kNumBars;
+    static constexpr int kSmem = kBytes + 128;                        // slack for alignment
+};
 
 // w[0..15] += q[0..15] * f for the 16 codes in `c`, each product rounded on its
 // own before the add (so that a shard and its negation cancel exactly, as in
@@ -60,7 +77,6 @@ __device__ __forceinline__ void accumulate_shard(float (&w)[kLaneCodes], uint4 c
     for (int k = 0; k < 4; k++) {
         const float2 q0 = e4m3x2_to_float2(words[k] & 0xffffu);
         const float2 q1 = e4m3x2_to_float2(words[k] >> 16);
-#if TACO_REDUCE_PACKED_ADD
         // Scalar products (never contracted), packed sums.
         const float2 t0 = make_float2(__fmul_rn(q0.x, f), __fmul_rn(q0.y, f));
         const float2 t1 = make_float2(__fmul_rn(q1.x, f), __fmul_rn(q1.y, f));
@@ -70,110 +86,213 @@ __device__ __forceinline__ void accumulate_shard(float (&w)[kLaneCodes], uint4 c
         w[4 * k + 1] = s0.y;
         w[4 * k + 2] = s1.x;
         w[4 * k + 3] = s1.y;
-#else
-        w[4 * k + 0] = __fadd_rn(w[4 * k + 0], __fmul_rn(q0.x, f));
-        w[4 * k + 1] = __fadd_rn(w[4 * k + 1], __fmul_rn(q0.y, f));
-        w[4 * k + 2] = __fadd_rn(w[4 * k + 2], __fmul_rn(q1.x, f));
-        w[4 * k + 3] = __fadd_rn(w[4 * k + 3], __fmul_rn(q1.y, f));
-#endif
     }
 }
 
-template <int B>
-__global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const ReduceArgs args)
+__device__ __forceinline__ uint2 ldg_u2(const uint8_t *p)
 {
-    constexpr int LPB = B / kLaneCodes;   // lanes per block
-    constexpr int kRec = B + 8;
-    const int64_t total = args.nblocks * LPB;
-    const int P = args.num_shards;
+    return *reinterpret_cast<const uint2 *>(p);
+}
+
+template <int B>
+__global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const ReduceArgs args, uint32_t *fault)
+{
+    using Lay = ReduceLayout<B>;
+    constexpr int T = Lay::kT;
+    constexpr int kRec = Lay::kRec;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *base = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
+    const uint32_t sbase = smem_addr(base);
+    const uint32_t bar0 = sbase + Lay::kOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+    auto sched_bar = [&](int q) { return bar0 + 8u * (2 * kMaxStages + q); };
+    const uint32_t resp0 = sbase + Lay::kOffResp;
+    const uint8_t **shard_ptr = reinterpret_cast<const uint8_t **>(base + Lay::kOffPtrs);
+
     grid_launch_dependents();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int P = args.num_shards;
+    const int64_t nblocks = args.nblocks;
+    // Stages of P record runs in the ring.
+    const int stage_bytes = P * Lay::kRunBytes;
+    int nst = kRingBytes / stage_bytes;
+    nst = nst > kMaxStages ? kMaxStages : nst;
+
+    // Work items: item 0 is the CTA's own tile; item j >= 1 is the tile of the
+    // CTA cancelled by request j (slot (j - 1) % kSched), -1 once none is left.
+    auto request_item = [&](int j) {   // loader thread
+        const int q = (j - 1) % kSched;
+        mbar_arrive_expect_tx(sched_bar(q), 16);
+        clc_try_cancel(resp0 + 16u * q, sched_bar(q));
+    };
+    auto item_tile_thread = [&](int j) -> int64_t {
+        if (j == 0)
+            return blockIdx.x;
+        const int q = (j - 1) % kSched;
+        if (!mbar_wait_bounded_thread(sched_bar(q), ((j - 1) / kSched) & 1, fault, kFaultReduce))
+            return -1;
+        return clc_response_ctaid_x(resp0 + 16u * q);
+    };
+    auto item_tile_warp = [&](int j) -> int64_t {
+        if (j == 0)
+            return blockIdx.x;
+        const int q = (j - 1) % kSched;
+        if (!mbar_wait_bounded(sched_bar(q), ((j - 1) / kSched) & 1, fault, kFaultReduce))
+            return -1;
+        return clc_response_ctaid_x(resp0 + 16u * q);
+    };
+    auto tile_valid = [&](int64_t t) {
+        const int64_t left = nblocks - t * T;
+        return static_cast<int>(left < T ? left : T);
+    };
+
+    // ---- set-up ----------------------------------------------------------
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMaxStages; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kConsumers / 32);
+        }
+        for (int q = 0; q < kSched; q++)
+            mbar_init(sched_bar(q), 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < kMaxShards)
+        shard_ptr[threadIdx.x] = args.shards[threadIdx.x];
     grid_dependency_wait();   // the shards may come from the previous kernel
+    cta_barrier();
 
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-         g - (threadIdx.x & 31) < total;  // whole warps iterate together
-         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const bool active = g < total;
-        const int64_t k = active ? g / LPB : 0;
-        const int part = static_cast<int>(g % LPB);
-        const int64_t off = k * kRec;
+    if (warp == kGroups * kConsumers / 32) {
+        // ---- loader --------------------------------------------------------
+        if (lane == 0) {
+            auto issue_tile = [&](int i, int64_t t) {
+                const int s = i % nst;
+                const int nvalid = tile_valid(t);
+                const uint32_t run = static_cast<uint32_t>(nvalid & ~1) * kRec;   // multiple of 16
+                mbar_arrive_expect_tx(full_bar(s), run * static_cast<uint32_t>(P));
+                if (run > 0) {
+                    const uint32_t dst = sbase + Lay::kOffRing + s * stage_bytes;
+                    for (int p = 0; p < P; p++)
+                        bulk_load(dst + p * Lay::kRunBytes, shard_ptr[p] + t * T * kRec, run, full_bar(s));
+                }
+            };
+            for (int j = 1; j <= kSchedAhead; j++)
+                request_item(j);
+            issue_tile(0, blockIdx.x);
+            int i = 1;                       // items 0 .. i-1 have been loaded
+            int requested = kSchedAhead;     // requests 1 .. requested issued
+            for (;; i++) {
+                const int64_t t = item_tile_thread(i);
+                if (t < 0)
+                    break;
+                request_item(++requested);   // no failure seen yet: keep kSchedAhead in flight
+                const int s = i % nst;
+                if (i >= nst && !mbar_wait_bounded_thread(empty_bar(s), ((i / nst) - 1) & 1, fault, kFaultReduce))
+                    break;
+                issue_tile(i, t);
+            }
+            // Responses still in flight and copies this thread issued must
+            // land before the CTA can exit.
+            for (int j = i; j <= requested; j++)
+                mbar_wait_bounded_thread(sched_bar((j - 1) % kSched), ((j - 1) / kSched) & 1, fault, kFaultReduce);
+            for (int j = i - nst > 0 ? i - nst : 0; j < i; j++)
+                mbar_wait_bounded_thread(full_bar(j % nst), (j / nst) & 1, fault, kFaultReduce);
+        }
+    } else {
+        // ---- consumers: 16 elements of one block per thread -----------------
+        const int grp = threadIdx.x / kConsumers;
+        const int c = threadIdx.x % kConsumers;
+        const int bl = c / Lay::kLpb;        // block within the tile
+        const int part = c % Lay::kLpb;      // 16-element part of the block
+        for (int i = grp;; i += kGroups) {
+            const int64_t t = item_tile_warp(i);
+            if (t < 0)
+                break;
+            const int s = i % nst;
+            if (!mbar_wait_bounded(full_bar(s), (i / nst) & 1, fault, kFaultReduce))
+                break;
+            const int nvalid = tile_valid(t);
+            const bool active = bl < nvalid;
+            const bool from_global = (nvalid & 1) && bl == nvalid - 1;   // not in the bulk copies
+            const int64_t blk = t * T + bl;
+            const uint32_t rec_s = sbase + Lay::kOffRing + s * stage_bytes + bl * kRec;
 
-        float w[kLaneCodes];
+            // W = sum_p q_p * (s_p / alpha_p) in shard order.
+            float w[kLaneCodes];
 #pragma unroll
-        for (int i = 0; i < kLaneCodes; i++)
-            w[i] = 0.f;
-
-        // W = sum_p q_p * (s_p / alpha_p) in shard order, the loads of up to
-        // kBatch shards in flight at a time.  The shard loop is unrolled to
-        // the maximum shard count so every shard pointer is a fixed kernel
-        // parameter (no indexed parameter access).
-#pragma unroll
-        for (int p0 = 0; p0 < kMaxShards; p0 += kBatch) {
-            if (p0 < P) {
-                uint4 codes[kBatch];
-                uint2 meta[kBatch];
-#pragma unroll
-                for (int i = 0; i < kBatch; i++) {
-                    if (p0 + i < P && active) {
-                        const uint8_t *rec = args.shards[p0 + i] + off;
-                        codes[i] = ldg_codes16(rec + kLaneCodes * part);
-                        meta[i] = ldg_nc_u2(rec + B);
+            for (int k = 0; k < kLaneCodes; k++)
+                w[k] = 0.f;
+            if (active) {
+                for (int p = 0; p < P; p++) {
+                    uint4 codes;
+                    uint2 meta;
+                    if (!from_global) {
+                        const uint32_t r = rec_s + p * Lay::kRunBytes;
+                        const uint2 a = lds64(r + kLaneCodes * part);
+                        const uint2 b = lds64(r + kLaneCodes * part + 8);
+                        codes = make_uint4(a.x, a.y, b.x, b.y);
+                        meta = lds64(r + B);
                     } else {
-                        codes[i] = make_uint4(0u, 0u, 0u, 0u);
-                        meta[i] = make_uint2(0x3f800000u, 0u);  // alpha = 1, s = 0
+                        const uint8_t *r = shard_ptr[p] + blk * kRec;
+                        const uint2 a = ldg_u2(r + kLaneCodes * part);
+                        const uint2 b = ldg_u2(r + kLaneCodes * part + 8);
+                        codes = make_uint4(a.x, a.y, b.x, b.y);
+                        meta = ldg_u2(r + B);
                     }
-                }
-#pragma unroll
-                for (int i = 0; i < kBatch; i++) {
-                    if (p0 + i < P) {
-                        // s_p / alpha_p (within 2 ulp; alpha_p <= 1e15 is far from
-                        // the range where the fast quotient underflows).
-                        const float f = __fdividef(__uint_as_float(meta[i].y), __uint_as_float(meta[i].x));
-                        accumulate_shard(w, codes[i], f);
-                    }
+                    // s_p / alpha_p (within 2 ulp; alpha_p <= 1e15 is far from
+                    // the range where the fast quotient underflows).
+                    const float f = __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x));
+                    accumulate_shard(w, codes, f);
                 }
             }
-        }
+            // The stage is read: hand it back to the loader.
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty_bar(s));
 
-        // Energy |W|^2 and max|W| over the block's lanes.
-        float2 e2 = make_float2(0.f, 0.f);
-        float wmax = 0.f;
+            // Energy |W|^2 and max|W| over the block's threads.
+            float2 e2 = make_float2(0.f, 0.f);
+            float wmax = 0.f;
 #pragma unroll
-        for (int i = 0; i < kLaneCodes; i += 2) {
-            const float2 wi = make_float2(w[i], w[i + 1]);
-            e2 = fma2(wi, wi, e2);
-            wmax = max3(wmax, fabsf(w[i]), fabsf(w[i + 1]));
-        }
-        float e = e2.x + e2.y;
-#pragma unroll
-        for (int d = 1; d < LPB; d <<= 1) {
-            e = e + __shfl_xor_sync(kFullMask, e, d);
-            wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, d));
-        }
-
-        const float m = e * (1.0f / B);
-        const float alpha = __fdiv_rn(kTau, __fsqrt_rn(m + kEps));
-        float s = 0.f;
-        uint4 out = make_uint4(0u, 0u, 0u, 0u);
-        if (wmax > 0.f) {
-            s = __fdiv_rn(__fmul_rn(alpha, wmax), kQmax);
-            const float kq = __fdiv_rn(kQmax, wmax);
-            const float2 k2 = make_float2(kq, kq);
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const float2 u0 = mul2(make_float2(w[4 * j], w[4 * j + 1]), k2);
-                const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
-                o[j] = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
+            for (int k = 0; k < kLaneCodes; k += 2) {
+                const float2 wi = make_float2(w[k], w[k + 1]);
+                e2 = fma2(wi, wi, e2);
+                wmax = max3(wmax, fabsf(w[k]), fabsf(w[k + 1]));
             }
-            out = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (active) {
-            uint8_t *rec = args.out + off;
-            // Records are 8-byte aligned: two 8-byte stores per lane.
-            *reinterpret_cast<uint2 *>(rec + kLaneCodes * part) = make_uint2(out.x, out.y);
-            *reinterpret_cast<uint2 *>(rec + kLaneCodes * part + 8) = make_uint2(out.z, out.w);
-            if (part == 0)
-                *reinterpret_cast<uint2 *>(rec + B) = make_uint2(__float_as_uint(alpha), __float_as_uint(s));
+            float e = e2.x + e2.y;
+#pragma unroll
+            for (int d = 1; d < Lay::kLpb; d <<= 1) {
+                e = e + __shfl_xor_sync(kFullMask, e, d);
+                wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, d));
+            }
+
+            const float m = e * (1.0f / B);
+            const float alpha = __fdiv_rn(kTau, __fsqrt_rn(m + kEps));
+            float sc = 0.f;
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (wmax > 0.f) {
+                sc = __fdiv_rn(__fmul_rn(alpha, wmax), kQmax);
+                const float kq = __fdiv_rn(kQmax, wmax);
+                const float2 k2 = make_float2(kq, kq);
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float2 u0 = mul2(make_float2(w[4 * j], w[4 * j + 1]), k2);
+                    const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
+                    o[j] = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
+                }
+                out = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (active) {
+                uint8_t *rec = args.out + blk * kRec;
+                // Records are 8-byte aligned: two 8-byte stores per thread.
+                *reinterpret_cast<uint2 *>(rec + kLaneCodes * part) = make_uint2(out.x, out.y);
+                *reinterpret_cast<uint2 *>(rec + kLaneCodes * part + 8) = make_uint2(out.z, out.w);
+                if (part == 0)
+                    *reinterpret_cast<uint2 *>(rec + B) = make_uint2(__float_as_uint(alpha), __float_as_uint(sc));
+            }
         }
     }
 }
@@ -181,8 +300,8 @@ __global__ void __launch_bounds__(kReduceThreads) taco_shard_reduce_kernel(const
 template <int B>
 KernelInfo info()
 {
-    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B>), 0, kReduceThreads, B / kLaneCodes,
-                      kReduceThreads / 32};
+    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B>), ReduceLayout<B>::kSmem, kRThreads,
+                      ReduceLayout<B>::kT, kRThreads / 32};
 }
 
 }  // namespace
@@ -197,14 +316,14 @@ KernelInfo reduce_kernel_info(int block)
     }
 }
 
-cudaError_t launch_reduce(int block, const ReduceArgs &args, int grid, cudaStream_t stream)
+cudaError_t launch_reduce(int block, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream)
 {
     const KernelInfo ki = reduce_kernel_info(block);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     ReduceArgs a = args;
-    void *params[] = {&a};
-    return launch_kernel(ki.fn, grid, ki.threads, 0, stream, params);
+    void *params[] = {&a, &fault};
+    return launch_kernel(ki.fn, grid, ki.threads, ki.smem, stream, params);
 }
 
 }  // namespace taco

@@ -120,7 +120,8 @@ TACO_API taco_status_t taco_reduce_shards(const void *const *packed_shards, int 
 
 /*
  * Synchronises `stream`, then reads and clears the current device's fault
- * flags (bit 0: compress, bit 1: decompress gave up waiting for a copy).
+ * flags (bit 0: compress, bit 1: decompress, bit 2: shard reduce gave up
+ * waiting for a copy or a tile assignment).
  * *flags_out (may be NULL) receives them.  Returns TACO_ERR_DEVICE_FAULT if any
  * flag was set, TACO_ERR_CUDA if a CUDA call failed, TACO_OK otherwise.
  */
