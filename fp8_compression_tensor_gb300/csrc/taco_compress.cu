@@ -8,11 +8,10 @@
 // and the tensor core accumulates in FP32, so Y is the unnormalised rotation
 // of Eq. (8) up to FP32 summation order.
 //
-// Scheduling: the grid has one CTA per tile of 128 blocks, and shared memory
-// admits one CTA per SM.  A running CTA takes its own tile, then claims the
-// tiles of CTAs that have not started yet by cancelling them (cluster launch
-// control), so CTAs that get more memory bandwidth take more tiles and all
-// SMs finish together.
+// Scheduling: one CTA per tile of 128 blocks, one CTA per SM resident; a
+// running CTA takes its own tile, then the tiles of CTAs it cancels before
+// they start (cluster launch control, taco_sched.cuh), so CTAs that get more
+// memory bandwidth take more tiles and all SMs finish together.
 //
 // Roles in a CTA, one tile at a time:
 //   warp 0  TMA producer: 2-D tiled loads (128-byte swizzle) of the tile into a
@@ -40,6 +39,7 @@
 
 #include "taco_device.cuh"
 #include "taco_kernels.h"
+#include "taco_sched.cuh"
 #include "taco_tcgen05.cuh"
 
 namespace taco {
@@ -72,17 +72,15 @@ struct TcCompressLayout {
     static constexpr int kOffA = 0;
     static constexpr int kOffH = kOffA + STAGES * kStageBytes;
     static constexpr int kOffOut = kOffH + kHBytes;
-    // Tile scheduling: ring of kSched 16-byte cluster-launch-control
-    // responses, kSchedAhead requests in flight.  A slot is reused only after
-    // the producer has passed the empty barrier kSchedAhead + STAGES + 3
-    // tiles later, when the MMA issuer and both epilogue groups have read it.
-    static constexpr int kSched = 16;
-    static constexpr int kSchedAhead = 4;
-    static_assert(kSched >= kSchedAhead + STAGES + 3, "response slot reused too early");
-    static_assert(kSchedAhead >= EPG, "every epilogue group must find the failed response");
-    static constexpr int kOffResp = kOffOut + NOUT * kOutBytes;    // 16-byte aligned
-    static constexpr int kOffBar = kOffResp + 16 * kSched;         // 8-byte aligned
-    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * NOUT + kSched;
+    // Tile scheduler.  The producer publishes item i after the empty barrier
+    // of item i - STAGES, when the epilogues have read items up to
+    // i - STAGES - 2: a published-tile slot (and the end marks of EPG items)
+    // is reused only after every reader is done with it.
+    static_assert(kTileRing >= STAGES + EPG + 2, "published-tile slot reused too early");
+    static constexpr int kOffSched = kOffOut + NOUT * kOutBytes;   // 16-byte aligned
+    static_assert(kOffSched % 16 == 0, "cancel responses need 16-byte alignment");
+    static constexpr int kOffBar = kOffSched + kSchedBytes;        // 8-byte aligned
+    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * NOUT;
     static constexpr int kOffTmem = kOffBar + 8 * kNumBars;
     static constexpr int kBytes = kOffTmem + 16;
     static constexpr int kSmem = kBytes + 1024;                    // slack for 1024-byte alignment
@@ -131,40 +129,12 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     auto acc_empty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     auto out_free_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
     auto rec_done_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + NOUT + b); };
-    auto sched_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 4 + 2 * NOUT + q); };
-    const uint32_t resp0 = sbase + Lay::kOffResp;
+    const TileSched sched{sbase + Lay::kOffSched, fault, kFaultCompress};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
     grid_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // Work items.  The grid has one CTA per tile; a running CTA takes item 0
-    // = its own tile, then cancels CTAs that have not started and takes their
-    // tiles (request j answers item j, in slot (j - 1) % kSched), until a
-    // request fails because none is left.  Faster CTAs so take more tiles.
-    auto request_item = [&](int j) {   // producer thread
-        const int q = (j - 1) % Lay::kSched;
-        mbar_arrive_expect_tx(sched_bar(q), 16);
-        clc_try_cancel(resp0 + 16u * q, sched_bar(q));
-    };
-    // Tile of item j, or -1 when none was left (or the wait timed out).
-    auto item_tile_thread = [&](int j) -> int64_t {
-        if (j == 0)
-            return blockIdx.x;
-        const int q = (j - 1) % Lay::kSched;
-        if (!mbar_wait_bounded_thread(sched_bar(q), ((j - 1) / Lay::kSched) & 1, fault, kFaultCompress))
-            return -1;
-        return clc_response_ctaid_x(resp0 + 16u * q);
-    };
-    auto item_tile_warp = [&](int j) -> int64_t {
-        if (j == 0)
-            return blockIdx.x;
-        const int q = (j - 1) % Lay::kSched;
-        if (!mbar_wait_bounded(sched_bar(q), ((j - 1) / Lay::kSched) & 1, fault, kFaultCompress))
-            return -1;
-        return clc_response_ctaid_x(resp0 + 16u * q);
-    };
 
     // ---- set-up ----------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -180,13 +150,12 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             mbar_init(out_free_bar(b), 1);
             mbar_init(rec_done_bar(b), kEpiThreads);
         }
-        for (int q = 0; q < Lay::kSched; q++)
-            mbar_init(sched_bar(q), 1);
+        sched.init();
         fence_mbar_init();
         prefetch_tmap(&tmap_x);
     }
-    // The producer (thread 0) starts its own tile's load and the first
-    // kSchedAhead tile requests before the rest of the set-up.
+    // The producer (thread 0) sends the first kSchedAhead tile requests and
+    // starts its own tile's load (item 0) before the rest of the set-up.
     auto issue_tile = [&](int i, int64_t t) {
         const int s = i % STAGES;
         mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
@@ -196,9 +165,10 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             tma_load_2d(dst + c * Lay::kChunkBytesA, &tmap_x, 64 * c, static_cast<int32_t>(t * kTcRows), full_bar(s));
     };
     if (threadIdx.x == 0) {
-        for (int j = 1; j <= Lay::kSchedAhead; j++)
-            request_item(j);
+        for (int j = 1; j <= kSchedAhead; j++)
+            sched.request(j);
         grid_dependency_wait();   // the input may come from the previous kernel
+        sched.publish(0, blockIdx.x);
         issue_tile(0, blockIdx.x);
     }
     if (warp == 1)
@@ -215,23 +185,26 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
         // ---- TMA producer ------------------------------------------------
         if (lane == 0) {
             int i = 1;                           // items 0 .. i-1 have been loaded
-            int requested = Lay::kSchedAhead;    // requests 1 .. requested issued
+            int requested = kSchedAhead;         // requests 1 .. requested issued
             for (;; i++) {
-                const int64_t t = item_tile_thread(i);
-                if (t < 0)
+                const int64_t t = sched.response(i);
+                if (t < 0) {
+                    sched.publish_end(i, EPG);
                     break;
-                request_item(++requested);       // no failure seen yet: keep kSchedAhead in flight
+                }
+                sched.request(++requested);      // no failure seen yet: keep kSchedAhead in flight
                 const int s = i % STAGES;
                 if (i >= STAGES &&
-                    !mbar_wait_bounded_thread(empty_bar(s), ((i / STAGES) - 1) & 1, fault, kFaultCompress))
+                    !mbar_wait_bounded_thread(empty_bar(s), ((i / STAGES) - 1) & 1, fault, kFaultCompress)) {
+                    sched.publish_end(i, EPG);
                     break;
+                }
+                sched.publish(i, t);
                 issue_tile(i, t);
             }
             // Responses still in flight and copies this thread issued must
             // land before the CTA can exit.
-            for (int j = i; j <= requested; j++)
-                mbar_wait_bounded_thread(sched_bar((j - 1) % Lay::kSched), ((j - 1) / Lay::kSched) & 1, fault,
-                                         kFaultCompress);
+            sched.drain(i, requested);
             const int issued = i;
             for (int j = issued - STAGES > 0 ? issued - STAGES : 0; j < issued; j++)
                 mbar_wait_bounded_thread(full_bar(j % STAGES), (j / STAGES) & 1, fault, kFaultCompress);
@@ -243,7 +216,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             const uint32_t a0 = sbase + Lay::kOffA, h0 = sbase + Lay::kOffH;
             int i = 0;
             for (;; i++) {
-                if (item_tile_thread(i) < 0)
+                if (sched.tile_thread(i) < 0)
                     break;
                 const int s = i % STAGES, acc = i & 1;
                 if (i >= 2 && !mbar_wait_bounded_thread(acc_empty_bar(acc), ((i >> 1) - 1) & 1, fault,
@@ -300,7 +273,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
         const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
         for (int kt = 0;; kt++) {                   // kt: tiles this group has handled
             const int i = EPG * kt + grp;               // the CTA's item counter
-            const int64_t t = item_tile_warp(i);
+            const int64_t t = sched.tile_warp(i);
             if (t < 0)
                 break;
             const int acc = i & 1;

@@ -10,7 +10,7 @@
 //
 // Scheduling: one CTA per tile, one CTA per SM resident (shared memory); a
 // running CTA takes its own tile, then the tiles of CTAs it cancels before
-// they start (cluster launch control), so faster CTAs take more tiles.
+// they start (cluster launch control, taco_sched.cuh).
 //
 // Roles in a CTA:
 //   warp 0    bulk-copies each tile of records (contiguous, B + 8 bytes each)
@@ -33,6 +33,7 @@
 
 #include "taco_device.cuh"
 #include "taco_kernels.h"
+#include "taco_sched.cuh"
 #include "taco_tcgen05.cuh"
 
 namespace taco {
@@ -66,16 +67,15 @@ struct TcDecompressLayout {
     static constexpr int kOffOut = kOffH + kHBytes;
     static constexpr int kOffRaw = kOffOut + NOUT * kOutBytes;
     static constexpr int kOffFac = kOffRaw + RS * kRawBytes;      // 16-byte aligned (kRawBytes % 16 == 0)
-    // Tile scheduling: ring of kSched cluster-launch-control responses,
-    // kSchedAhead requests in flight.  A slot is reused only after the loader
-    // has passed the raw-stage barrier kSchedAhead + RS + AS + 3 tiles later,
-    // when the transposers, the MMA issuer and the epilogue have read it.
-    static constexpr int kSched = 16;
-    static constexpr int kSchedAhead = 4;
-    static_assert(kSched >= kSchedAhead + RS + AS + 3, "response slot reused too early");
-    static constexpr int kOffResp = kOffFac + FS * kTileBlocks * 4;   // 16-byte aligned
-    static constexpr int kOffBar = kOffResp + 16 * kSched;
-    static constexpr int kNumBars = 2 * RS + 2 * AS + 4 + 2 * NOUT + FS + kSched;
+    // Tile scheduler.  The loader publishes item i after the raw-stage
+    // barrier of item i - RS, when the epilogue has read items up to
+    // i - RS - AS - 2: a published-tile slot is reused only after every
+    // reader is done with it.
+    static_assert(kTileRing >= RS + AS + 3, "published-tile slot reused too early");
+    static constexpr int kOffSched = kOffFac + FS * kTileBlocks * 4;   // 16-byte aligned
+    static_assert(kOffSched % 16 == 0, "cancel responses need 16-byte alignment");
+    static constexpr int kOffBar = kOffSched + kSchedBytes;
+    static constexpr int kNumBars = 2 * RS + 2 * AS + 4 + 2 * NOUT + FS;
     static constexpr int kOffTmem = kOffBar + 8 * kNumBars;
     static constexpr int kBytes = kOffTmem + 16;
     static constexpr int kSmem = kBytes + 1024;
@@ -130,38 +130,13 @@ __global__ void __launch_bounds__(kDThreads, 1)
     auto out_free = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + b); };
     auto out_done = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + NOUT + b); };
     auto fac_full = [&](int f) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + 2 * NOUT + f); };
-    auto sched_bar = [&](int q) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + 2 * NOUT + FS + q); };
-    const uint32_t resp0 = sbase + Lay::kOffResp;
+    const TileSched sched{sbase + Lay::kOffSched, fault, kFaultDecompress};
     float *factors = reinterpret_cast<float *>(base + Lay::kOffFac);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
     grid_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // Work items: item 0 is the CTA's own tile; item j >= 1 is the tile of the
-    // CTA cancelled by request j (slot (j - 1) % kSched), -1 once none is left.
-    auto request_item = [&](int j) {   // loader thread
-        const int q = (j - 1) % Lay::kSched;
-        mbar_arrive_expect_tx(sched_bar(q), 16);
-        clc_try_cancel(resp0 + 16u * q, sched_bar(q));
-    };
-    auto item_tile_thread = [&](int j) -> int64_t {
-        if (j == 0)
-            return blockIdx.x;
-        const int q = (j - 1) % Lay::kSched;
-        if (!mbar_wait_bounded_thread(sched_bar(q), ((j - 1) / Lay::kSched) & 1, fault, kFaultDecompress))
-            return -1;
-        return clc_response_ctaid_x(resp0 + 16u * q);
-    };
-    auto item_tile_warp = [&](int j) -> int64_t {
-        if (j == 0)
-            return blockIdx.x;
-        const int q = (j - 1) % Lay::kSched;
-        if (!mbar_wait_bounded(sched_bar(q), ((j - 1) / Lay::kSched) & 1, fault, kFaultDecompress))
-            return -1;
-        return clc_response_ctaid_x(resp0 + 16u * q);
-    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < RS; s++) {
@@ -182,13 +157,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         for (int f = 0; f < FS; f++)
             mbar_init(fac_full(f), kGroup / 32);
-        for (int q = 0; q < Lay::kSched; q++)
-            mbar_init(sched_bar(q), 1);
+        sched.init();
         fence_mbar_init();
         prefetch_tmap(&tmap_y);
     }
-    // The loader (thread 0) starts its own tile's record copy and the first
-    // kSchedAhead tile requests before the rest of the set-up.
+    // The loader (thread 0) sends the first kSchedAhead tile requests and
+    // starts its own tile's record copy (item 0) before the rest of the set-up.
     auto issue_tile = [&](int i, int64_t t) {
         const int s = i % RS;
         const int64_t blk0 = t * Lay::kTileBlocks;
@@ -199,9 +173,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
             bulk_load(sbase + Lay::kOffRaw + s * Lay::kRawBytes, packed + blk0 * Lay::kRec, bytes, raw_full(s));
     };
     if (threadIdx.x == 0) {
-        for (int j = 1; j <= Lay::kSchedAhead; j++)
-            request_item(j);
+        for (int j = 1; j <= kSchedAhead; j++)
+            sched.request(j);
         grid_dependency_wait();   // the input may come from the previous kernel
+        sched.publish(0, blockIdx.x);
         issue_tile(0, blockIdx.x);
     }
     if (warp == 1)
@@ -218,22 +193,25 @@ __global__ void __launch_bounds__(kDThreads, 1)
         // ---- record loader ----------------------------------------------
         if (lane == 0) {
             int i = 1;                           // items 0 .. i-1 have been loaded
-            int requested = Lay::kSchedAhead;    // requests 1 .. requested issued
+            int requested = kSchedAhead;         // requests 1 .. requested issued
             for (;; i++) {
-                const int64_t t = item_tile_thread(i);
-                if (t < 0)
+                const int64_t t = sched.response(i);
+                if (t < 0) {
+                    sched.publish_end(i, 1);
                     break;
-                request_item(++requested);       // no failure seen yet: keep kSchedAhead in flight
+                }
+                sched.request(++requested);      // no failure seen yet: keep kSchedAhead in flight
                 const int s = i % RS;
-                if (i >= RS && !mbar_wait_bounded_thread(raw_empty(s), ((i / RS) - 1) & 1, fault, kFaultDecompress))
+                if (i >= RS && !mbar_wait_bounded_thread(raw_empty(s), ((i / RS) - 1) & 1, fault, kFaultDecompress)) {
+                    sched.publish_end(i, 1);
                     break;
+                }
+                sched.publish(i, t);
                 issue_tile(i, t);
             }
             // Responses still in flight and copies this thread issued must
             // land before the CTA can exit.
-            for (int j = i; j <= requested; j++)
-                mbar_wait_bounded_thread(sched_bar((j - 1) % Lay::kSched), ((j - 1) / Lay::kSched) & 1, fault,
-                                         kFaultDecompress);
+            sched.drain(i, requested);
             const int issued = i;
             for (int j = issued - RS > 0 ? issued - RS : 0; j < issued; j++)
                 mbar_wait_bounded_thread(raw_full(j % RS), (j / RS) & 1, fault, kFaultDecompress);
@@ -245,7 +223,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
             const uint32_t h0 = sbase + Lay::kOffH;
             int i = 0;
             for (;; i++) {
-                if (item_tile_thread(i) < 0)
+                if (sched.tile_thread(i) < 0)
                     break;
                 const int j = i % AS, acc = i & 1;
                 if (i >= 2 &&
@@ -280,7 +258,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const int m = threadIdx.x - 64;    // 0..127
         const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
         for (int i = 0;; i++) {
-            const int64_t t = item_tile_warp(i);
+            const int64_t t = sched.tile_warp(i);
             if (t < 0)
                 break;
             const int s = i % RS, j = i % AS, fs = i % FS;
@@ -338,7 +316,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const int q = warp & 3;
         const int m = 32 * q + lane;               // accumulator row
         for (int i = 0;; i++) {
-            const int64_t t = item_tile_warp(i);
+            const int64_t t = sched.tile_warp(i);
             if (t < 0)
                 break;
             const int acc = i & 1, fs = i % FS, ob = i % NOUT;

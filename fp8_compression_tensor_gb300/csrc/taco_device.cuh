@@ -66,15 +66,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+#ifndef TACO_WAIT_HINT_NS
+#define TACO_WAIT_HINT_NS 1000000
+#endif
+
+// Tests phase `parity` of the barrier; if it is not complete, the thread may
+// be suspended (instead of spinning) until it completes or about
+// TACO_WAIT_HINT_NS nanoseconds pass.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(TACO_WAIT_HINT_NS)
         : "memory");
     return ok != 0;
 }

@@ -22,9 +22,13 @@
 //
 // Scheduling: one CTA per tile, one CTA per SM resident (shared memory); the
 // resident CTA takes its own tile, then the tiles of CTAs it cancels before
-// they start (cluster launch control).
+// they start (cluster launch control, taco_sched.cuh).  The loader publishes a
+// tile to the consumers only when it issues its copies, after the stage's
+// previous item was released, so the consumer groups, which take turns on the
+// stages, never see an older phase of a stage barrier as the one they wait for.
 #include "taco_device.cuh"
 #include "taco_kernels.h"
+#include "taco_sched.cuh"
 #include "taco_tcgen05.cuh"
 
 namespace taco {
@@ -32,6 +36,9 @@ namespace {
 
 #ifndef TACO_REDUCE_RING_KB
 #define TACO_REDUCE_RING_KB 192
+#endif
+#ifndef TACO_REDUCE_UNROLL2
+#define TACO_REDUCE_UNROLL2 0
 #endif
 #ifndef TACO_REDUCE_GROUPS
 #define TACO_REDUCE_GROUPS 3
@@ -42,12 +49,10 @@ constexpr int kRThreads = kGroups * kConsumers + 32;   // + the loader warp
 constexpr int kLaneCodes = 16;                  // codes (elements) per thread per shard
 constexpr int kRingBytes = TACO_REDUCE_RING_KB * 1024;
 constexpr int kMaxStages = 8;
-constexpr int kSched = 16;                      // cluster-launch-control response slots
-constexpr int kSchedAhead = 4;                  // requests kept in flight
-// A response slot is reused kSchedAhead requests after the loader passed the
-// empty barrier of a stage the consumers released up to kMaxStages items earlier.
-static_assert(kSched >= kSchedAhead + kMaxStages + 1, "response slot reused too early");
-static_assert(kSchedAhead >= kGroups, "every consumer group must find the failed response");
+// The loader publishes item i after the empty barrier of item i - nst, when
+// the consumers have read every item up to i - nst: a published-tile slot
+// (and the end marks of kGroups items) is reused only after its readers are done.
+static_assert(kTileRing >= kMaxStages + kGroups, "published-tile slot reused too early");
 
 template <int B>
 struct ReduceLayout {
@@ -59,10 +64,10 @@ struct ReduceLayout {
     static_assert(kRingBytes >= 2 * kMaxShards * kRunBytes, "at least two stages at P = 16");
     // Offsets from the 128-byte aligned base.
     static constexpr int kOffRing = 0;
-    static constexpr int kOffResp = kOffRing + kRingBytes;            // 16-byte aligned
-    static constexpr int kOffPtrs = kOffResp + 16 * kSched;
+    static constexpr int kOffSched = kOffRing + kRingBytes;           // 16-byte aligned
+    static constexpr int kOffPtrs = kOffSched + kSchedBytes;
     static constexpr int kOffBar = kOffPtrs + 8 * kMaxShards;
-    static constexpr int kNumBars = 2 * kMaxStages + kSched;
+    static constexpr int kNumBars = 2 * kMaxStages;
     static constexpr int kBytes = kOffBar + 8 * kNumBars;
     static constexpr int kSmem = kBytes + 128;                        // slack for alignment
 };
@@ -107,8 +112,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     const uint32_t bar0 = sbase + Lay::kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
-    auto sched_bar = [&](int q) { return bar0 + 8u * (2 * kMaxStages + q); };
-    const uint32_t resp0 = sbase + Lay::kOffResp;
+    const TileSched sched{sbase + Lay::kOffSched, fault, kFaultReduce};
     const uint8_t **shard_ptr = reinterpret_cast<const uint8_t **>(base + Lay::kOffPtrs);
 
     grid_launch_dependents();
@@ -121,29 +125,6 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     int nst = kRingBytes / stage_bytes;
     nst = nst > kMaxStages ? kMaxStages : nst;
 
-    // Work items: item 0 is the CTA's own tile; item j >= 1 is the tile of the
-    // CTA cancelled by request j (slot (j - 1) % kSched), -1 once none is left.
-    auto request_item = [&](int j) {   // loader thread
-        const int q = (j - 1) % kSched;
-        mbar_arrive_expect_tx(sched_bar(q), 16);
-        clc_try_cancel(resp0 + 16u * q, sched_bar(q));
-    };
-    auto item_tile_thread = [&](int j) -> int64_t {
-        if (j == 0)
-            return blockIdx.x;
-        const int q = (j - 1) % kSched;
-        if (!mbar_wait_bounded_thread(sched_bar(q), ((j - 1) / kSched) & 1, fault, kFaultReduce))
-            return -1;
-        return clc_response_ctaid_x(resp0 + 16u * q);
-    };
-    auto item_tile_warp = [&](int j) -> int64_t {
-        if (j == 0)
-            return blockIdx.x;
-        const int q = (j - 1) % kSched;
-        if (!mbar_wait_bounded(sched_bar(q), ((j - 1) / kSched) & 1, fault, kFaultReduce))
-            return -1;
-        return clc_response_ctaid_x(resp0 + 16u * q);
-    };
     auto tile_valid = [&](int64_t t) {
         const int64_t left = nblocks - t * T;
         return static_cast<int>(left < T ? left : T);
@@ -155,8 +136,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), kConsumers / 32);
         }
-        for (int q = 0; q < kSched; q++)
-            mbar_init(sched_bar(q), 1);
+        sched.init();
         fence_mbar_init();
     }
     if (threadIdx.x < kMaxShards)
@@ -179,24 +159,29 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                 }
             };
             for (int j = 1; j <= kSchedAhead; j++)
-                request_item(j);
+                sched.request(j);
+            sched.publish(0, blockIdx.x);
             issue_tile(0, blockIdx.x);
             int i = 1;                       // items 0 .. i-1 have been loaded
             int requested = kSchedAhead;     // requests 1 .. requested issued
             for (;; i++) {
-                const int64_t t = item_tile_thread(i);
-                if (t < 0)
+                const int64_t t = sched.response(i);
+                if (t < 0) {
+                    sched.publish_end(i, kGroups);
                     break;
-                request_item(++requested);   // no failure seen yet: keep kSchedAhead in flight
+                }
+                sched.request(++requested);  // no failure seen yet: keep kSchedAhead in flight
                 const int s = i % nst;
-                if (i >= nst && !mbar_wait_bounded_thread(empty_bar(s), ((i / nst) - 1) & 1, fault, kFaultReduce))
+                if (i >= nst && !mbar_wait_bounded_thread(empty_bar(s), ((i / nst) - 1) & 1, fault, kFaultReduce)) {
+                    sched.publish_end(i, kGroups);
                     break;
+                }
+                sched.publish(i, t);
                 issue_tile(i, t);
             }
             // Responses still in flight and copies this thread issued must
             // land before the CTA can exit.
-            for (int j = i; j <= requested; j++)
-                mbar_wait_bounded_thread(sched_bar((j - 1) % kSched), ((j - 1) / kSched) & 1, fault, kFaultReduce);
+            sched.drain(i, requested);
             for (int j = i - nst > 0 ? i - nst : 0; j < i; j++)
                 mbar_wait_bounded_thread(full_bar(j % nst), (j / nst) & 1, fault, kFaultReduce);
         }
@@ -207,7 +192,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
         const int bl = c / Lay::kLpb;        // block within the tile
         const int part = c % Lay::kLpb;      // 16-element part of the block
         for (int i = grp;; i += kGroups) {
-            const int64_t t = item_tile_warp(i);
+            const int64_t t = sched.tile_warp(i);
             if (t < 0)
                 break;
             const int s = i % nst;
@@ -224,27 +209,41 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
 #pragma unroll
             for (int k = 0; k < kLaneCodes; k++)
                 w[k] = 0.f;
-            if (active) {
+            // s_p / alpha_p below is within 2 ulp (alpha_p <= 1e15 is far from
+            // the range where the fast quotient underflows).
+            if (active && !from_global) {
+                const uint32_t r0 = rec_s + kLaneCodes * part;
+#if TACO_REDUCE_UNROLL2
+                int p = 0;
+                for (; p + 2 <= P; p += 2) {
+                    const uint32_t r = r0 + p * Lay::kRunBytes;
+                    const uint2 a0 = lds64(r), b0 = lds64(r + 8);
+                    const uint2 m0 = lds64(r - kLaneCodes * part + B);
+                    const uint2 a1 = lds64(r + Lay::kRunBytes), b1 = lds64(r + Lay::kRunBytes + 8);
+                    const uint2 m1 = lds64(r + Lay::kRunBytes - kLaneCodes * part + B);
+                    accumulate_shard(w, make_uint4(a0.x, a0.y, b0.x, b0.y),
+                                     __fdividef(__uint_as_float(m0.y), __uint_as_float(m0.x)));
+                    accumulate_shard(w, make_uint4(a1.x, a1.y, b1.x, b1.y),
+                                     __fdividef(__uint_as_float(m1.y), __uint_as_float(m1.x)));
+                }
+                if (p < P) {
+#else
                 for (int p = 0; p < P; p++) {
-                    uint4 codes;
-                    uint2 meta;
-                    if (!from_global) {
-                        const uint32_t r = rec_s + p * Lay::kRunBytes;
-                        const uint2 a = lds64(r + kLaneCodes * part);
-                        const uint2 b = lds64(r + kLaneCodes * part + 8);
-                        codes = make_uint4(a.x, a.y, b.x, b.y);
-                        meta = lds64(r + B);
-                    } else {
-                        const uint8_t *r = shard_ptr[p] + blk * kRec;
-                        const uint2 a = ldg_u2(r + kLaneCodes * part);
-                        const uint2 b = ldg_u2(r + kLaneCodes * part + 8);
-                        codes = make_uint4(a.x, a.y, b.x, b.y);
-                        meta = ldg_u2(r + B);
-                    }
-                    // s_p / alpha_p (within 2 ulp; alpha_p <= 1e15 is far from
-                    // the range where the fast quotient underflows).
-                    const float f = __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x));
-                    accumulate_shard(w, codes, f);
+#endif
+                    const uint32_t r = r0 + p * Lay::kRunBytes;
+                    const uint2 a = lds64(r), b = lds64(r + 8);
+                    const uint2 meta = lds64(r - kLaneCodes * part + B);
+                    accumulate_shard(w, make_uint4(a.x, a.y, b.x, b.y),
+                                     __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
+                }
+            } else if (active) {
+                // The tile's odd last record is not in the bulk copies.
+                for (int p = 0; p < P; p++) {
+                    const uint8_t *r = shard_ptr[p] + blk * kRec;
+                    const uint2 a = ldg_u2(r + kLaneCodes * part), b = ldg_u2(r + kLaneCodes * part + 8);
+                    const uint2 meta = ldg_u2(r + B);
+                    accumulate_shard(w, make_uint4(a.x, a.y, b.x, b.y),
+                                     __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
                 }
             }
             // The stage is read: hand it back to the loader.

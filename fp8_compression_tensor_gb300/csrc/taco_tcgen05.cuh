@@ -159,14 +159,15 @@ __device__ __forceinline__ void clc_try_cancel(uint32_t result_addr, uint32_t ba
 // now does), or -1 if no CTA was left to cancel.
 __device__ __forceinline__ int64_t clc_response_ctaid_x(uint32_t result_addr)
 {
-    uint32_t ok, x;
+    uint32_t ok, x = 0;
+    // The cancelled CTA's index is read only from a successful response.
     asm volatile(
         "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
         "ld.shared.b128 r, [%2];\n\t"
         "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t"
-        "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
-        : "=r"(ok), "=r"(x)
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "+r"(x)
         : "r"(result_addr)
         : "memory");
     return ok ? static_cast<int64_t>(x) : -1;
