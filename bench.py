@@ -85,7 +85,9 @@ def parse_args():
 def source_hash(rel: str) -> str:
     h = hashlib.sha256()
     for p in (rel, "fp8_compression_tensor_gb300/csrc/taco_device.cuh",
-              "fp8_compression_tensor_gb300/csrc/taco_tcgen05.cuh"):
+              "fp8_compression_tensor_gb300/csrc/taco_tcgen05.cuh",
+              "fp8_compression_tensor_gb300/csrc/taco_sched.cuh",
+              "fp8_compression_tensor_gb300/csrc/taco_kernels.h"):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
