@@ -17,6 +17,12 @@ two-shot AllReduce (Section 4.4.2).
 Packed format (Section 4.4.2, zero-copy metadata layout): record k occupies
 bytes [k*(B+8), (k+1)*(B+8)): B E4M3 codes, then alpha_k and s_k as
 little-endian float32.
+
+Ablations (``variant``, ``code`` arguments; default ASH + DS with E4M3):
+standard Hadamard + DS (alpha = 1, Section 5.3.1), DS only (alpha = 1, no
+rotation, Section 5.2.2), ASH only (s = 1, direct cast, Section 5.2.2); codes
+E4M3, E5M2 (Q_max 57344, Section 5.3.2) and INT8 (Q_max 127, round half to
+even, Sections 2 and 6).
 """
 from __future__ import annotations
 
@@ -35,6 +41,12 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
 TAU = 1.0
 EPS = np.float32(1e-30)
 QMAX = 448.0
+
+ASH_DS, HADAMARD_DS, DS_ONLY, ASH_ONLY = 0, 1, 2, 3
+E4M3, E5M2, INT8 = 0, 1, 2
+VARIANTS = {"ash_ds": ASH_DS, "hadamard_ds": HADAMARD_DS, "ds_only": DS_ONLY, "ash_only": ASH_ONLY}
+CODES = {"e4m3": E4M3, "e5m2": E5M2, "int8": INT8}
+CODE_QMAX = {E4M3: 448.0, E5M2: 57344.0, INT8: 127.0}
 
 _lock = threading.Lock()
 _lib = None
@@ -66,11 +78,13 @@ def _load():
     i64, i32 = ctypes.c_int64, ctypes.c_int
     sig = {
         "taco_oracle_packed_bytes": (i64, [i64, i32]),
-        "taco_oracle_compress_bf16": (i32, [c_u16p, i64, i32, c_u8p]),
-        "taco_oracle_compress_f32": (i32, [c_f32p, i64, i32, c_u8p]),
-        "taco_oracle_decompress_f32": (i32, [c_u8p, i64, i32, c_f32p]),
-        "taco_oracle_decompress_bf16": (i32, [c_u8p, i64, i32, c_u16p]),
-        "taco_oracle_reduce_shards": (i32, [ctypes.POINTER(c_u8p), i32, i64, i32, c_u8p]),
+        "taco_oracle_compress_bf16_ex": (i32, [c_u16p, i64, i32, i32, i32, c_u8p]),
+        "taco_oracle_compress_f32_ex": (i32, [c_f32p, i64, i32, i32, i32, c_u8p]),
+        "taco_oracle_decompress_f32_ex": (i32, [c_u8p, i64, i32, i32, i32, c_f32p]),
+        "taco_oracle_decompress_bf16_ex": (i32, [c_u8p, i64, i32, i32, i32, c_u16p]),
+        "taco_oracle_reduce_shards_ex": (i32, [ctypes.POINTER(c_u8p), i32, i64, i32, i32, i32, c_u8p]),
+        "taco_oracle_code_encode_array": (None, [i32, c_f32p, i64, c_u8p]),
+        "taco_oracle_code_value_array": (None, [i32, c_u8p, i64, c_f64p]),
         "taco_oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
         "taco_oracle_e4m3_value": (ctypes.c_double, [ctypes.c_uint8]),
         "taco_oracle_e4m3_encode_array": (None, [c_f32p, i64, c_u8p]),
@@ -101,52 +115,68 @@ def packed_bytes(n: int, block: int) -> int:
     return int(_load().taco_oracle_packed_bytes(n, block))
 
 
-def compress(x_bf16: np.ndarray, block: int) -> np.ndarray:
+def compress(x_bf16: np.ndarray, block: int, variant: int = ASH_DS, code: int = E4M3) -> np.ndarray:
     """Algorithm 1 sender (Eqs. 5-10) on a bf16 tensor given as uint16 bit patterns.
 
     Returns the packed records as a flat uint8 array of (n/B)*(B+8) bytes.
     """
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1)
     out = np.empty(max(packed_bytes(x.size, block), 0), dtype=np.uint8)
-    _check(_load().taco_oracle_compress_bf16(_ptr(x, ctypes.c_uint16), x.size, block,
-                                             _ptr(out, ctypes.c_uint8)), "compress")
+    _check(_load().taco_oracle_compress_bf16_ex(_ptr(x, ctypes.c_uint16), x.size, block, variant, code,
+                                                _ptr(out, ctypes.c_uint8)), "compress")
     return out
 
 
-def compress_f32(x: np.ndarray, block: int) -> np.ndarray:
+def compress_f32(x: np.ndarray, block: int, variant: int = ASH_DS, code: int = E4M3) -> np.ndarray:
     """Algorithm 1 sender on a float32 tensor (used for the re-compression of a sum)."""
     x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
     out = np.empty(max(packed_bytes(x.size, block), 0), dtype=np.uint8)
-    _check(_load().taco_oracle_compress_f32(_ptr(x, ctypes.c_float), x.size, block,
-                                            _ptr(out, ctypes.c_uint8)), "compress_f32")
+    _check(_load().taco_oracle_compress_f32_ex(_ptr(x, ctypes.c_float), x.size, block, variant, code,
+                                               _ptr(out, ctypes.c_uint8)), "compress_f32")
     return out
 
 
-def decompress_f32(packed: np.ndarray, n: int, block: int) -> np.ndarray:
+def decompress_f32(packed: np.ndarray, n: int, block: int, variant: int = ASH_DS, code: int = E4M3) -> np.ndarray:
     """Algorithm 1 receiver (Eqs. 11-13) returning G' in float32."""
     p = np.ascontiguousarray(packed, dtype=np.uint8).reshape(-1)
     out = np.empty(n, dtype=np.float32)
-    _check(_load().taco_oracle_decompress_f32(_ptr(p, ctypes.c_uint8), n, block,
-                                              _ptr(out, ctypes.c_float)), "decompress_f32")
+    _check(_load().taco_oracle_decompress_f32_ex(_ptr(p, ctypes.c_uint8), n, block, variant, code,
+                                                 _ptr(out, ctypes.c_float)), "decompress_f32")
     return out
 
 
-def decompress(packed: np.ndarray, n: int, block: int) -> np.ndarray:
+def decompress(packed: np.ndarray, n: int, block: int, variant: int = ASH_DS, code: int = E4M3) -> np.ndarray:
     """Algorithm 1 receiver returning the bf16 tensor as uint16 bit patterns (RNE)."""
     p = np.ascontiguousarray(packed, dtype=np.uint8).reshape(-1)
     out = np.empty(n, dtype=np.uint16)
-    _check(_load().taco_oracle_decompress_bf16(_ptr(p, ctypes.c_uint8), n, block,
-                                               _ptr(out, ctypes.c_uint16)), "decompress")
+    _check(_load().taco_oracle_decompress_bf16_ex(_ptr(p, ctypes.c_uint8), n, block, variant, code,
+                                                  _ptr(out, ctypes.c_uint16)), "decompress")
     return out
 
 
-def reduce_shards(shards, n: int, block: int) -> np.ndarray:
+def reduce_shards(shards, n: int, block: int, variant: int = ASH_DS, code: int = E4M3) -> np.ndarray:
     """Decode P packed shards to float32, sum them in shard order, compress the sum once."""
     arrs = [np.ascontiguousarray(s, dtype=np.uint8).reshape(-1) for s in shards]
     ptrs = (ctypes.POINTER(ctypes.c_uint8) * len(arrs))(*[_ptr(a, ctypes.c_uint8) for a in arrs])
     out = np.empty(max(packed_bytes(n, block), 0), dtype=np.uint8)
-    _check(_load().taco_oracle_reduce_shards(ptrs, len(arrs), n, block,
-                                             _ptr(out, ctypes.c_uint8)), "reduce_shards")
+    _check(_load().taco_oracle_reduce_shards_ex(ptrs, len(arrs), n, block, variant, code,
+                                                _ptr(out, ctypes.c_uint8)), "reduce_shards")
+    return out
+
+
+def code_encode(code: int, u: np.ndarray) -> np.ndarray:
+    """The code format's conversion of float32 values (E4M3 / E5M2 / INT8 bytes)."""
+    u = np.ascontiguousarray(u, dtype=np.float32).reshape(-1)
+    out = np.empty(u.size, dtype=np.uint8)
+    _load().taco_oracle_code_encode_array(code, _ptr(u, ctypes.c_float), u.size, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def code_value(code: int, codes: np.ndarray) -> np.ndarray:
+    """The float64 value of each code byte of the given format."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    out = np.empty(c.size, dtype=np.float64)
+    _load().taco_oracle_code_value_array(code, _ptr(c, ctypes.c_uint8), c.size, _ptr(out, ctypes.c_double))
     return out
 
 

@@ -36,6 +36,23 @@
  *     sums the shards left to right in shard order, and compresses the sum
  *     once from binary32 (Section 4.4.2, two-shot AllReduce: one compressed
  *     AlltoAll followed by a single local reduction).
+ *
+ * Ablation variants and code formats (the "_ex" entry points; the plain
+ * entry points are ASH + DS with E4M3):
+ *   - ASH + DS (the method), standard Hadamard + DS (alpha = 1, Section
+ *     5.3.1 "standard Hadamard transform"), DS only (alpha = 1 and no
+ *     rotation, Section 5.2.2 "Dual-Scale quantization in isolation") and
+ *     ASH only (no post-rotation scale: s = 1 and the rotated value is cast
+ *     directly, Section 5.2.2 "ASH alone");
+ *   - codes E4M3 (Q_max 448), E5M2 (Q_max 57344, the largest finite OCP
+ *     E5M2 value; Section 5.3.2 format ablation) rounded to nearest even and
+ *     saturated to +-Q_max like E4M3, and INT8 (Q_max 127, Section 2's
+ *     round(x / Delta) with Delta = max|x| / 127, ties to even, clamped to
+ *     +-127; the INT8 fallback of Section 6 is ASH + DS with these codes);
+ *   - the record layout stays [B codes | alpha | s], with alpha = 1 where the
+ *     variant has no adaptive scale and s = 1 where it has no post-rotation
+ *     scale; decoding is always q * s, then the inverse rotation if the
+ *     variant rotates, then the division by alpha.
  */
 #include <math.h>
 #include <stdint.h>
@@ -46,11 +63,16 @@
 #define ORACLE_QMAX 448.0f
 #define ORACLE_MAX_BLOCK 512
 
+/* Variants and code formats of the "_ex" entry points. */
+enum { VARIANT_ASH_DS = 0, VARIANT_HADAMARD_DS = 1, VARIANT_DS_ONLY = 2, VARIANT_ASH_ONLY = 3 };
+enum { CODE_E4M3 = 0, CODE_E5M2 = 1, CODE_INT8 = 2 };
+
 enum {
     ORACLE_OK = 0,
     ORACLE_ERR_BLOCK = -1,  /* B not a power of two in [2, 512] */
     ORACLE_ERR_SHAPE = -2,  /* n < 0 or n not a multiple of B */
     ORACLE_ERR_SHARDS = -3, /* P < 1 */
+    ORACLE_ERR_SCHEME = -4, /* unknown variant or code format */
 };
 
 /* ------------------------------------------------------------------ */
@@ -163,6 +185,110 @@ uint8_t taco_oracle_e4m3_encode(float u)
     return (uint8_t)(sign | c);
 }
 
+/* Magnitude of the E5M2 pattern whose low seven bits are c7 (0..123):
+ * exponent field E = c7 >> 2 (bias 15), mantissa M = c7 & 3.  E = 0 is the
+ * subnormal range, 2^-14 * M/4.  0x7C is infinity, 0x7D..0x7F NaN. */
+static double e5m2_magnitude(int c7)
+{
+    int E = c7 >> 2, M = c7 & 3;
+    if (E == 0)
+        return ldexp((double)M, -16);
+    return ldexp(4.0 + (double)M, E - 17); /* 2^(E-15) * (1 + M/4) */
+}
+
+double taco_oracle_e5m2_value(uint8_t code)
+{
+    int c7 = code & 0x7f;
+    if (c7 == 0x7c)
+        return (code & 0x80) ? -INFINITY : INFINITY;
+    if (c7 > 0x7c)
+        return NAN;
+    double v = e5m2_magnitude(c7);
+    return (code & 0x80) ? -v : v;
+}
+
+/* Nearest E5M2 value, ties to the even code, magnitudes at or above 57344
+ * saturate to 57344, the sign of zero is kept. */
+uint8_t taco_oracle_e5m2_encode(float u)
+{
+    if (isnan(u))
+        return 0x7f;
+    uint8_t sign = signbit(u) ? 0x80 : 0x00;
+    double a = fabs((double)u);
+    if (a >= 57344.0)
+        return (uint8_t)(sign | 0x7b);
+    int lo = 0, hi = 123; /* magnitude(123) = 57344 > a */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (e5m2_magnitude(mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double twice_mid = e5m2_magnitude(lo) + e5m2_magnitude(hi);
+    double twice_a = 2.0 * a;
+    int c;
+    if (twice_a < twice_mid)
+        c = lo;
+    else if (twice_a > twice_mid)
+        c = hi;
+    else
+        c = (lo % 2 == 0) ? lo : hi;
+    return (uint8_t)(sign | c);
+}
+
+/* round(u) to the nearest integer, ties to even, clamped to [-127, 127],
+ * as a two's complement byte. */
+uint8_t taco_oracle_int8_encode(float u)
+{
+    if (isnan(u))
+        return 0;
+    double a = (double)u;
+    double f = floor(a);
+    double d = a - f; /* exact: |a| < 2^24 or a is an integer */
+    double r;
+    if (d < 0.5)
+        r = f;
+    else if (d > 0.5)
+        r = f + 1.0;
+    else
+        r = (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+    if (r > 127.0)
+        r = 127.0;
+    if (r < -127.0)
+        r = -127.0;
+    return (uint8_t)(int8_t)r;
+}
+
+double taco_oracle_int8_value(uint8_t code)
+{
+    return (double)(int8_t)code;
+}
+
+static int scheme_ok(int variant, int code)
+{
+    return variant >= VARIANT_ASH_DS && variant <= VARIANT_ASH_ONLY && code >= CODE_E4M3 && code <= CODE_INT8;
+}
+
+static float code_qmax(int code)
+{
+    return code == CODE_E4M3 ? ORACLE_QMAX : code == CODE_E5M2 ? 57344.0f : 127.0f;
+}
+
+static uint8_t code_encode(int code, float u)
+{
+    return code == CODE_E4M3 ? taco_oracle_e4m3_encode(u)
+           : code == CODE_E5M2 ? taco_oracle_e5m2_encode(u)
+                                : taco_oracle_int8_encode(u);
+}
+
+static double code_value(int code, uint8_t c)
+{
+    return code == CODE_E4M3 ? taco_oracle_e4m3_value(c)
+           : code == CODE_E5M2 ? taco_oracle_e5m2_value(c)
+                                : taco_oracle_int8_value(c);
+}
+
 /* ------------------------------------------------------------------ */
 /* Hadamard rotation                                                   */
 /* ------------------------------------------------------------------ */
@@ -195,39 +321,55 @@ static int block_ok(int B)
 /* Sender: Algorithm 1, lines 4-16                                     */
 /* ------------------------------------------------------------------ */
 
-static void compress_block(const float *G, int B, uint8_t *rec)
+static void compress_block(const float *G, int B, int variant, int code, uint8_t *rec)
 {
-    /* Eq. (6): sigma_k = sqrt(mean_j G_kj^2 + eps). */
-    double acc = 0.0;
-    for (int j = 0; j < B; j++)
-        acc += (double)G[j] * (double)G[j];
-    float m = (float)(acc / (double)B);
-    float sigma = sqrtf(m + ORACLE_EPS);
-
-    /* Eq. (7): alpha_k = tau / sigma_k; G~_k = alpha_k * G_k. */
-    float alpha = ORACLE_TAU / sigma;
+    const int adaptive = variant == VARIANT_ASH_DS || variant == VARIANT_ASH_ONLY;
+    const int rotate = variant != VARIANT_DS_ONLY;
+    const int dual_scale = variant != VARIANT_ASH_ONLY;
+    float alpha = 1.0f;
     float Z[ORACLE_MAX_BLOCK];
-    for (int j = 0; j < B; j++)
-        Z[j] = alpha * G[j];
+    if (adaptive) {
+        /* Eq. (6): sigma_k = sqrt(mean_j G_kj^2 + eps). */
+        double acc = 0.0;
+        for (int j = 0; j < B; j++)
+            acc += (double)G[j] * (double)G[j];
+        float m = (float)(acc / (double)B);
+        float sigma = sqrtf(m + ORACLE_EPS);
 
-    /* Eq. (8): Z_k = (1/sqrt(B)) H_B G~_k. */
-    taco_oracle_fwht(Z, B);
-    float r = inv_sqrt_block(B);
-    float zmax = 0.0f;
-    for (int j = 0; j < B; j++) {
-        Z[j] = r * Z[j];
-        if (fabsf(Z[j]) > zmax)
-            zmax = fabsf(Z[j]);
+        /* Eq. (7): alpha_k = tau / sigma_k; G~_k = alpha_k * G_k. */
+        alpha = ORACLE_TAU / sigma;
+        for (int j = 0; j < B; j++)
+            Z[j] = alpha * G[j];
+    } else {
+        for (int j = 0; j < B; j++)
+            Z[j] = G[j];
     }
 
-    /* Eq. (9): s_k = max|Z_k| / Q_max.  Eq. (10): q_k = Cvt_FP8(Z_k / s_k). */
-    float s = zmax / ORACLE_QMAX;
-    if (zmax == 0.0f) {
+    /* Eq. (8): Z_k = (1/sqrt(B)) H_B G~_k. */
+    if (rotate) {
+        taco_oracle_fwht(Z, B);
+        float r = inv_sqrt_block(B);
+        for (int j = 0; j < B; j++)
+            Z[j] = r * Z[j];
+    }
+    float zmax = 0.0f;
+    for (int j = 0; j < B; j++)
+        if (fabsf(Z[j]) > zmax)
+            zmax = fabsf(Z[j]);
+
+    /* Eq. (9): s_k = max|Z_k| / Q_max.  Eq. (10): q_k = Cvt(Z_k / s_k). */
+    float s;
+    if (!dual_scale) {
+        s = 1.0f;
+        for (int j = 0; j < B; j++)
+            rec[j] = code_encode(code, Z[j]);
+    } else if (zmax == 0.0f) {
         s = 0.0f;
         memset(rec, 0, (size_t)B);
     } else {
+        s = zmax / code_qmax(code);
         for (int j = 0; j < B; j++)
-            rec[j] = taco_oracle_e4m3_encode(Z[j] / s);
+            rec[j] = code_encode(code, Z[j] / s);
     }
     memcpy(rec + B, &alpha, 4);
     memcpy(rec + B + 4, &s, 4);
@@ -237,22 +379,24 @@ static void compress_block(const float *G, int B, uint8_t *rec)
 /* Receiver: Algorithm 1, lines 19-24; Eqs. (11)-(13)                  */
 /* ------------------------------------------------------------------ */
 
-static void decompress_block(const uint8_t *rec, int B, float *out)
+static void decompress_block(const uint8_t *rec, int B, int variant, int code, float *out)
 {
     float alpha, s;
     memcpy(&alpha, rec + B, 4);
     memcpy(&s, rec + B + 4, 4);
     float Zh[ORACLE_MAX_BLOCK];
     for (int j = 0; j < B; j++) {
-        float q = (float)taco_oracle_e4m3_value(rec[j]); /* Eq. (11) */
+        float q = (float)code_value(code, rec[j]); /* Eq. (11) */
         Zh[j] = q * s;
     }
-    taco_oracle_fwht(Zh, B); /* Eq. (12) */
-    float r = inv_sqrt_block(B);
-    for (int j = 0; j < B; j++) {
-        float Gh = r * Zh[j];
-        out[j] = Gh / alpha; /* Eq. (13) */
+    if (variant != VARIANT_DS_ONLY) {
+        taco_oracle_fwht(Zh, B); /* Eq. (12) */
+        float r = inv_sqrt_block(B);
+        for (int j = 0; j < B; j++)
+            Zh[j] = r * Zh[j];
     }
+    for (int j = 0; j < B; j++)
+        out[j] = Zh[j] / alpha; /* Eq. (13) */
 }
 
 /* ------------------------------------------------------------------ */
@@ -266,54 +410,61 @@ int64_t taco_oracle_packed_bytes(int64_t n, int B)
     return n / B * (int64_t)(B + 8);
 }
 
-int taco_oracle_compress_bf16(const uint16_t *x, int64_t n, int B, uint8_t *packed)
+static int check_args(int64_t n, int B, int variant, int code)
 {
     if (!block_ok(B))
         return ORACLE_ERR_BLOCK;
     if (n < 0 || n % B != 0)
         return ORACLE_ERR_SHAPE;
+    if (!scheme_ok(variant, code))
+        return ORACLE_ERR_SCHEME;
+    return ORACLE_OK;
+}
+
+int taco_oracle_compress_bf16_ex(const uint16_t *x, int64_t n, int B, int variant, int code, uint8_t *packed)
+{
+    int st = check_args(n, B, variant, code);
+    if (st != ORACLE_OK)
+        return st;
     float G[ORACLE_MAX_BLOCK];
     for (int64_t k = 0; k < n / B; k++) {
         for (int j = 0; j < B; j++)
             G[j] = bf16_to_f32(x[k * B + j]);
-        compress_block(G, B, packed + k * (int64_t)(B + 8));
+        compress_block(G, B, variant, code, packed + k * (int64_t)(B + 8));
     }
     return ORACLE_OK;
 }
 
-int taco_oracle_compress_f32(const float *x, int64_t n, int B, uint8_t *packed)
+int taco_oracle_compress_f32_ex(const float *x, int64_t n, int B, int variant, int code, uint8_t *packed)
 {
-    if (!block_ok(B))
-        return ORACLE_ERR_BLOCK;
-    if (n < 0 || n % B != 0)
-        return ORACLE_ERR_SHAPE;
+    int st = check_args(n, B, variant, code);
+    if (st != ORACLE_OK)
+        return st;
     for (int64_t k = 0; k < n / B; k++)
-        compress_block(x + k * B, B, packed + k * (int64_t)(B + 8));
+        compress_block(x + k * B, B, variant, code, packed + k * (int64_t)(B + 8));
     return ORACLE_OK;
 }
 
-int taco_oracle_decompress_f32(const uint8_t *packed, int64_t n, int B, float *y)
+int taco_oracle_decompress_f32_ex(const uint8_t *packed, int64_t n, int B, int variant, int code, float *y)
 {
-    if (!block_ok(B))
-        return ORACLE_ERR_BLOCK;
-    if (n < 0 || n % B != 0)
-        return ORACLE_ERR_SHAPE;
+    int st = check_args(n, B, variant, code);
+    if (st != ORACLE_OK)
+        return st;
     for (int64_t k = 0; k < n / B; k++)
-        decompress_block(packed + k * (int64_t)(B + 8), B, y + k * B);
+        decompress_block(packed + k * (int64_t)(B + 8), B, variant, code, y + k * B);
     return ORACLE_OK;
 }
 
 /* Decompression to the tensor's own dtype: bf16, rounded to nearest even
  * from the binary32 G'_k. */
-int taco_oracle_decompress_bf16(const uint8_t *packed, int64_t n, int B, uint16_t *y)
+int taco_oracle_decompress_bf16_ex(const uint8_t *packed, int64_t n, int B, int variant, int code, uint16_t *y)
 {
-    if (!block_ok(B))
-        return ORACLE_ERR_BLOCK;
-    if (n < 0 || n % B != 0)
-        return ORACLE_ERR_SHAPE;
+    int st = check_args(n, B, variant, code);
+    if (st != ORACLE_OK)
+        return st;
     float out[ORACLE_MAX_BLOCK];
     for (int64_t k = 0; k < n / B; k++) {
-        decompress_block(packed + k * (int64_t)(B + 8), B, out);
+        decompress_block(packed + k * (int64_t)(B + 8), B, variant, code, out);
         for (int j = 0; j < B; j++)
             y[k * B + j] = f32_to_bf16_rne(out[j]);
     }
@@ -322,14 +473,14 @@ int taco_oracle_decompress_bf16(const uint8_t *packed, int64_t n, int B, uint16_
 
 /* Receive side of the two-shot AllReduce (Section 4.4.2): the P compressed
  * shards of the same n elements are decoded to binary32, summed in shard
- * order, and the sum is compressed once. */
-int taco_oracle_reduce_shards(const uint8_t *const *shards, int P, int64_t n, int B,
-                              uint8_t *out)
+ * order, and the sum is compressed once, all with the same variant and code
+ * format. */
+int taco_oracle_reduce_shards_ex(const uint8_t *const *shards, int P, int64_t n, int B, int variant, int code,
+                                 uint8_t *out)
 {
-    if (!block_ok(B))
-        return ORACLE_ERR_BLOCK;
-    if (n < 0 || n % B != 0)
-        return ORACLE_ERR_SHAPE;
+    int st = check_args(n, B, variant, code);
+    if (st != ORACLE_OK)
+        return st;
     if (P < 1)
         return ORACLE_ERR_SHARDS;
     float S[ORACLE_MAX_BLOCK], t[ORACLE_MAX_BLOCK];
@@ -337,13 +488,39 @@ int taco_oracle_reduce_shards(const uint8_t *const *shards, int P, int64_t n, in
         for (int j = 0; j < B; j++)
             S[j] = 0.0f;
         for (int p = 0; p < P; p++) {
-            decompress_block(shards[p] + k * (int64_t)(B + 8), B, t);
+            decompress_block(shards[p] + k * (int64_t)(B + 8), B, variant, code, t);
             for (int j = 0; j < B; j++)
                 S[j] = S[j] + t[j];
         }
-        compress_block(S, B, out + k * (int64_t)(B + 8));
+        compress_block(S, B, variant, code, out + k * (int64_t)(B + 8));
     }
     return ORACLE_OK;
+}
+
+/* The method itself: ASH + DS with E4M3 codes. */
+int taco_oracle_compress_bf16(const uint16_t *x, int64_t n, int B, uint8_t *packed)
+{
+    return taco_oracle_compress_bf16_ex(x, n, B, VARIANT_ASH_DS, CODE_E4M3, packed);
+}
+
+int taco_oracle_compress_f32(const float *x, int64_t n, int B, uint8_t *packed)
+{
+    return taco_oracle_compress_f32_ex(x, n, B, VARIANT_ASH_DS, CODE_E4M3, packed);
+}
+
+int taco_oracle_decompress_f32(const uint8_t *packed, int64_t n, int B, float *y)
+{
+    return taco_oracle_decompress_f32_ex(packed, n, B, VARIANT_ASH_DS, CODE_E4M3, y);
+}
+
+int taco_oracle_decompress_bf16(const uint8_t *packed, int64_t n, int B, uint16_t *y)
+{
+    return taco_oracle_decompress_bf16_ex(packed, n, B, VARIANT_ASH_DS, CODE_E4M3, y);
+}
+
+int taco_oracle_reduce_shards(const uint8_t *const *shards, int P, int64_t n, int B, uint8_t *out)
+{
+    return taco_oracle_reduce_shards_ex(shards, P, n, B, VARIANT_ASH_DS, CODE_E4M3, out);
 }
 
 /* Array helpers for the tests. */
@@ -376,4 +553,16 @@ void taco_oracle_fwht_rows(float *v, int64_t rows, int B)
 {
     for (int64_t i = 0; i < rows; i++)
         taco_oracle_fwht(v + i * B, B);
+}
+
+void taco_oracle_code_encode_array(int code, const float *u, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = code_encode(code, u[i]);
+}
+
+void taco_oracle_code_value_array(int code, const uint8_t *codes, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = code_value(code, codes[i]);
 }
