@@ -27,9 +27,26 @@ STATUS = {
     6: "TACO_ERR_OVERLAP",
     7: "TACO_ERR_CUDA",
     8: "TACO_ERR_DEVICE_FAULT",
+    9: "TACO_ERR_BAD_OPTIONS",
 }
 MAX_SHARDS = 16
 SUPPORTED_BLOCKS = (64, 128, 256)
+# Ablations (taco_variant_t, taco_code_t of include/taco.h).
+VARIANTS = {"ash_ds": 0, "hadamard_ds": 1, "ds_only": 2, "ash_only": 3}
+CODES = {"e4m3": 0, "e5m2": 1, "int8": 2}
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int), ("variant", ctypes.c_int), ("code", ctypes.c_int)]
+
+
+def _options(block: int, variant, code) -> Optional[_Options]:
+    """None for the method itself (ASH + DS, E4M3), else the _ex options."""
+    v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    c = CODES[code] if isinstance(code, str) else int(code)
+    if v == 0 and c == 0:
+        return None
+    return _Options(block, v, c)
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +78,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.taco_decompress.restype = i32
         lib.taco_reduce_shards.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]
         lib.taco_reduce_shards.restype = i32
+        optp = ctypes.POINTER(_Options)
+        lib.taco_compress_ex.argtypes = [vp, i64, i64, optp, vp, vp]
+        lib.taco_compress_ex.restype = i32
+        lib.taco_decompress_ex.argtypes = [vp, i64, i64, optp, vp, vp]
+        lib.taco_decompress_ex.restype = i32
+        lib.taco_reduce_shards_ex.argtypes = [ctypes.POINTER(vp), i32, i64, i64, optp, vp, vp]
+        lib.taco_reduce_shards_ex.restype = i32
         lib.taco_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.taco_device_status.restype = i32
         lib.taco_status_string.argtypes = [i32]
@@ -116,10 +140,12 @@ def _rows_hidden(x: torch.Tensor):
     return rows, hidden
 
 
-def compress(x: torch.Tensor, block: int = 128, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+def compress(x: torch.Tensor, block: int = 128, out: Optional[torch.Tensor] = None, stream=None,
+             variant="ash_ds", code="e4m3") -> torch.Tensor:
     """TACO compression (Algorithm 1 sender side) of a bf16 CUDA tensor, viewed
     as [rows, hidden] with hidden = x.shape[-1].  Returns (or fills) a uint8
-    tensor of compressed_bytes(rows, hidden, block) packed bytes."""
+    tensor of compressed_bytes(rows, hidden, block) packed bytes.  `variant`
+    and `code` select an ablation (VARIANTS, CODES)."""
     _check_cuda_tensor(x, torch.bfloat16, "x")
     rows, hidden = _rows_hidden(x)
     nbytes = compressed_bytes(rows, hidden, block)
@@ -129,15 +155,20 @@ def compress(x: torch.Tensor, block: int = 128, out: Optional[torch.Tensor] = No
         _check_cuda_tensor(out, torch.uint8, "out")
         if out.numel() != nbytes:
             raise ValueError(f"out must have {nbytes} bytes, has {out.numel()}")
+    opt = _options(block, variant, code)
     with torch.cuda.device(x.device):
-        rc = load_library().taco_compress(x.data_ptr(), rows, hidden, block, out.data_ptr(),
-                                          _stream_handle(x.device, stream))
+        if opt is None:
+            rc = load_library().taco_compress(x.data_ptr(), rows, hidden, block, out.data_ptr(),
+                                              _stream_handle(x.device, stream))
+        else:
+            rc = load_library().taco_compress_ex(x.data_ptr(), rows, hidden, ctypes.byref(opt), out.data_ptr(),
+                                                 _stream_handle(x.device, stream))
     _check(rc, "taco_compress")
     return out
 
 
 def decompress(packed: torch.Tensor, rows: int, hidden: int, block: int = 128,
-               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+               out: Optional[torch.Tensor] = None, stream=None, variant="ash_ds", code="e4m3") -> torch.Tensor:
     """TACO decompression (Algorithm 1 receiver side) of packed records into a
     bf16 [rows, hidden] CUDA tensor."""
     _check_cuda_tensor(packed, torch.uint8, "packed")
@@ -150,15 +181,20 @@ def decompress(packed: torch.Tensor, rows: int, hidden: int, block: int = 128,
         _check_cuda_tensor(out, torch.bfloat16, "out")
         if out.numel() != rows * hidden:
             raise ValueError("out has the wrong number of elements")
+    opt = _options(block, variant, code)
     with torch.cuda.device(packed.device):
-        rc = load_library().taco_decompress(packed.data_ptr(), rows, hidden, block, out.data_ptr(),
-                                            _stream_handle(packed.device, stream))
+        if opt is None:
+            rc = load_library().taco_decompress(packed.data_ptr(), rows, hidden, block, out.data_ptr(),
+                                                _stream_handle(packed.device, stream))
+        else:
+            rc = load_library().taco_decompress_ex(packed.data_ptr(), rows, hidden, ctypes.byref(opt),
+                                                   out.data_ptr(), _stream_handle(packed.device, stream))
     _check(rc, "taco_decompress")
     return out
 
 
 def reduce_shards(shards: Sequence[torch.Tensor], rows: int, hidden: int, block: int = 128,
-                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                  out: Optional[torch.Tensor] = None, stream=None, variant="ash_ds", code="e4m3") -> torch.Tensor:
     """Decode P packed shards of a [rows, hidden] tensor, sum them in FP32 and
     compress the sum once (the local reduction of a two-shot AllReduce)."""
     shards = list(shards)
@@ -177,9 +213,14 @@ def reduce_shards(shards: Sequence[torch.Tensor], rows: int, hidden: int, block:
         if out.numel() != nbytes:
             raise ValueError(f"out must have {nbytes} bytes")
     ptrs = (ctypes.c_void_p * len(shards))(*[s.data_ptr() for s in shards])
+    opt = _options(block, variant, code)
     with torch.cuda.device(dev):
-        rc = load_library().taco_reduce_shards(ptrs, len(shards), rows, hidden, block, out.data_ptr(),
-                                               _stream_handle(dev, stream))
+        if opt is None:
+            rc = load_library().taco_reduce_shards(ptrs, len(shards), rows, hidden, block, out.data_ptr(),
+                                                   _stream_handle(dev, stream))
+        else:
+            rc = load_library().taco_reduce_shards_ex(ptrs, len(shards), rows, hidden, ctypes.byref(opt),
+                                                      out.data_ptr(), _stream_handle(dev, stream))
     _check(rc, "taco_reduce_shards")
     return out
 

@@ -16,7 +16,7 @@
 namespace taco {
 namespace {
 
-// Device-side fault flags (bits kFaultCompress, kFaultDecompress).
+// Device-side fault flags (bits kFaultCompress, kFaultDecompress, kFaultReduce).
 __device__ uint32_t g_fault_flags;
 
 thread_local int t_last_cuda_error = 0;
@@ -28,9 +28,7 @@ struct DeviceState {
     cudaError_t init_error = cudaSuccess;
     int sm_count = 0;
     uint32_t *fault = nullptr;  // device address of g_fault_flags
-    int compress_ctas_per_sm[3] = {0, 0, 0};
-    int decompress_ctas_per_sm[3] = {0, 0, 0};
-    int reduce_ctas_per_sm[3] = {0, 0, 0};
+    int ctas_per_sm = 0;        // last occupancy query (set-up check only)
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -66,11 +64,13 @@ void init_device(DeviceState &st)
         e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
     const int blocks[3] = {64, 128, 256};
     for (int i = 0; i < 3 && e == cudaSuccess; i++) {
-        e = init_kernel(compress_kernel_info(blocks[i]), &st.compress_ctas_per_sm[i]);
-        if (e == cudaSuccess)
-            e = init_kernel(decompress_kernel_info(blocks[i]), &st.decompress_ctas_per_sm[i]);
-        if (e == cudaSuccess)
-            e = init_kernel(reduce_kernel_info(blocks[i]), &st.reduce_ctas_per_sm[i]);
+        e = init_kernel(compress_kernel_info(blocks[i]), &st.ctas_per_sm);
+        for (int code = 0; code < 3 && e == cudaSuccess; code++) {
+            if (code != 1)   // E4M3 and E5M2 share a decompress kernel
+                e = init_kernel(decompress_kernel_info(blocks[i], code), &st.ctas_per_sm);
+            if (e == cudaSuccess)
+                e = init_kernel(reduce_kernel_info(blocks[i], code), &st.ctas_per_sm);
+        }
     }
     st.init_error = e;
 }
@@ -155,23 +155,19 @@ taco_status_t check_shape(int64_t rows, int64_t hidden, int block, int64_t *n, i
     return TACO_OK;
 }
 
-}  // namespace
-}  // namespace taco
-
-using namespace taco;
-
-extern "C" {
-
-int64_t taco_compressed_bytes(int64_t rows, int64_t hidden, int block)
+taco_status_t check_options(const taco_options_t *opt, Scheme *scheme)
 {
-    int64_t n = 0, bytes = 0;
-    if (check_shape(rows, hidden, block, &n, &bytes) != TACO_OK)
-        return -1;
-    return bytes;
+    if (!opt)
+        return TACO_ERR_BAD_OPTIONS;
+    if (opt->variant < TACO_VARIANT_ASH_DS || opt->variant > TACO_VARIANT_ASH_ONLY || opt->code < TACO_CODE_E4M3 ||
+        opt->code > TACO_CODE_INT8)
+        return TACO_ERR_BAD_OPTIONS;
+    *scheme = Scheme{opt->variant, opt->code};
+    return TACO_OK;
 }
 
-taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t hidden, int block, void *packed_out,
-                            taco_stream_t stream)
+taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, int block, Scheme scheme,
+                            void *packed_out, taco_stream_t stream)
 {
     int64_t n = 0, bytes = 0;
     taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
@@ -198,12 +194,13 @@ taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t hidden, in
     if (e != cudaSuccess)
         return cuda_fail(e);
     const int grid = static_cast<int>(ntiles);
-    e = launch_compress(block, &map, packed_out, nblocks, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
+    e = launch_compress(block, scheme, &map, packed_out, nblocks, dev->fault, grid,
+                        reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }
 
-taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidden, int block, void *y_bf16_out,
-                              taco_stream_t stream)
+taco_status_t decompress_impl(const void *packed_in, int64_t rows, int64_t hidden, int block, Scheme scheme,
+                              void *y_bf16_out, taco_stream_t stream)
 {
     int64_t n = 0, bytes = 0;
     taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
@@ -221,7 +218,7 @@ taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidde
     // Tensor-core kernel over tiles of 128 (B = 64: 256) blocks: one CTA per
     // tile, of which one per SM runs and takes the tiles of CTAs it cancels.
     const int64_t nblocks = n / block;
-    const KernelInfo ki = decompress_kernel_info(block);
+    const KernelInfo ki = decompress_kernel_info(block, scheme.code);
     const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
     if (ntiles > INT32_MAX)
         return TACO_ERR_BAD_SHAPE;
@@ -230,12 +227,13 @@ taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidde
     if (e != cudaSuccess)
         return cuda_fail(e);
     const int grid = static_cast<int>(ntiles);
-    e = launch_decompress(block, &map, packed_in, nblocks, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
+    e = launch_decompress(block, scheme, &map, packed_in, nblocks, dev->fault, grid,
+                          reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }
 
-taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shards, int64_t rows, int64_t hidden,
-                                 int block, void *packed_out, taco_stream_t stream)
+taco_status_t reduce_impl(const void *const *packed_shards, int num_shards, int64_t rows, int64_t hidden, int block,
+                          Scheme scheme, void *packed_out, taco_stream_t stream)
 {
     int64_t n = 0, bytes = 0;
     taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
@@ -265,15 +263,82 @@ taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shard
     args.out = static_cast<uint8_t *>(packed_out);
     args.nblocks = n / block;
     args.num_shards = num_shards;
+    args.variant = scheme.variant;
     // One CTA per tile of blocks; one per SM runs and takes the tiles of CTAs
     // it cancels before they start.
-    const KernelInfo ki = reduce_kernel_info(block);
+    const KernelInfo ki = reduce_kernel_info(block, scheme.code);
     const int64_t ntiles = (args.nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
     if (ntiles > INT32_MAX)
         return TACO_ERR_BAD_SHAPE;
     const int grid = static_cast<int>(ntiles);
-    const cudaError_t e = launch_reduce(block, args, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e =
+        launch_reduce(block, scheme.code, args, dev->fault, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TACO_OK : cuda_fail(e);
+}
+
+constexpr Scheme kMethod{TACO_VARIANT_ASH_DS, TACO_CODE_E4M3};
+
+}  // namespace
+}  // namespace taco
+
+using namespace taco;
+
+extern "C" {
+
+int64_t taco_compressed_bytes(int64_t rows, int64_t hidden, int block)
+{
+    int64_t n = 0, bytes = 0;
+    if (check_shape(rows, hidden, block, &n, &bytes) != TACO_OK)
+        return -1;
+    return bytes;
+}
+
+taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t hidden, int block, void *packed_out,
+                            taco_stream_t stream)
+{
+    return compress_impl(x_bf16, rows, hidden, block, kMethod, packed_out, stream);
+}
+
+taco_status_t taco_decompress(const void *packed_in, int64_t rows, int64_t hidden, int block, void *y_bf16_out,
+                              taco_stream_t stream)
+{
+    return decompress_impl(packed_in, rows, hidden, block, kMethod, y_bf16_out, stream);
+}
+
+taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shards, int64_t rows, int64_t hidden,
+                                 int block, void *packed_out, taco_stream_t stream)
+{
+    return reduce_impl(packed_shards, num_shards, rows, hidden, block, kMethod, packed_out, stream);
+}
+
+taco_status_t taco_compress_ex(const void *x_bf16, int64_t rows, int64_t hidden, const taco_options_t *options,
+                               void *packed_out, taco_stream_t stream)
+{
+    Scheme scheme{};
+    const taco_status_t st = check_options(options, &scheme);
+    if (st != TACO_OK)
+        return st;
+    return compress_impl(x_bf16, rows, hidden, options->block, scheme, packed_out, stream);
+}
+
+taco_status_t taco_decompress_ex(const void *packed_in, int64_t rows, int64_t hidden, const taco_options_t *options,
+                                 void *y_bf16_out, taco_stream_t stream)
+{
+    Scheme scheme{};
+    const taco_status_t st = check_options(options, &scheme);
+    if (st != TACO_OK)
+        return st;
+    return decompress_impl(packed_in, rows, hidden, options->block, scheme, y_bf16_out, stream);
+}
+
+taco_status_t taco_reduce_shards_ex(const void *const *packed_shards, int num_shards, int64_t rows, int64_t hidden,
+                                    const taco_options_t *options, void *packed_out, taco_stream_t stream)
+{
+    Scheme scheme{};
+    const taco_status_t st = check_options(options, &scheme);
+    if (st != TACO_OK)
+        return st;
+    return reduce_impl(packed_shards, num_shards, rows, hidden, options->block, scheme, packed_out, stream);
 }
 
 taco_status_t taco_device_status(taco_stream_t stream, uint32_t *flags_out)
@@ -309,6 +374,7 @@ const char *taco_status_string(taco_status_t status)
     case TACO_ERR_OVERLAP: return "TACO_ERR_OVERLAP: an output overlaps an input";
     case TACO_ERR_CUDA: return "TACO_ERR_CUDA: a CUDA call failed (see taco_last_cuda_error)";
     case TACO_ERR_DEVICE_FAULT: return "TACO_ERR_DEVICE_FAULT: a kernel gave up waiting for a copy";
+    case TACO_ERR_BAD_OPTIONS: return "TACO_ERR_BAD_OPTIONS: options NULL, or unknown variant or code format";
     default: return "unknown taco_status_t";
     }
 }

@@ -33,6 +33,11 @@
 // Scales: m = sum y^2 / B^2 (Eq. 6), alpha = tau / sqrt(m + eps) (Eq. 7),
 // s = alpha * max|y| * (1/sqrt B) / Q_max (Eq. 9), codes of y * (Q_max / max|y|)
 // (Eq. 10, alpha cancels); equal to the literal order up to FP32 rounding.
+//
+// Ablations (Scheme): standard Hadamard + DS takes alpha = 1; DS only puts
+// the identity in place of H (y = G) with alpha = 1; ASH only stores s = 1
+// and converts Z = alpha y / sqrt(B) directly; E5M2 and INT8 codes use
+// Q_max = 57344 and 127.
 #include <cstring>
 
 #include <cuda.h>
@@ -86,12 +91,12 @@ struct TcCompressLayout {
     static constexpr int kSmem = kBytes + 1024;                    // slack for 1024-byte alignment
 };
 
-// Writes H_B (+-1 in bf16, Sylvester order) into shared memory as the K-major
-// B operand in the 128-byte swizzled layout: chunk c holds columns
-// [64c, 64c+64); row n of a chunk is 128 bytes whose 16-byte unit u sits at
-// unit u ^ (n % 8).
+// Writes H_B (+-1 in bf16, Sylvester order; the identity when `rotate` is
+// false) into shared memory as the K-major B operand in the 128-byte swizzled
+// layout: chunk c holds columns [64c, 64c+64); row n of a chunk is 128 bytes
+// whose 16-byte unit u sits at unit u ^ (n % 8).
 template <int B>
-__device__ void write_hadamard_sw128(uint8_t *h)
+__device__ void write_hadamard_sw128(uint8_t *h, bool rotate)
 {
     constexpr int kUnits = B * (B / 8);    // 16-byte units of H
     for (int idx = threadIdx.x; idx < kUnits; idx += blockDim.x) {
@@ -102,8 +107,12 @@ __device__ void write_hadamard_sw128(uint8_t *h)
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             const int k0 = 8 * u_all + 2 * q;
-            const uint32_t lo = (__popc(n & k0) & 1) ? 0xBF80u : 0x3F80u;
-            const uint32_t hi = (__popc(n & (k0 + 1)) & 1) ? 0xBF80u : 0x3F80u;
+            uint32_t lo = (__popc(n & k0) & 1) ? 0xBF80u : 0x3F80u;
+            uint32_t hi = (__popc(n & (k0 + 1)) & 1) ? 0xBF80u : 0x3F80u;
+            if (!rotate) {
+                lo = (n == k0) ? 0x3F80u : 0u;
+                hi = (n == k0 + 1) ? 0x3F80u : 0u;
+            }
             w[q] = lo | (hi << 16);
         }
         uint8_t *dst = h + c * (B * 128) + n * 128 + ((u ^ (n & 7)) * 16);
@@ -114,7 +123,7 @@ __device__ void write_hadamard_sw128(uint8_t *h)
 template <int B, int STAGES, int EPG, int NBG>
 __global__ void __launch_bounds__(tc_threads(EPG), 1)
     taco_compress_kernel(const __grid_constant__ CUtensorMap tmap_x, uint8_t *__restrict__ packed,
-                            int64_t nblocks, uint32_t *__restrict__ fault)
+                            int64_t nblocks, uint32_t *__restrict__ fault, const Scheme scheme)
 {
     using Lay = TcCompressLayout<B, STAGES, EPG, NBG>;
     constexpr int NOUT = Lay::NOUT;
@@ -173,7 +182,10 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     }
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
-    write_hadamard_sw128<Lay::kN>(base + Lay::kOffH);
+    const bool rotate = scheme.variant != 2;                        // DS only: no rotation
+    const bool adaptive = scheme.variant == 0 || scheme.variant == 3;  // alpha from Eqs. (6)-(7)
+    const bool dual_scale = scheme.variant != 3;                    // s from Eq. (9)
+    write_hadamard_sw128<Lay::kN>(base + Lay::kOffH, rotate);
     fence_proxy_async_smem();   // H is read by the tensor core (async proxy)
     tc_fence_before_sync();
     grid_dependency_wait();   // before any global access of this thread
@@ -240,18 +252,23 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                     // columns [0, 128) get H g0 + H g1 and [128, 256) get
                     // H g0 - H g1, where g0 / g1 are the block's two halves
                     // (A chunks 0-1 / 2-3); the minus is the negate-A bit.
+                    // Without rotation (identity) half h gets g_h only.
 #pragma unroll
                     for (int out_half = 0; out_half < 2; out_half++) {
 #pragma unroll
                         for (int in_half = 0; in_half < 2; in_half++) {
-                            const uint32_t id = (out_half == 1 && in_half == 1) ? (idesc | kMmaNegateA) : idesc;
+                            if (!rotate && in_half != out_half)
+                                continue;
+                            const uint32_t id =
+                                (rotate && out_half == 1 && in_half == 1) ? (idesc | kMmaNegateA) : idesc;
+                            const bool first = rotate ? in_half == 0 : true;
 #pragma unroll
                             for (int kk = 0; kk < Lay::kKSteps; kk++) {
                                 const uint32_t koff = (kk & 3) * 32;
                                 const uint64_t ad = sw128_kmajor_desc(
                                     a_stage + (2 * in_half + (kk >> 2)) * Lay::kChunkBytesA + koff);
                                 const uint64_t bd = sw128_kmajor_desc(h0 + (kk >> 2) * Lay::kChunkBytesH + koff);
-                                tc_mma_bf16(d + out_half * 128, ad, bd, id, (in_half == 0 && kk == 0) ? 0u : 1u);
+                                tc_mma_bf16(d + out_half * 128, ad, bd, id, (first && kk == 0) ? 0u : 1u);
                             }
                         }
                     }
@@ -301,11 +318,16 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             const float2 e01 = add2(e2[0], e2[1]), e23 = add2(e2[2], e2[3]);
             const float2 ee = add2(e01, e23);
             const float m = (ee.x + ee.y) * (1.0f / (static_cast<float>(B) * B));
-            const float alpha = __fdiv_rn(kTau, __fsqrt_rn(m + kEps));
+            const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(m + kEps)) : 1.0f;
+            const float rr = rotate ? rB : 1.0f;
+            const float qmax = code_qmax(scheme.code);
             float s = 0.f, k = 0.f;
-            if (ymax > 0.f) {
-                s = __fdiv_rn(__fmul_rn(__fmul_rn(alpha, ymax), rB), kQmax);
-                k = __fdiv_rn(kQmax, ymax);
+            if (!dual_scale) {            // ASH only: codes of Z = alpha r y, s = 1
+                s = 1.0f;
+                k = __fmul_rn(alpha, rr);
+            } else if (ymax > 0.f) {
+                s = __fdiv_rn(__fmul_rn(__fmul_rn(alpha, ymax), rr), qmax);
+                k = __fdiv_rn(qmax, ymax);
             }
 
             // The group's record tile buffer used NBG tiles ago must have been read
@@ -335,7 +357,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                     const float2 u0 = mul2(make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), k2);
                     const float2 u1 =
                         mul2(make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), k2);
-                    cw[j] = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
+                    cw[j] = encode4(scheme.code, u0.x, u0.y, u1.x, u1.y);
                 }
                 if (!(ymax > 0.f)) {
 #pragma unroll
@@ -426,8 +448,8 @@ KernelInfo compress_kernel_info(int block)
     }
 }
 
-cudaError_t launch_compress(int block, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault, int grid,
-                            cudaStream_t stream)
+cudaError_t launch_compress(int block, Scheme scheme, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault,
+                            int grid, cudaStream_t stream)
 {
     const KernelInfo ki = compress_kernel_info(block);
     if (!ki.fn)
@@ -435,7 +457,7 @@ cudaError_t launch_compress(int block, const void *tmap, void *packed, int64_t n
     CUtensorMap map;
     memcpy(&map, tmap, sizeof map);
     uint8_t *pp = static_cast<uint8_t *>(packed);
-    void *args[] = {&map, &pp, &nblocks, &fault};
+    void *args[] = {&map, &pp, &nblocks, &fault, &scheme};
     return launch_kernel(ki.fn, grid, ki.threads, ki.smem, stream, args);
 }
 

@@ -27,6 +27,12 @@
 // Block sizes: 128 (one block per row, H_128), 256 (one block per row, two
 // 128-code halves; H_256 = [[H, H], [H, -H]] with the negate-A bit), and 64
 // (two blocks per row, H = diag(H_64, H_64)).
+//
+// Ablations (Scheme): E5M2 codes are the MMA's operand as E5M2 (H in E5M2);
+// INT8 codes v are split as v = 16 floor(v / 16) + (v mod 16), both terms
+// exact in E4M3, and the two products accumulate in the same tensor memory
+// (SPLIT = 2); DS only puts the identity in place of H; the factor is
+// s / sqrt(B) / alpha, or s / alpha without rotation.
 #include <cstring>
 
 #include <cuda.h>
@@ -43,7 +49,7 @@ constexpr int kDRows = 128;        // MMA rows per tile
 constexpr int kDThreads = 320;     // 10 warps
 constexpr int kGroup = 128;        // threads of the transposer / epilogue groups
 
-template <int B, int RS, int AS, int NOUT>
+template <int B, int RS, int AS, int NOUT, int SPLIT>
 struct TcDecompressLayout {
     static constexpr int kBlocksPerRow = B == 64 ? 2 : 1;
     static constexpr int kTileBlocks = kDRows * kBlocksPerRow;
@@ -53,7 +59,8 @@ struct TcDecompressLayout {
     static constexpr int kAccCols = 128 * kHalves;                 // TMEM columns per tile
     static constexpr int kRec = B + 8;
     static constexpr int kRawBytes = kTileBlocks * kRec;
-    static constexpr int kAStageBytes = kDRows * kRowCodes;
+    static constexpr int kSplitBytes = kDRows * kRowCodes;         // one term of the codes
+    static constexpr int kAStageBytes = SPLIT * kSplitBytes;
     static constexpr int kAChunkBytes = kDRows * 128;
     static constexpr int kHBytes = 128 * 128;
     static constexpr int kOutRows = kTileBlocks;                   // rows of y per tile
@@ -82,11 +89,13 @@ struct TcDecompressLayout {
     static constexpr int kTmemCols = 2 * kAccCols;
 };
 
-// The MMA's B operand, K-major, 128-byte swizzle, E4M3 (+1 = 0x38, -1 = 0xB8):
-// H_128 for B = 128 / 256, diag(H_64, H_64) for B = 64.
+// The MMA's B operand, K-major, 128-byte swizzle, in E4M3 (+1 = 0x38,
+// -1 = 0xB8) or E5M2 (+1 = 0x3C, -1 = 0xBC): H_128 for B = 128 / 256,
+// diag(H_64, H_64) for B = 64, the identity when `rotate` is false.
 template <int B>
-__device__ void write_hadamard_e4m3_sw128(uint8_t *h)
+__device__ void write_hadamard_f8_sw128(uint8_t *h, bool e5m2, bool rotate)
 {
+    const uint32_t plus = e5m2 ? 0x3Cu : 0x38u, minus = e5m2 ? 0xBCu : 0xB8u;
     for (int idx = threadIdx.x; idx < 128 * 8; idx += blockDim.x) {
         const int n = idx / 8, u = idx % 8;
         uint32_t w[4];
@@ -97,10 +106,12 @@ __device__ void write_hadamard_e4m3_sw128(uint8_t *h)
             for (int b = 0; b < 4; b++) {
                 const int k = 16 * u + 4 * q + b;
                 uint32_t code;
-                if (B == 64)
-                    code = (n / 64 != k / 64) ? 0x00u : ((__popc((n & 63) & (k & 63)) & 1) ? 0xB8u : 0x38u);
+                if (!rotate)
+                    code = (n == k) ? plus : 0x00u;
+                else if (B == 64)
+                    code = (n / 64 != k / 64) ? 0x00u : ((__popc((n & 63) & (k & 63)) & 1) ? minus : plus);
                 else
-                    code = (__popc(n & k) & 1) ? 0xB8u : 0x38u;
+                    code = (__popc(n & k) & 1) ? minus : plus;
                 word |= code << (8 * b);
             }
             w[q] = word;
@@ -109,12 +120,12 @@ __device__ void write_hadamard_e4m3_sw128(uint8_t *h)
     }
 }
 
-template <int B, int RS, int AS, int NOUT>
+template <int B, int RS, int AS, int NOUT, int SPLIT>
 __global__ void __launch_bounds__(kDThreads, 1)
     taco_decompress_kernel(const __grid_constant__ CUtensorMap tmap_y, const uint8_t *__restrict__ packed,
-                              int64_t nblocks, uint32_t *__restrict__ fault)
+                              int64_t nblocks, uint32_t *__restrict__ fault, const Scheme scheme)
 {
-    using Lay = TcDecompressLayout<B, RS, AS, NOUT>;
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT, SPLIT>;
     constexpr int FS = Lay::FS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -181,7 +192,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
-    write_hadamard_e4m3_sw128<B>(base + Lay::kOffH);
+    const bool rotate = scheme.variant != 2;   // DS only: no rotation
+    const bool e5m2 = SPLIT == 1 && scheme.code == 1;
+    write_hadamard_f8_sw128<B>(base + Lay::kOffH, e5m2, rotate);
     fence_proxy_async_smem();
     tc_fence_before_sync();
     grid_dependency_wait();   // before any global access of this thread
@@ -219,7 +232,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     } else if (warp == 1) {
         // ---- MMA issuer ----------------------------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = mma_idesc_e4m3_f32(kDRows, 128);
+            const uint32_t idesc = e5m2 ? mma_idesc_e5m2_f32(kDRows, 128) : mma_idesc_e4m3_f32(kDRows, 128);
             const uint32_t h0 = sbase + Lay::kOffH;
             int i = 0;
             for (;; i++) {
@@ -236,14 +249,22 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 const uint32_t a_st = sbase + Lay::kOffA + j * Lay::kAStageBytes;
 #pragma unroll
                 for (int oh = 0; oh < Lay::kHalves; oh++) {
+                    bool first = true;
 #pragma unroll
-                    for (int ih = 0; ih < Lay::kAChunks; ih++) {
-                        const uint32_t id = (oh == 1 && ih == 1) ? (idesc | kMmaNegateA) : idesc;
+                    for (int sp = 0; sp < SPLIT; sp++) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; kk++) {   // 32 codes = 32 bytes per MMA
-                            const uint64_t ad = sw128_kmajor_desc(a_st + ih * Lay::kAChunkBytes + 32 * kk);
-                            const uint64_t bd = sw128_kmajor_desc(h0 + 32 * kk);
-                            tc_mma_f8(d + 128 * oh, ad, bd, id, (ih == 0 && kk == 0) ? 0u : 1u);
+                        for (int ih = 0; ih < Lay::kAChunks; ih++) {
+                            if (!rotate && Lay::kHalves == 2 && ih != oh)
+                                continue;   // identity: output half h takes input half h only
+                            const uint32_t id = (rotate && oh == 1 && ih == 1) ? (idesc | kMmaNegateA) : idesc;
+#pragma unroll
+                            for (int kk = 0; kk < 4; kk++) {   // 32 codes = 32 bytes per MMA
+                                const uint64_t ad = sw128_kmajor_desc(a_st + sp * Lay::kSplitBytes +
+                                                                      ih * Lay::kAChunkBytes + 32 * kk);
+                                const uint64_t bd = sw128_kmajor_desc(h0 + 32 * kk);
+                                tc_mma_f8(d + 128 * oh, ad, bd, id, (first && kk == 0) ? 0u : 1u);
+                            }
+                            first = false;
                         }
                     }
                 }
@@ -257,6 +278,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         // ---- transposers (warps 2..5): one MMA row per thread ---------------
         const int m = threadIdx.x - 64;    // 0..127
         const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
+        const float rr = rotate ? rB : 1.0f;
         for (int i = 0;; i++) {
             const int64_t t = sched.tile_warp(i);
             if (t < 0)
@@ -286,7 +308,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
                         w[2 * q + 1] = v.y;
                     }
                     const uint2 meta = from_global ? *reinterpret_cast<const uint2 *>(rg + B) : lds64(rs + B);
-                    f = __fdiv_rn(__fmul_rn(__uint_as_float(meta.y), rB), __uint_as_float(meta.x));
+                    f = __fdiv_rn(__fmul_rn(__uint_as_float(meta.y), rr), __uint_as_float(meta.x));
                 } else {
 #pragma unroll
                     for (int q = 0; q < B / 4; q++)
@@ -298,8 +320,28 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 for (int u = 0; u < B / 16; u++) {
                     const int ua = b * (B / 16) + u;          // unit index along the A row
                     const int chunk = ua / 8, uc = ua % 8;
-                    sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
-                           make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]));
+                    const uint32_t dst = a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16);
+                    if constexpr (SPLIT == 1) {
+                        sts128(dst, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]));
+                    } else {
+                        // INT8 code v = 16 * (v >> 4) + (v & 15), both terms as E4M3.
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            const uint32_t x = w[4 * u + q];
+                            float fh[4], fl[4];
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                const int v = static_cast<int>(static_cast<int8_t>(x >> (8 * e)));
+                                fh[e] = static_cast<float>((v >> 4) * 16);
+                                fl[e] = static_cast<float>(v & 15);
+                            }
+                            hi[q] = encode4(0, fh[0], fh[1], fh[2], fh[3]);
+                            lo[q] = encode4(0, fl[0], fl[1], fl[2], fl[3]);
+                        }
+                        sts128(dst, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+                        sts128(dst + Lay::kSplitBytes, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -396,12 +438,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
 }
 
-template <int B, int RS, int AS, int NOUT>
+template <int B, int RS, int AS, int NOUT, int SPLIT>
 struct TcDecompressConfig {
-    using Lay = TcDecompressLayout<B, RS, AS, NOUT>;
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT, SPLIT>;
     static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
     static_assert(Lay::kRawBytes % 16 == 0, "raw stage alignment");
-    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, RS, AS, NOUT>); }
+    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, RS, AS, NOUT, SPLIT>); }
     static KernelInfo info()
     {
         return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), kDThreads, Lay::kTileBlocks, 0};
@@ -418,16 +460,28 @@ struct TcDecompressConfig {
 #define TACO_DTC256_CFG 221
 #endif
 // Per block size, three digits: raw stages, A stages, output tiles.
-using DecompressTc64 = TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10>;
+using DecompressTc64 = TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 1>;
 using DecompressTc128 =
-    TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10>;
+    TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10, 1>;
 using DecompressTc256 =
-    TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10>;
+    TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10, 1>;
+// INT8 codes (two E4M3 terms per code: A stages twice as large).
+using DecompressI8x64 = TcDecompressConfig<64, 3, 2, 2, 2>;
+using DecompressI8x128 = TcDecompressConfig<128, 3, 2, 2, 2>;
+using DecompressI8x256 = TcDecompressConfig<256, 2, 1, 1, 2>;
 
 }  // namespace
 
-KernelInfo decompress_kernel_info(int block)
+KernelInfo decompress_kernel_info(int block, int code)
 {
+    if (code == 2) {
+        switch (block) {
+        case 64: return DecompressI8x64::info();
+        case 128: return DecompressI8x128::info();
+        case 256: return DecompressI8x256::info();
+        default: return KernelInfo{};
+        }
+    }
     switch (block) {
     case 64: return DecompressTc64::info();
     case 128: return DecompressTc128::info();
@@ -436,16 +490,16 @@ KernelInfo decompress_kernel_info(int block)
     }
 }
 
-cudaError_t launch_decompress(int block, const void *tmap_y, const void *packed, int64_t nblocks, uint32_t *fault,
-                              int grid, cudaStream_t stream)
+cudaError_t launch_decompress(int block, Scheme scheme, const void *tmap_y, const void *packed, int64_t nblocks,
+                              uint32_t *fault, int grid, cudaStream_t stream)
 {
-    const KernelInfo ki = decompress_kernel_info(block);
+    const KernelInfo ki = decompress_kernel_info(block, scheme.code);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     CUtensorMap map;
     memcpy(&map, tmap_y, sizeof map);
     const uint8_t *pp = static_cast<const uint8_t *>(packed);
-    void *args[] = {&map, &pp, &nblocks, &fault};
+    void *args[] = {&map, &pp, &nblocks, &fault, &scheme};
     return launch_kernel(ki.fn, grid, ki.threads, ki.smem, stream, args);
 }
 

@@ -201,12 +201,54 @@ __device__ __forceinline__ uint32_t e4m3x2_from_float2(float lo, float hi)
     return r;
 }
 
+// Same conversion to OCP E5M2 (round to nearest even, saturating to +-57344).
+__device__ __forceinline__ uint32_t e5m2x2_from_float2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Largest code magnitude of a code format (0 E4M3, 1 E5M2, 2 INT8).
+__device__ __forceinline__ float code_qmax(int code)
+{
+    return code == 0 ? 448.0f : code == 1 ? 57344.0f : 127.0f;
+}
+
+// Codes of four values, first value in the low byte.  INT8 rounds to the
+// nearest integer, ties to even; the callers keep |u| <= 127 (u = Q_max y /
+// max|y| rounds to at most 127, and a direct cast has |u| <= sqrt(B) <= 16).
+__device__ __forceinline__ uint32_t encode4(int code, float a, float b, float c, float d)
+{
+    if (code == 0)
+        return e4m3x2_from_float2(a, b) | (e4m3x2_from_float2(c, d) << 16);
+    if (code == 1)
+        return e5m2x2_from_float2(a, b) | (e5m2x2_from_float2(c, d) << 16);
+    const uint32_t ia = static_cast<uint32_t>(__float2int_rn(a)) & 0xffu;
+    const uint32_t ib = static_cast<uint32_t>(__float2int_rn(b)) & 0xffu;
+    const uint32_t ic = static_cast<uint32_t>(__float2int_rn(c)) & 0xffu;
+    const uint32_t id = static_cast<uint32_t>(__float2int_rn(d)) & 0xffu;
+    return ia | (ib << 8) | (ic << 16) | (id << 24);
+}
+
 // Cvt_FP32 (Eq. 11) of the two E4M3 codes in the low 16 bits of `pair`
 // (exact): low byte -> .x, high byte -> .y.
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair)
 {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// The two E5M2 codes in the low 16 bits of `pair` as floats (exact).
+__device__ __forceinline__ float2 e5m2x2_to_float2(uint32_t pair)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
     float lo, hi;
     asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
         : "=f"(lo), "=f"(hi)

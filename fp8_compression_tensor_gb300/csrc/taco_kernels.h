@@ -38,18 +38,27 @@ inline cudaError_t launch_kernel(const void *fn, int grid, int threads, size_t s
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// Compression scheme: the method (ASH + DS with E4M3 codes) or one of the
+// paper's ablations.  Variants: 0 ASH + DS, 1 standard Hadamard + DS
+// (alpha = 1), 2 DS only (alpha = 1, no rotation), 3 ASH only (s = 1).
+// Codes: 0 E4M3 (Q_max 448), 1 E5M2 (57344), 2 INT8 (127, ties to even).
+struct Scheme {
+    int variant;
+    int code;
+};
+
 KernelInfo compress_kernel_info(int block);
-KernelInfo decompress_kernel_info(int block);
-KernelInfo reduce_kernel_info(int block);
+KernelInfo decompress_kernel_info(int block, int code);   // code 2 (INT8) has its own kernel
+KernelInfo reduce_kernel_info(int block, int code);
 
 // `tmap` points to a CUtensorMap of x viewed as [nblocks, block] bf16, box
 // {64, 128}, 128-byte swizzle.
-cudaError_t launch_compress(int block, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault, int grid,
-                            cudaStream_t stream);
+cudaError_t launch_compress(int block, Scheme scheme, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault,
+                            int grid, cudaStream_t stream);
 // `tmap_y` points to a CUtensorMap of y viewed as [nblocks, block] bf16, box
 // {64, tile_blocks}, 128-byte swizzle.
-cudaError_t launch_decompress(int block, const void *tmap_y, const void *packed, int64_t nblocks, uint32_t *fault,
-                              int grid, cudaStream_t stream);
+cudaError_t launch_decompress(int block, Scheme scheme, const void *tmap_y, const void *packed, int64_t nblocks,
+                              uint32_t *fault, int grid, cudaStream_t stream);
 
 constexpr int kMaxShards = 16;
 
@@ -58,10 +67,11 @@ struct ReduceArgs {
     uint8_t *out;
     int64_t nblocks;
     int num_shards;
+    int variant;    // Scheme::variant (the code format selects the kernel)
 };
 
 // One CTA per tile of KernelInfo::tile_blocks blocks (tiles of CTAs that have
 // not started are taken over by running ones).
-cudaError_t launch_reduce(int block, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream);
+cudaError_t launch_reduce(int block, int code, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream);
 
 }  // namespace taco

@@ -20,6 +20,11 @@
 // the block's threads with xor-shuffles (every thread ends with the same bits),
 // and every thread stores its 16 codes directly (8-byte stores).
 //
+// Ablations: the decode of every code format is exact (E4M3 and E5M2 through
+// f16, INT8 as integers), W is the same for every variant, and the output
+// takes alpha' = 1 for standard Hadamard + DS and DS only (s' = max|W| / Q_max),
+// or s' = 1 and codes Cvt(alpha' W) for ASH only.
+//
 // Scheduling: one CTA per tile, one CTA per SM resident (shared memory); the
 // resident CTA takes its own tile, then the tiles of CTAs it cancels before
 // they start (cluster launch control, taco_sched.cuh).  The loader publishes a
@@ -72,16 +77,34 @@ struct ReduceLayout {
     static constexpr int kSmem = kBytes + 128;                        // slack for alignment
 };
 
+// Values of the four codes in `x`, first code in .x of the first pair.
+template <int CODE>
+__device__ __forceinline__ void decode4(uint32_t x, float2 &q0, float2 &q1)
+{
+    if constexpr (CODE == 0) {
+        q0 = e4m3x2_to_float2(x & 0xffffu);
+        q1 = e4m3x2_to_float2(x >> 16);
+    } else if constexpr (CODE == 1) {
+        q0 = e5m2x2_to_float2(x & 0xffffu);
+        q1 = e5m2x2_to_float2(x >> 16);
+    } else {
+        q0 = make_float2(static_cast<float>(static_cast<int8_t>(x)), static_cast<float>(static_cast<int8_t>(x >> 8)));
+        q1 = make_float2(static_cast<float>(static_cast<int8_t>(x >> 16)),
+                         static_cast<float>(static_cast<int8_t>(x >> 24)));
+    }
+}
+
 // w[0..15] += q[0..15] * f for the 16 codes in `c`, each product rounded on its
 // own before the add (so that a shard and its negation cancel exactly, as in
 // an FP32 sum of decoded shards).
+template <int CODE>
 __device__ __forceinline__ void accumulate_shard(float (&w)[kLaneCodes], uint4 c, float f)
 {
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int k = 0; k < 4; k++) {
-        const float2 q0 = e4m3x2_to_float2(words[k] & 0xffffu);
-        const float2 q1 = e4m3x2_to_float2(words[k] >> 16);
+        float2 q0, q1;
+        decode4<CODE>(words[k], q0, q1);
         // Scalar products (never contracted), packed sums.
         const float2 t0 = make_float2(__fmul_rn(q0.x, f), __fmul_rn(q0.y, f));
         const float2 t1 = make_float2(__fmul_rn(q1.x, f), __fmul_rn(q1.y, f));
@@ -99,7 +122,7 @@ __device__ __forceinline__ uint2 ldg_u2(const uint8_t *p)
     return *reinterpret_cast<const uint2 *>(p);
 }
 
-template <int B>
+template <int B, int CODE>
 __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const ReduceArgs args, uint32_t *fault)
 {
     using Lay = ReduceLayout<B>;
@@ -120,6 +143,8 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     const int lane = threadIdx.x & 31;
     const int P = args.num_shards;
     const int64_t nblocks = args.nblocks;
+    const bool adaptive = args.variant == 0 || args.variant == 3;   // alpha' from the energy of W
+    const bool dual_scale = args.variant != 3;                      // s' from max|W|
     // Stages of P record runs in the ring.
     const int stage_bytes = P * Lay::kRunBytes;
     int nst = kRingBytes / stage_bytes;
@@ -221,9 +246,9 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                     const uint2 m0 = lds64(r - kLaneCodes * part + B);
                     const uint2 a1 = lds64(r + Lay::kRunBytes), b1 = lds64(r + Lay::kRunBytes + 8);
                     const uint2 m1 = lds64(r + Lay::kRunBytes - kLaneCodes * part + B);
-                    accumulate_shard(w, make_uint4(a0.x, a0.y, b0.x, b0.y),
+                    accumulate_shard<CODE>(w, make_uint4(a0.x, a0.y, b0.x, b0.y),
                                      __fdividef(__uint_as_float(m0.y), __uint_as_float(m0.x)));
-                    accumulate_shard(w, make_uint4(a1.x, a1.y, b1.x, b1.y),
+                    accumulate_shard<CODE>(w, make_uint4(a1.x, a1.y, b1.x, b1.y),
                                      __fdividef(__uint_as_float(m1.y), __uint_as_float(m1.x)));
                 }
                 if (p < P) {
@@ -233,7 +258,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                     const uint32_t r = r0 + p * Lay::kRunBytes;
                     const uint2 a = lds64(r), b = lds64(r + 8);
                     const uint2 meta = lds64(r - kLaneCodes * part + B);
-                    accumulate_shard(w, make_uint4(a.x, a.y, b.x, b.y),
+                    accumulate_shard<CODE>(w, make_uint4(a.x, a.y, b.x, b.y),
                                      __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
                 }
             } else if (active) {
@@ -242,7 +267,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                     const uint8_t *r = shard_ptr[p] + blk * kRec;
                     const uint2 a = ldg_u2(r + kLaneCodes * part), b = ldg_u2(r + kLaneCodes * part + 8);
                     const uint2 meta = ldg_u2(r + B);
-                    accumulate_shard(w, make_uint4(a.x, a.y, b.x, b.y),
+                    accumulate_shard<CODE>(w, make_uint4(a.x, a.y, b.x, b.y),
                                      __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
                 }
             }
@@ -268,19 +293,25 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             }
 
             const float m = e * (1.0f / B);
-            const float alpha = __fdiv_rn(kTau, __fsqrt_rn(m + kEps));
-            float sc = 0.f;
+            const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(m + kEps)) : 1.0f;
+            constexpr float qmax = CODE == 0 ? 448.0f : CODE == 1 ? 57344.0f : 127.0f;
+            float sc = 0.f, kq = 0.f;
+            if (!dual_scale) {          // ASH only: codes of alpha' W, s' = 1
+                sc = 1.0f;
+                kq = alpha;
+            } else if (wmax > 0.f) {
+                sc = __fdiv_rn(__fmul_rn(alpha, wmax), qmax);
+                kq = __fdiv_rn(qmax, wmax);
+            }
             uint4 out = make_uint4(0u, 0u, 0u, 0u);
             if (wmax > 0.f) {
-                sc = __fdiv_rn(__fmul_rn(alpha, wmax), kQmax);
-                const float kq = __fdiv_rn(kQmax, wmax);
                 const float2 k2 = make_float2(kq, kq);
                 uint32_t o[4];
 #pragma unroll
                 for (int j = 0; j < 4; j++) {
                     const float2 u0 = mul2(make_float2(w[4 * j], w[4 * j + 1]), k2);
                     const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
-                    o[j] = e4m3x2_from_float2(u0.x, u0.y) | (e4m3x2_from_float2(u1.x, u1.y) << 16);
+                    o[j] = encode4(CODE, u0.x, u0.y, u1.x, u1.y);
                 }
                 out = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -296,28 +327,39 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     }
 }
 
-template <int B>
+template <int B, int CODE>
 KernelInfo info()
 {
-    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B>), ReduceLayout<B>::kSmem, kRThreads,
-                      ReduceLayout<B>::kT, kRThreads / 32};
+    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B, CODE>), ReduceLayout<B>::kSmem,
+                      kRThreads, ReduceLayout<B>::kT, kRThreads / 32};
 }
 
-}  // namespace
-
-KernelInfo reduce_kernel_info(int block)
+template <int CODE>
+KernelInfo info_for_block(int block)
 {
     switch (block) {
-    case 64: return info<64>();
-    case 128: return info<128>();
-    case 256: return info<256>();
+    case 64: return info<64, CODE>();
+    case 128: return info<128, CODE>();
+    case 256: return info<256, CODE>();
     default: return KernelInfo{};
     }
 }
 
-cudaError_t launch_reduce(int block, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream)
+}  // namespace
+
+KernelInfo reduce_kernel_info(int block, int code)
 {
-    const KernelInfo ki = reduce_kernel_info(block);
+    switch (code) {
+    case 0: return info_for_block<0>(block);
+    case 1: return info_for_block<1>(block);
+    case 2: return info_for_block<2>(block);
+    default: return KernelInfo{};
+    }
+}
+
+cudaError_t launch_reduce(int block, int code, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream)
+{
+    const KernelInfo ki = reduce_kernel_info(block, code);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     ReduceArgs a = args;

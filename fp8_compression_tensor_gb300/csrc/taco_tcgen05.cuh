@@ -106,6 +106,16 @@ __host__ __device__ constexpr uint32_t mma_idesc_e4m3_f32(int M, int N)
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Same with E5M2 A and B (format 1 of .kind::f8f6f4).
+__host__ __device__ constexpr uint32_t mma_idesc_e5m2_f32(int M, int N)
+{
+    return (1u << 4)                                   // D format: F32
+           | (1u << 7)                                 // A format: E5M2
+           | (1u << 10)                                // B format: E5M2
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 constexpr uint32_t kMmaNegateA = 1u << 13;   // instruction-descriptor bit: negate A
 
 // D[tmem] = A * B^T (+ D if accumulate): A is M x K, B is N x K, both from

@@ -66,11 +66,35 @@ typedef enum taco_status {
     TACO_ERR_BAD_SHARDS = 5,        /* num_shards < 1 or > TACO_MAX_SHARDS */
     TACO_ERR_OVERLAP = 6,           /* an output overlaps an input */
     TACO_ERR_CUDA = 7,              /* a CUDA runtime call or launch failed; see taco_last_cuda_error() */
-    TACO_ERR_DEVICE_FAULT = 8       /* taco_device_status(): a kernel gave up waiting */
+    TACO_ERR_DEVICE_FAULT = 8,      /* taco_device_status(): a kernel gave up waiting */
+    TACO_ERR_BAD_OPTIONS = 9        /* the _ex calls: options NULL, or unknown variant or code format */
 } taco_status_t;
 
 #define TACO_MAX_SHARDS 16
-#define TACO_ABI_VERSION 1
+#define TACO_ABI_VERSION 2
+
+/*
+ * Ablations of the method for the _ex calls (paper Sections 5.2.2, 5.3.1,
+ * 5.3.2 and 6).  The record layout is always [block codes | alpha | s].
+ */
+typedef enum taco_variant {
+    TACO_VARIANT_ASH_DS = 0,      /* the method: Adaptive Scale + Hadamard + Dual-Scale */
+    TACO_VARIANT_HADAMARD_DS = 1, /* standard Hadamard + Dual-Scale: alpha = 1 (Section 5.3.1) */
+    TACO_VARIANT_DS_ONLY = 2,     /* Dual-Scale only: alpha = 1, no rotation (Section 5.2.2) */
+    TACO_VARIANT_ASH_ONLY = 3     /* ASH only: s = 1, Z cast directly (Section 5.2.2) */
+} taco_variant_t;
+
+typedef enum taco_code {
+    TACO_CODE_E4M3 = 0,           /* OCP E4M3FN, Q_max = 448: the method */
+    TACO_CODE_E5M2 = 1,           /* OCP E5M2, Q_max = 57344, nearest even, saturating (Section 5.3.2) */
+    TACO_CODE_INT8 = 2            /* int8, Q_max = 127, nearest integer with ties to even (Sections 2, 6) */
+} taco_code_t;
+
+typedef struct taco_options {
+    int block;                    /* 64, 128 or 256 */
+    int variant;                  /* taco_variant_t */
+    int code;                     /* taco_code_t */
+} taco_options_t;
 
 /* Bytes of the packed buffer for a [rows, hidden] tensor: (rows*hidden/block)*(block+8).
  * Returns -1 for an unsupported block, a bad shape or an overflow. */
@@ -117,6 +141,27 @@ TACO_API taco_status_t taco_decompress(const void *packed_in, int64_t rows, int6
  */
 TACO_API taco_status_t taco_reduce_shards(const void *const *packed_shards, int num_shards, int64_t rows,
                                  int64_t hidden, int block, void *packed_out, taco_stream_t stream);
+
+/*
+ * The three calls above for any variant and code format (taco_options_t; the
+ * plain calls are block = options->block, TACO_VARIANT_ASH_DS, TACO_CODE_E4M3).
+ * Per block, with y the Hadamard rotation H_B G (G itself for DS only), Z =
+ * alpha y / sqrt(B) and Q_max of the code format:
+ *   ASH + DS            alpha = tau / sigma, s = max|Z| / Q_max, q = Cvt(Z / s)
+ *   standard Hadamard   alpha = 1,           s = max|Z| / Q_max, q = Cvt(Z / s)
+ *   DS only             alpha = 1, Z = G,    s = max|G| / Q_max, q = Cvt(G / s)
+ *   ASH only            alpha = tau / sigma, s = 1,              q = Cvt(Z)
+ * and decompression computes (Cvt^-1(q) s, rotated back unless DS only) / alpha.
+ * A record must be decoded and reduced with the options it was written with.
+ * options == NULL or an unknown variant or code: TACO_ERR_BAD_OPTIONS.
+ */
+TACO_API taco_status_t taco_compress_ex(const void *x_bf16, int64_t rows, int64_t hidden,
+                                        const taco_options_t *options, void *packed_out, taco_stream_t stream);
+TACO_API taco_status_t taco_decompress_ex(const void *packed_in, int64_t rows, int64_t hidden,
+                                          const taco_options_t *options, void *y_bf16_out, taco_stream_t stream);
+TACO_API taco_status_t taco_reduce_shards_ex(const void *const *packed_shards, int num_shards, int64_t rows,
+                                             int64_t hidden, const taco_options_t *options, void *packed_out,
+                                             taco_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's fault

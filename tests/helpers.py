@@ -71,9 +71,23 @@ def rel_l2(xhat, x) -> float:
     return float(np.linalg.norm(xhat - x) / nx) if nx > 0 else float(np.linalg.norm(xhat))
 
 
-def code_step_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
-    """Distance in E4M3 grid steps between codes a and b (same sign), with +0
-    and -0 counted as the same value; a sign change counts as a large step."""
+def decode_table(code: int = 0) -> np.ndarray:
+    """float64 value of each code byte: E4M3 (0) and E5M2 (1) as PyTorch
+    decodes them, INT8 (2) as two's complement."""
+    import torch
+    if code == 2:
+        return np.arange(256, dtype=np.uint8).view(np.int8).astype(np.float64)
+    dt = torch.float8_e4m3fn if code == 0 else torch.float8_e5m2
+    return torch.arange(256, dtype=torch.uint8).view(dt).to(torch.float64).numpy()
+
+
+def code_step_distance(a: np.ndarray, b: np.ndarray, code: int = 0) -> np.ndarray:
+    """Distance in grid steps between codes a and b of a format (E4M3 / E5M2:
+    sign-magnitude, +0 and -0 the same value, a sign change adds the two
+    magnitudes; INT8: the difference of the integers)."""
+    if code == 2:
+        return np.abs(np.asarray(a, dtype=np.uint8).view(np.int8).astype(np.int32)
+                      - np.asarray(b, dtype=np.uint8).view(np.int8).astype(np.int32))
     a = np.asarray(a, dtype=np.int32)
     b = np.asarray(b, dtype=np.int32)
     ma, mb = a & 0x7F, b & 0x7F

@@ -35,14 +35,14 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_host_side_queries(lib):
     import fp8_compression_tensor_gb300 as t
-    assert lib.taco_abi_version() == 1
+    assert lib.taco_abi_version() == 2
     assert t.compressed_bytes(8192, 4096, 128) == 8192 * 4096 // 128 * 136
     assert t.compressed_bytes(0, 4096, 64) == 0
     assert lib.taco_compressed_bytes(16, 100, 64) == -1
     assert lib.taco_compressed_bytes(16, 128, 32) == -1
     assert lib.taco_compressed_bytes(-1, 128, 128) == -1
     assert lib.taco_compressed_bytes(1 << 40, 1 << 40, 128) == -1
-    for s in range(9):
+    for s in range(10):
         assert lib.taco_status_string(s)
     # Argument errors are found before any CUDA call.
     assert lib.taco_compress(None, 4, 100, 64, None, None) == 2
@@ -53,6 +53,27 @@ def test_host_side_queries(lib):
     ptrs = (ctypes.c_void_p * 1)(16)
     assert lib.taco_reduce_shards(ptrs, 0, 4, 128, 128, 32, None) == 5
     assert lib.taco_reduce_shards(ptrs, 17, 4, 128, 128, 32, None) == 5
+
+
+def test_options_validated_on_host(lib):
+    """The _ex calls check their options before anything else."""
+    from fp8_compression_tensor_gb300._binding import _Options
+    optp = ctypes.POINTER(_Options)
+    for fn in (lib.taco_compress_ex, lib.taco_decompress_ex):
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, optp, ctypes.c_void_p, ctypes.c_void_p]
+        assert fn(None, 4, 128, None, None, None) == 9
+        assert fn(None, 4, 128, ctypes.byref(_Options(128, 4, 0)), None, None) == 9
+        assert fn(None, 4, 128, ctypes.byref(_Options(128, 0, 3)), None, None) == 9
+        assert fn(None, 4, 128, ctypes.byref(_Options(128, -1, 0)), None, None) == 9
+        assert fn(None, 4, 128, ctypes.byref(_Options(96, 1, 1)), None, None) == 3
+        assert fn(None, 4, 100, ctypes.byref(_Options(64, 2, 2)), None, None) == 2
+        assert fn(None, 4, 128, ctypes.byref(_Options(128, 3, 1)), None, None) == 1
+        assert fn(0, 0, 128, ctypes.byref(_Options(128, 1, 2)), 0, None) == 0
+    lib.taco_reduce_shards_ex.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int64,
+                                          ctypes.c_int64, optp, ctypes.c_void_p, ctypes.c_void_p]
+    ptrs = (ctypes.c_void_p * 1)(16)
+    assert lib.taco_reduce_shards_ex(ptrs, 1, 4, 128, None, 32, None) == 9
+    assert lib.taco_reduce_shards_ex(ptrs, 0, 4, 128, ctypes.byref(_Options(128, 1, 1)), 32, None) == 5
 
 
 def test_binding_refuses_cpu_tensors():

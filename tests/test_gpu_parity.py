@@ -173,7 +173,7 @@ def test_argument_errors_launch_nothing(taco):
     assert torch.all(out == 7)                                           # untouched
     with pytest.raises(taco.TacoError):
         taco.compress(x, 96)
-    assert lib.taco_abi_version() == 1
+    assert lib.taco_abi_version() == 2
 
 
 def test_streams_are_respected(taco):
