@@ -72,6 +72,10 @@ def parse_args():
     ap.add_argument("--workload", default="gpt_activation_8192x4096", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--block", type=int, default=128)
     ap.add_argument("--shards", type=int, default=8)
+    ap.add_argument("--variant", default="ash_ds", choices=["ash_ds", "hadamard_ds", "ds_only", "ash_only"],
+                    help="ablation variant (the method is ash_ds)")
+    ap.add_argument("--code", default="e4m3", choices=["e4m3", "e5m2", "int8"],
+                    help="code format (the method is e4m3)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -328,14 +332,16 @@ def run_taco(args, rank, world):
     segs = [[packs[r][p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)] for r in range(R)]
     stream = torch.cuda.Stream(dev)
 
+    scheme = {"variant": args.variant, "code": args.code}
+
     def op_compress(r):
-        taco.compress(xs[r], block, out=packs[r], stream=stream)
+        taco.compress(xs[r], block, out=packs[r], stream=stream, **scheme)
 
     def op_reduce(r):
-        taco.reduce_shards(segs[r], seg_rows, hidden, block, out=reds[r], stream=stream)
+        taco.reduce_shards(segs[r], seg_rows, hidden, block, out=reds[r], stream=stream, **scheme)
 
     def op_decompress(r):
-        taco.decompress(packs[r], rows, hidden, block, out=ys[r], stream=stream)
+        taco.decompress(packs[r], rows, hidden, block, out=ys[r], stream=stream, **scheme)
 
     def step(k):
         op_compress(k % R)
@@ -412,8 +418,47 @@ def run_taco(args, rank, world):
             solo_ms[name] = a.elapsed_time(b) / (reps * R)
     tot = max_over_ranks([solo_ms["compress"], solo_ms["reduce"], solo_ms["decompress"]], device=dev)
     solo_ms = dict(zip(("compress", "reduce", "decompress"), tot))
+
+    # Workloads of P seeded shards (the owner's step of the two-shot AllReduce
+    # on full-size shards): the reduce of the P packed tensors, timed alone.
+    full_reduce = None
+    if len(w.seeds) > 1:
+        Pf = len(w.seeds)
+        xsf = [torch.from_numpy(w.tensor(seed=sd).view(np.int16)).view(torch.bfloat16).to(dev).view(rows, hidden)
+               for sd in w.seeds]
+        full = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(Pf)]
+        full_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            for p_ in range(Pf):
+                taco.compress(xsf[p_], block, out=full[p_], stream=stream, **scheme)
+            del xsf
+            g_full = capture(lambda: taco.reduce_shards(full, rows, hidden, block, out=full_out, stream=stream,
+                                                        **scheme))
+            for _ in range(3):
+                g_full.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps_f = 50
+            a.record(stream)
+            for _ in range(reps_f):
+                g_full.replay()
+            b.record(stream)
+            stream.synchronize()
+        ms_f = max_over_ranks([a.elapsed_time(b) / reps_f], device=dev)[0]
+        alg_f = (Pf + 1) * nbytes
+        full_reduce = {"ms": ms_f, "shards": Pf, "algorithmic_bytes": alg_f, "hbm_gbs": alg_f / ms_f / 1e6,
+                       "logical_bf16_gbs": Pf * 2 * n / ms_f / 1e6,
+                       "what": f"reduce of {Pf} full-size packed shards (seeds {list(w.seeds)}), "
+                               f"back-to-back graph replays"}
     x, packed, reduced, y = xs[0], packs[0], reds[0], ys[0]
     segments = segs[0]
+
+    # Reconstruction error of the round trip (paper Eq. 21), fp64 over the tensor.
+    with torch.cuda.stream(stream):
+        op_compress(0)
+        op_decompress(0)
+    stream.synchronize()
+    xd, yd = x.double(), y.double()
+    rel_l2 = float(torch.linalg.vector_norm(yd - xd) / torch.linalg.vector_norm(xd))
 
     # End to end through the public API with host buffers: pinned H2D of the
     # step's input, the three calls, D2H of the decompressed tensor and of
@@ -425,9 +470,9 @@ def run_taco(args, rank, world):
 
         def e2e_step():
             x.copy_(x_pinned, non_blocking=True)
-            taco.compress(x, block, out=packed, stream=stream)
-            taco.reduce_shards(segments, seg_rows, hidden, block, out=reduced, stream=stream)
-            taco.decompress(packed, rows, hidden, block, out=y, stream=stream)
+            taco.compress(x, block, out=packed, stream=stream, **scheme)
+            taco.reduce_shards(segments, seg_rows, hidden, block, out=reduced, stream=stream, **scheme)
+            taco.decompress(packed, rows, hidden, block, out=y, stream=stream, **scheme)
             y_pinned.copy_(y, non_blocking=True)
             r_pinned.copy_(reduced, non_blocking=True)
 
@@ -464,6 +509,7 @@ def run_taco(args, rank, world):
         t = avg_ms[op] * 1e-3
         ops[op] = {"ms": avg_ms[op], "bf16_gbs": 2 * n / t / 1e9,
                    "hbm_gbs": alg[op] / t / 1e9, "frac_of_measured_hbm": alg[op] / t / 1e9 / peak,
+                   "frac_of_nominal_8tbs": alg[op] / t / 1e9 / 8000.0,
                    "algorithmic_bytes": alg[op], "launches_timed": reps * R}
     dom = max(avg_ms, key=avg_ms.get)
     achieved = alg[dom] / (avg_ms[dom] * 1e-3) / 1e9
@@ -507,6 +553,7 @@ def run_taco(args, rank, world):
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "rows": rows, "hidden": hidden, "block": block, "reduce_shards": P,
+                   "variant": args.variant, "code": args.code,
                    "step": "compress + reduce_shards(P row-slices of the packed tensor) + decompress",
                    "bytes_per_step": "6N: 2N compressed + 2N logical bf16 of the reduced segments + 2N decompressed",
                    "l2": (f"no flush; inputs larger than L2: {R} rotating buffer sets of {set_bytes / 1e6:.1f} MB "
@@ -516,6 +563,8 @@ def run_taco(args, rank, world):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops,
         "ops_sum_ms": sum(avg_ms.values()),
+        "quality": {"rel_l2_round_trip": rel_l2},
+        "reduce_full_shards": full_reduce,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
