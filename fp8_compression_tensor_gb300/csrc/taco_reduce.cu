@@ -1,6 +1,6 @@
 // taco_reduce.cu -- receive-side local reduction of TACO's two-shot compressed
-// AllReduce (Section 4.4.2, "one compressed AlltoAll operation followed by a
-// single local reduction") for GB300 (sm_103a): P packed shards in local HBM
+// AllReduce (Section 4.4.2: a compressed all-to-all exchange, then one
+// reduction per owner) for GB300 (sm_103a): P packed shards in local HBM
 // are decoded to FP32, summed, and the sum is compressed once.
 //
 // No rotation is needed.  Shard p decodes to G'_p = R (q_p s_p / alpha_p) with

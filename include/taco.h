@@ -16,7 +16,8 @@
  * Tensor layout: a row-major bf16 tensor [rows, hidden] with hidden % block == 0,
  * seen as M = rows*hidden/block contiguous blocks of `block` elements (Eq. 5).
  *
- * Packed layout ("zero-copy metadata layout", Section 4.4.2): one buffer of
+ * Packed layout (Section 4.4.2, the codes with their scales stored right
+ * after them in the same buffer): one buffer of
  * M records; record k starts at byte k*(block+8) and holds the block's `block`
  * E4M3 codes in element order, then alpha_k and s_k as little-endian float32.
  * taco_compressed_bytes() gives its size.
@@ -127,8 +128,8 @@ TACO_API taco_status_t taco_decompress(const void *packed_in, int64_t rows, int6
 
 /*
  * Receive-side local reduction of the two-shot compressed AllReduce (Section
- * 4.4.2: "one compressed AlltoAll operation followed by a single local
- * reduction"): the P packed shards of the same [rows, hidden] tensor are
+ * 4.4.2: after the compressed all-to-all exchange, each owner reduces its
+ * segment once): the P packed shards of the same [rows, hidden] tensor are
  * decoded to FP32 (Eqs. 11-13, no bf16 rounding), summed, and the FP32 sum is
  * compressed once (Eqs. 6-10) into packed_out.
  *

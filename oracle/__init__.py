@@ -14,7 +14,7 @@ block energy (Eq. 6), Adaptive Scale (Eq. 7), orthogonal Hadamard rotation
 inverse (Eqs. 11-13); ``reduce_shards`` is the single local reduction of the
 two-shot AllReduce (Section 4.4.2).
 
-Packed format (Section 4.4.2, zero-copy metadata layout): record k occupies
+Packed format (Section 4.4.2, metadata stored right after the codes): record k occupies
 bytes [k*(B+8), (k+1)*(B+8)): B E4M3 codes, then alpha_k and s_k as
 little-endian float32.
 

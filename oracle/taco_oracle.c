@@ -31,11 +31,11 @@
  *   - an all-zero block (max|Z| = 0) stores s = 0 and all codes 0x00;
  *   - the packed record of block k sits at byte k*(B+8): B E4M3 codes in
  *     element order, then alpha_k, then s_k, both little-endian binary32
- *     (Section 4.4.2, zero-copy metadata layout);
+ *     (Section 4.4.2, metadata stored right after the codes);
  *   - the shard reduction decodes each shard to binary32 (no bf16 rounding),
  *     sums the shards left to right in shard order, and compresses the sum
- *     once from binary32 (Section 4.4.2, two-shot AllReduce: one compressed
- *     AlltoAll followed by a single local reduction).
+ *     once from binary32 (Section 4.4.2, two-shot AllReduce: a compressed
+ *     all-to-all exchange, then one reduction per owner).
  *
  * Ablation variants and code formats (the "_ex" entry points; the plain
  * entry points are ASH + DS with E4M3):
