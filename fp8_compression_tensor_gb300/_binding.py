@@ -30,7 +30,7 @@ STATUS = {
     9: "TACO_ERR_BAD_OPTIONS",
 }
 MAX_SHARDS = 16
-SUPPORTED_BLOCKS = (64, 128, 256)
+SUPPORTED_BLOCKS = (32, 64, 128, 256, 512)
 # Ablations (taco_variant_t, taco_code_t of include/taco.h).
 VARIANTS = {"ash_ds": 0, "hadamard_ds": 1, "ds_only": 2, "ash_only": 3}
 CODES = {"e4m3": 0, "e5m2": 1, "int8": 2}

@@ -33,9 +33,16 @@ struct DeviceState {
 
 DeviceState g_devices[kMaxDevices];
 
-int block_index(int block)
+bool block_supported(int block)
 {
-    return block == 64 ? 0 : block == 128 ? 1 : block == 256 ? 2 : -1;
+    return block == 32 || block == 64 || block == 128 || block == 256 || block == 512;
+}
+
+// Blocks 64, 128 and 256 run on the tensor-core kernels, 32 and 512 on the
+// warp-per-block codec (the shard reduce takes every block size).
+bool tensor_core_block(int block)
+{
+    return block == 64 || block == 128 || block == 256;
 }
 
 taco_status_t cuda_fail(cudaError_t e)
@@ -62,15 +69,19 @@ void init_device(DeviceState &st)
         e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    const int blocks[3] = {64, 128, 256};
-    for (int i = 0; i < 3 && e == cudaSuccess; i++) {
-        e = init_kernel(compress_kernel_info(blocks[i]), &st.ctas_per_sm);
-        for (int code = 0; code < 3 && e == cudaSuccess; code++) {
-            if (code != 1)   // E4M3 and E5M2 share a decompress kernel
+    const int blocks[5] = {32, 64, 128, 256, 512};
+    for (int i = 0; i < 5 && e == cudaSuccess; i++) {
+        if (tensor_core_block(blocks[i])) {
+            e = init_kernel(compress_kernel_info(blocks[i]), &st.ctas_per_sm);
+            for (int code = 0; code < 3 && e == cudaSuccess; code += 2)   // E5M2 shares the E4M3 kernel
                 e = init_kernel(decompress_kernel_info(blocks[i], code), &st.ctas_per_sm);
+        } else {
+            e = init_kernel(warp_codec_info(blocks[i], true), &st.ctas_per_sm);
             if (e == cudaSuccess)
-                e = init_kernel(reduce_kernel_info(blocks[i], code), &st.ctas_per_sm);
+                e = init_kernel(warp_codec_info(blocks[i], false), &st.ctas_per_sm);
         }
+        for (int code = 0; code < 3 && e == cudaSuccess; code++)
+            e = init_kernel(reduce_kernel_info(blocks[i], code), &st.ctas_per_sm);
     }
     st.init_error = e;
 }
@@ -144,7 +155,7 @@ bool overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes)
 // Validates block and shape; on success sets the element count and packed bytes.
 taco_status_t check_shape(int64_t rows, int64_t hidden, int block, int64_t *n, int64_t *packed_bytes)
 {
-    if (block_index(block) < 0)
+    if (!block_supported(block))
         return TACO_ERR_UNSUPPORTED_BLOCK;
     if (rows < 0 || hidden < 0 || hidden % block != 0)
         return TACO_ERR_BAD_SHAPE;
@@ -182,9 +193,16 @@ taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, in
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != TACO_OK)
         return st;
+    const int64_t nblocks = n / block;
+    if (!tensor_core_block(block)) {
+        const int64_t want = (nblocks + 7) / 8, cap = static_cast<int64_t>(dev->sm_count) * 16;
+        const cudaError_t e = launch_warp_compress(block, scheme, x_bf16, packed_out, nblocks,
+                                                   static_cast<int>(want < cap ? want : cap),
+                                                   reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? TACO_OK : cuda_fail(e);
+    }
     // Tensor-core kernel over tiles of 128 blocks: one CTA per tile, of which
     // one per SM runs and takes the tiles of CTAs it cancels before they start.
-    const int64_t nblocks = n / block;
     const KernelInfo ki = compress_kernel_info(block);
     const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
     if (ntiles > INT32_MAX)
@@ -215,9 +233,16 @@ taco_status_t decompress_impl(const void *packed_in, int64_t rows, int64_t hidde
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != TACO_OK)
         return st;
+    const int64_t nblocks = n / block;
+    if (!tensor_core_block(block)) {
+        const int64_t want = (nblocks + 7) / 8, cap = static_cast<int64_t>(dev->sm_count) * 16;
+        const cudaError_t e = launch_warp_decompress(block, scheme, packed_in, y_bf16_out, nblocks,
+                                                     static_cast<int>(want < cap ? want : cap),
+                                                     reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? TACO_OK : cuda_fail(e);
+    }
     // Tensor-core kernel over tiles of 128 (B = 64: 256) blocks: one CTA per
     // tile, of which one per SM runs and takes the tiles of CTAs it cancels.
-    const int64_t nblocks = n / block;
     const KernelInfo ki = decompress_kernel_info(block, scheme.code);
     const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
     if (ntiles > INT32_MAX)
@@ -368,7 +393,7 @@ const char *taco_status_string(taco_status_t status)
     case TACO_OK: return "TACO_OK";
     case TACO_ERR_NULL_POINTER: return "TACO_ERR_NULL_POINTER: a required pointer is NULL";
     case TACO_ERR_BAD_SHAPE: return "TACO_ERR_BAD_SHAPE: rows/hidden negative, hidden not a multiple of the block, or too large";
-    case TACO_ERR_UNSUPPORTED_BLOCK: return "TACO_ERR_UNSUPPORTED_BLOCK: block must be 64, 128 or 256";
+    case TACO_ERR_UNSUPPORTED_BLOCK: return "TACO_ERR_UNSUPPORTED_BLOCK: block must be 32, 64, 128, 256 or 512";
     case TACO_ERR_MISALIGNED: return "TACO_ERR_MISALIGNED: device pointers must be 16-byte aligned";
     case TACO_ERR_BAD_SHARDS: return "TACO_ERR_BAD_SHARDS: num_shards must be in [1, 16]";
     case TACO_ERR_OVERLAP: return "TACO_ERR_OVERLAP: an output overlaps an input";

@@ -338,9 +338,11 @@ template <int CODE>
 KernelInfo info_for_block(int block)
 {
     switch (block) {
+    case 32: return info<32, CODE>();
     case 64: return info<64, CODE>();
     case 128: return info<128, CODE>();
     case 256: return info<256, CODE>();
+    case 512: return info<512, CODE>();
     default: return KernelInfo{};
     }
 }

@@ -33,7 +33,9 @@
  *     launch and leave every output untouched.
  *   - rows == 0 or hidden == 0 is an empty tensor: TACO_OK, nothing launched,
  *     pointers may be NULL.
- *   - Supported blocks: 64, 128, 256 (TACO_ERR_UNSUPPORTED_BLOCK otherwise).
+ *   - Supported blocks: 32, 64, 128, 256, 512 (TACO_ERR_UNSUPPORTED_BLOCK
+ *     otherwise; Section 5.3.3 ablates these sizes).  64, 128 and 256 run on
+ *     the tensor cores, 32 and 512 on a warp-per-block CUDA-core codec.
  *   - Inputs must be finite with |x| < 2^56; beyond that the FP32 block
  *     energy of Eq. (6) can overflow and the output is unspecified.
  *   - Kernels that wait on the copy engine give up after about one second,
@@ -62,7 +64,7 @@ typedef enum taco_status {
     TACO_OK = 0,
     TACO_ERR_NULL_POINTER = 1,      /* a required pointer is NULL */
     TACO_ERR_BAD_SHAPE = 2,         /* rows < 0, hidden < 0, hidden % block != 0, or size overflow */
-    TACO_ERR_UNSUPPORTED_BLOCK = 3, /* block not in {64, 128, 256} */
+    TACO_ERR_UNSUPPORTED_BLOCK = 3, /* block not in {32, 64, 128, 256, 512} */
     TACO_ERR_MISALIGNED = 4,        /* a device pointer is not 16-byte aligned */
     TACO_ERR_BAD_SHARDS = 5,        /* num_shards < 1 or > TACO_MAX_SHARDS */
     TACO_ERR_OVERLAP = 6,           /* an output overlaps an input */
@@ -92,7 +94,7 @@ typedef enum taco_code {
 } taco_code_t;
 
 typedef struct taco_options {
-    int block;                    /* 64, 128 or 256 */
+    int block;                    /* 32, 64, 128, 256 or 512 */
     int variant;                  /* taco_variant_t */
     int code;                     /* taco_code_t */
 } taco_options_t;

@@ -39,7 +39,10 @@ def test_host_side_queries(lib):
     assert t.compressed_bytes(8192, 4096, 128) == 8192 * 4096 // 128 * 136
     assert t.compressed_bytes(0, 4096, 64) == 0
     assert lib.taco_compressed_bytes(16, 100, 64) == -1
-    assert lib.taco_compressed_bytes(16, 128, 32) == -1
+    assert lib.taco_compressed_bytes(16, 128, 32) == 16 * 128 // 32 * 40
+    assert lib.taco_compressed_bytes(16, 1024, 512) == 16 * 1024 // 512 * 520
+    assert lib.taco_compressed_bytes(16, 128, 96) == -1
+    assert lib.taco_compressed_bytes(16, 512, 1024) == -1
     assert lib.taco_compressed_bytes(-1, 128, 128) == -1
     assert lib.taco_compressed_bytes(1 << 40, 1 << 40, 128) == -1
     for s in range(10):

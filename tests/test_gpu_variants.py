@@ -54,9 +54,12 @@ def exact_u(bits, B, variant, code):
     return np.where(m > 0, qmax * y / np.where(m > 0, m, 1.0), 0.0)
 
 
+BLOCKS = [32, 64, 128, 256, 512]
+
+
 @pytest.mark.parametrize("code", CODES)
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("B", [64, 128, 256])
+@pytest.mark.parametrize("B", BLOCKS)
 def test_compress_decompress(taco, B, variant, code):
     bits = workloads.generate("laplace_outliers", ROWS, HIDDEN, 11 + variant + 4 * code)
     n = bits.size
@@ -77,7 +80,7 @@ def test_compress_decompress(taco, B, variant, code):
 
 @pytest.mark.parametrize("code", CODES)
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("B", [64, 128, 256])
+@pytest.mark.parametrize("B", BLOCKS)
 def test_reduce(taco, B, variant, code):
     rows, hidden, P = 96, 1024, 3
     shards = [oracle.compress(workloads.generate("student_t_channels", rows, hidden, p), B, variant, code)
@@ -115,6 +118,26 @@ def test_special_blocks(taco, variant, code):
     compare_records(r, oracle.reduce_shards([ref, neg], bits.size, B, variant, code), B, code=code)
     c, a, s = records(r, B)
     assert np.all(s == (1.0 if variant == 3 else 0.0))
+    assert taco.device_status() == 0
+
+
+@pytest.mark.parametrize("B", [32, 512])
+def test_small_and_large_blocks_ragged(taco, B):
+    """Blocks 32 and 512 (the warp-per-block codec) on shapes with an odd
+    number of blocks, a partial last tile of the shard reduce and a single
+    block, for the method itself."""
+    for rows, hidden in ((301, 3 * B), (1, B), (7, 5 * B)):
+        bits = workloads.generate("gaussian_sparse", rows, hidden, rows)
+        ref = oracle.compress(bits, B)
+        got = taco.compress(to_dev(bits).view(rows, hidden), B).cpu().numpy()
+        compare_records(got, ref, B)
+        y = from_dev(taco.decompress(torch.from_numpy(ref).cuda(), rows, hidden, B))
+        compare_decoded(y, oracle.decompress(ref, bits.size, B), B)
+        shards = [ref, oracle.compress(workloads.generate("laplace_outliers", rows, hidden, 99), B)]
+        r = taco.reduce_shards([torch.from_numpy(x).cuda() for x in shards], rows, hidden, B).cpu().numpy()
+        u = reduce_exact_u(shards, B)
+        compare_records(r, oracle.reduce_shards(shards, bits.size, B), B,
+                        ambiguous=near_midpoint(u) | noise_zone(u, B))
     assert taco.device_status() == 0
 
 
