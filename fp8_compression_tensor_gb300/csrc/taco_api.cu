@@ -195,7 +195,9 @@ taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, in
         return st;
     const int64_t nblocks = n / block;
     if (!tensor_core_block(block)) {
-        const int64_t want = (nblocks + 7) / 8, cap = static_cast<int64_t>(dev->sm_count) * 16;
+        const KernelInfo wk = warp_codec_info(block, true);
+        const int64_t want = (nblocks + wk.tile_blocks - 1) / wk.tile_blocks;
+        const int64_t cap = static_cast<int64_t>(dev->sm_count) * 16;
         const cudaError_t e = launch_warp_compress(block, scheme, x_bf16, packed_out, nblocks,
                                                    static_cast<int>(want < cap ? want : cap),
                                                    reinterpret_cast<cudaStream_t>(stream));
@@ -235,7 +237,9 @@ taco_status_t decompress_impl(const void *packed_in, int64_t rows, int64_t hidde
         return st;
     const int64_t nblocks = n / block;
     if (!tensor_core_block(block)) {
-        const int64_t want = (nblocks + 7) / 8, cap = static_cast<int64_t>(dev->sm_count) * 16;
+        const KernelInfo wk = warp_codec_info(block, false);
+        const int64_t want = (nblocks + wk.tile_blocks - 1) / wk.tile_blocks;
+        const int64_t cap = static_cast<int64_t>(dev->sm_count) * 16;
         const cudaError_t e = launch_warp_decompress(block, scheme, packed_in, y_bf16_out, nblocks,
                                                      static_cast<int>(want < cap ? want : cap),
                                                      reinterpret_cast<cudaStream_t>(stream));
