@@ -81,7 +81,9 @@ void init_device(DeviceState &st)
                 e = init_kernel(warp_codec_info(blocks[i], false), &st.ctas_per_sm);
         }
         for (int code = 0; code < 3 && e == cudaSuccess; code++)
-            e = init_kernel(reduce_kernel_info(blocks[i], code), &st.ctas_per_sm);
+            e = init_kernel(reduce_kernel_info(blocks[i], code, 1), &st.ctas_per_sm);
+        if (e == cudaSuccess && tensor_core_block(blocks[i]))
+            e = init_kernel(reduce_kernel_info(blocks[i], 0, 8), &st.ctas_per_sm);
     }
     st.init_error = e;
 }
@@ -295,7 +297,7 @@ taco_status_t reduce_impl(const void *const *packed_shards, int num_shards, int6
     args.variant = scheme.variant;
     // One CTA per tile of blocks; one per SM runs and takes the tiles of CTAs
     // it cancels before they start.
-    const KernelInfo ki = reduce_kernel_info(block, scheme.code);
+    const KernelInfo ki = reduce_kernel_info(block, scheme.code, num_shards);
     const int64_t ntiles = (args.nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
     if (ntiles > INT32_MAX)
         return TACO_ERR_BAD_SHAPE;

@@ -49,7 +49,7 @@ struct Scheme {
 
 KernelInfo compress_kernel_info(int block);
 KernelInfo decompress_kernel_info(int block, int code);   // code 2 (INT8) has its own kernel
-KernelInfo reduce_kernel_info(int block, int code);
+KernelInfo reduce_kernel_info(int block, int code, int num_shards);
 
 // `tmap` points to a CUtensorMap of x viewed as [nblocks, block] bf16, box
 // {64, 128}, 128-byte swizzle.

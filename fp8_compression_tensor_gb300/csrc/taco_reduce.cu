@@ -42,8 +42,8 @@ namespace {
 #ifndef TACO_REDUCE_RING_KB
 #define TACO_REDUCE_RING_KB 192
 #endif
-#ifndef TACO_REDUCE_UNROLL2
-#define TACO_REDUCE_UNROLL2 0
+#ifndef TACO_REDUCE_FIXED_P8
+#define TACO_REDUCE_FIXED_P8 1
 #endif
 #ifndef TACO_REDUCE_GROUPS
 #define TACO_REDUCE_GROUPS 3
@@ -122,7 +122,8 @@ __device__ __forceinline__ uint2 ldg_u2(const uint8_t *p)
     return *reinterpret_cast<const uint2 *>(p);
 }
 
-template <int B, int CODE>
+// PFIX > 0: the shard count is fixed at compile time (the shard loop unrolls).
+template <int B, int CODE, int PFIX>
 __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const ReduceArgs args, uint32_t *fault)
 {
     using Lay = ReduceLayout<B>;
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     grid_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int P = args.num_shards;
+    const int P = PFIX > 0 ? PFIX : args.num_shards;
     const int64_t nblocks = args.nblocks;
     const bool adaptive = args.variant == 0 || args.variant == 3;   // alpha' from the energy of W
     const bool dual_scale = args.variant != 3;                      // s' from max|W|
@@ -238,23 +239,8 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             // the range where the fast quotient underflows).
             if (active && !from_global) {
                 const uint32_t r0 = rec_s + kLaneCodes * part;
-#if TACO_REDUCE_UNROLL2
-                int p = 0;
-                for (; p + 2 <= P; p += 2) {
-                    const uint32_t r = r0 + p * Lay::kRunBytes;
-                    const uint2 a0 = lds64(r), b0 = lds64(r + 8);
-                    const uint2 m0 = lds64(r - kLaneCodes * part + B);
-                    const uint2 a1 = lds64(r + Lay::kRunBytes), b1 = lds64(r + Lay::kRunBytes + 8);
-                    const uint2 m1 = lds64(r + Lay::kRunBytes - kLaneCodes * part + B);
-                    accumulate_shard<CODE>(w, make_uint4(a0.x, a0.y, b0.x, b0.y),
-                                     __fdividef(__uint_as_float(m0.y), __uint_as_float(m0.x)));
-                    accumulate_shard<CODE>(w, make_uint4(a1.x, a1.y, b1.x, b1.y),
-                                     __fdividef(__uint_as_float(m1.y), __uint_as_float(m1.x)));
-                }
-                if (p < P) {
-#else
+#pragma unroll(PFIX > 0 ? PFIX : 1)
                 for (int p = 0; p < P; p++) {
-#endif
                     const uint32_t r = r0 + p * Lay::kRunBytes;
                     const uint2 a = lds64(r), b = lds64(r + 8);
                     const uint2 meta = lds64(r - kLaneCodes * part + B);
@@ -327,10 +313,10 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     }
 }
 
-template <int B, int CODE>
+template <int B, int CODE, int PFIX = 0>
 KernelInfo info()
 {
-    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B, CODE>), ReduceLayout<B>::kSmem,
+    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B, CODE, PFIX>), ReduceLayout<B>::kSmem,
                       kRThreads, ReduceLayout<B>::kT, kRThreads / 32};
 }
 
@@ -349,8 +335,17 @@ KernelInfo info_for_block(int block)
 
 }  // namespace
 
-KernelInfo reduce_kernel_info(int block, int code)
+KernelInfo reduce_kernel_info(int block, int code, int num_shards)
 {
+    // The method's own case (E4M3, 8 shards) has kernels with the shard loop unrolled.
+    if (TACO_REDUCE_FIXED_P8 && code == 0 && num_shards == 8) {
+        switch (block) {
+        case 64: return info<64, 0, 8>();
+        case 128: return info<128, 0, 8>();
+        case 256: return info<256, 0, 8>();
+        default: break;
+        }
+    }
     switch (code) {
     case 0: return info_for_block<0>(block);
     case 1: return info_for_block<1>(block);
@@ -361,7 +356,7 @@ KernelInfo reduce_kernel_info(int block, int code)
 
 cudaError_t launch_reduce(int block, int code, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream)
 {
-    const KernelInfo ki = reduce_kernel_info(block, code);
+    const KernelInfo ki = reduce_kernel_info(block, code, args.num_shards);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     ReduceArgs a = args;
