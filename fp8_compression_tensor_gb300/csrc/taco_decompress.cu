@@ -29,10 +29,14 @@
 // (two blocks per row, H = diag(H_64, H_64)).
 //
 // Ablations (Scheme): E5M2 codes are the MMA's operand as E5M2 (H in E5M2);
-// INT8 codes v are split as v = 16 floor(v / 16) + (v mod 16), both terms
-// exact in E4M3, and the two products accumulate in the same tensor memory
-// (SPLIT = 2); DS only puts the identity in place of H; the factor is
-// s / sqrt(B) / alpha, or s / alpha without rotation.
+// INT8 codes (A16: the 8-bit integer MMA kind does not exist on sm_103a) go
+// through .kind::f16: a code v becomes the f16 1152 + v exactly (the bytes
+// v ^ 0x80 under the exponent byte 0x64 give 1024 + (v + 128)), H holds +-1 in
+// f16, and since H 1 = B e_0 the epilogue subtracts 1152 B from each block's
+// first column (1152 from every column without rotation); all sums are
+// integers below 2^24, so the decoded H v is exact.  DS only puts the
+// identity in place of H; the factor is s / sqrt(B) / alpha, or s / alpha
+// without rotation.
 #include <cstring>
 
 #include <cuda.h>
@@ -49,20 +53,23 @@ constexpr int kDRows = 128;        // MMA rows per tile
 constexpr int kDThreads = 320;     // 10 warps
 constexpr int kGroup = 128;        // threads of the transposer / epilogue groups
 
-template <int B, int RS, int AS, int NOUT, int SPLIT>
+template <int B, int RS, int AS, int NOUT, int A16>
 struct TcDecompressLayout {
     static constexpr int kBlocksPerRow = B == 64 ? 2 : 1;
     static constexpr int kTileBlocks = kDRows * kBlocksPerRow;
     static constexpr int kRowCodes = B * kBlocksPerRow;            // 128 or 256
-    static constexpr int kAChunks = kRowCodes / 128;               // 128-byte chunks of an A row
+    static constexpr int kElem = A16 ? 2 : 1;                      // bytes per code in the A operand
+    static constexpr int kAChunks = kRowCodes * kElem / 128;       // 128-byte chunks of an A row
+    static constexpr int kInHalves = B == 256 ? 2 : 1;             // 128-code halves of a block
+    static constexpr int kChunksPerHalf = kAChunks / kInHalves;    // = H's K chunks
     static constexpr int kHalves = B == 256 ? 2 : 1;
     static constexpr int kAccCols = 128 * kHalves;                 // TMEM columns per tile
     static constexpr int kRec = B + 8;
     static constexpr int kRawBytes = kTileBlocks * kRec;
-    static constexpr int kSplitBytes = kDRows * kRowCodes;         // one term of the codes
-    static constexpr int kAStageBytes = SPLIT * kSplitBytes;
+    static constexpr int kAStageBytes = kDRows * kRowCodes * kElem;
     static constexpr int kAChunkBytes = kDRows * 128;
-    static constexpr int kHBytes = 128 * 128;
+    static constexpr int kHChunkBytes = 128 * 128;                 // 128 rows of H, 128 bytes of K
+    static constexpr int kHBytes = kChunksPerHalf * kHChunkBytes;
     static constexpr int kOutRows = kTileBlocks;                   // rows of y per tile
     static constexpr int kOutChunks = B == 64 ? 1 : B / 64;        // 64-element chunks of a y row
     static constexpr int kOutChunkBytes = kOutRows * 128;
@@ -120,12 +127,43 @@ __device__ void write_hadamard_f8_sw128(uint8_t *h, bool e5m2, bool rotate)
     }
 }
 
-template <int B, int RS, int AS, int NOUT, int SPLIT>
+// The same in f16 (+1 = 0x3C00, -1 = 0xBC00): two 128-byte K chunks of 64
+// columns each.
+template <int B>
+__device__ void write_hadamard_f16_sw128(uint8_t *h, bool rotate)
+{
+    for (int idx = threadIdx.x; idx < 128 * 16; idx += blockDim.x) {
+        const int n = idx / 16, ua = idx % 16;   // row, 16-byte unit along K (8 columns)
+        const int c = ua / 8, u = ua % 8;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int k = 8 * ua + 2 * q + e;
+                uint32_t v;
+                if (!rotate)
+                    v = (n == k) ? 0x3C00u : 0u;
+                else if (B == 64)
+                    v = (n / 64 != k / 64) ? 0u : ((__popc((n & 63) & (k & 63)) & 1) ? 0xBC00u : 0x3C00u);
+                else
+                    v = (__popc(n & k) & 1) ? 0xBC00u : 0x3C00u;
+                word |= v << (16 * e);
+            }
+            w[q] = word;
+        }
+        *reinterpret_cast<uint4 *>(h + c * 16384 + n * 128 + ((u ^ (n & 7)) * 16)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <int B, int RS, int AS, int NOUT, int A16>
 __global__ void __launch_bounds__(kDThreads, 1)
     taco_decompress_kernel(const __grid_constant__ CUtensorMap tmap_y, const uint8_t *__restrict__ packed,
                               int64_t nblocks, uint32_t *__restrict__ fault, const Scheme scheme)
 {
-    using Lay = TcDecompressLayout<B, RS, AS, NOUT, SPLIT>;
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT, A16>;
     constexpr int FS = Lay::FS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -193,8 +231,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
     const bool rotate = scheme.variant != 2;   // DS only: no rotation
-    const bool e5m2 = SPLIT == 1 && scheme.code == 1;
-    write_hadamard_f8_sw128<B>(base + Lay::kOffH, e5m2, rotate);
+    const bool e5m2 = !A16 && scheme.code == 1;
+    if constexpr (A16)
+        write_hadamard_f16_sw128<B>(base + Lay::kOffH, rotate);
+    else
+        write_hadamard_f8_sw128<B>(base + Lay::kOffH, e5m2, rotate);
     fence_proxy_async_smem();
     tc_fence_before_sync();
     grid_dependency_wait();   // before any global access of this thread
@@ -232,7 +273,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
     } else if (warp == 1) {
         // ---- MMA issuer ----------------------------------------------------
         if (lane == 0) {
-            const uint32_t idesc = e5m2 ? mma_idesc_e5m2_f32(kDRows, 128) : mma_idesc_e4m3_f32(kDRows, 128);
+            const uint32_t idesc = A16    ? mma_idesc_f16_f32(kDRows, 128)
+                                   : e5m2 ? mma_idesc_e5m2_f32(kDRows, 128)
+                                          : mma_idesc_e4m3_f32(kDRows, 128);
             const uint32_t h0 = sbase + Lay::kOffH;
             int i = 0;
             for (;; i++) {
@@ -251,20 +294,23 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 for (int oh = 0; oh < Lay::kHalves; oh++) {
                     bool first = true;
 #pragma unroll
-                    for (int sp = 0; sp < SPLIT; sp++) {
+                    for (int ih = 0; ih < Lay::kInHalves; ih++) {
+                        if (!rotate && Lay::kHalves == 2 && ih != oh)
+                            continue;   // identity: output half h takes input half h only
+                        const uint32_t id = (rotate && oh == 1 && ih == 1) ? (idesc | kMmaNegateA) : idesc;
 #pragma unroll
-                        for (int ih = 0; ih < Lay::kAChunks; ih++) {
-                            if (!rotate && Lay::kHalves == 2 && ih != oh)
-                                continue;   // identity: output half h takes input half h only
-                            const uint32_t id = (rotate && oh == 1 && ih == 1) ? (idesc | kMmaNegateA) : idesc;
+                        for (int c = 0; c < Lay::kChunksPerHalf; c++) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; kk++) {   // 32 codes = 32 bytes per MMA
-                                const uint64_t ad = sw128_kmajor_desc(a_st + sp * Lay::kSplitBytes +
-                                                                      ih * Lay::kAChunkBytes + 32 * kk);
-                                const uint64_t bd = sw128_kmajor_desc(h0 + 32 * kk);
-                                tc_mma_f8(d + 128 * oh, ad, bd, id, (first && kk == 0) ? 0u : 1u);
+                            for (int kk = 0; kk < 4; kk++) {   // 32 bytes of K per MMA
+                                const uint64_t ad = sw128_kmajor_desc(
+                                    a_st + (ih * Lay::kChunksPerHalf + c) * Lay::kAChunkBytes + 32 * kk);
+                                const uint64_t bd = sw128_kmajor_desc(h0 + c * Lay::kHChunkBytes + 32 * kk);
+                                if constexpr (A16)
+                                    tc_mma_bf16(d + 128 * oh, ad, bd, id, (first && kk == 0) ? 0u : 1u);
+                                else
+                                    tc_mma_f8(d + 128 * oh, ad, bd, id, (first && kk == 0) ? 0u : 1u);
+                                first = false;
                             }
-                            first = false;
                         }
                     }
                 }
@@ -315,32 +361,30 @@ __global__ void __launch_bounds__(kDThreads, 1)
                         w[q] = 0u;
                 }
                 factors[fs * Lay::kTileBlocks + bl] = f;
-                // Codes to the swizzled A row: 16 codes per 16-byte unit.
+                // Codes to the swizzled A row: 16 codes per 16-byte unit (8 in f16).
 #pragma unroll
                 for (int u = 0; u < B / 16; u++) {
-                    const int ua = b * (B / 16) + u;          // unit index along the A row
-                    const int chunk = ua / 8, uc = ua % 8;
-                    const uint32_t dst = a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16);
-                    if constexpr (SPLIT == 1) {
-                        sts128(dst, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]));
+                    if constexpr (!A16) {
+                        const int ua = b * (B / 16) + u;          // unit index along the A row
+                        const int chunk = ua / 8, uc = ua % 8;
+                        sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
+                               make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]));
                     } else {
-                        // INT8 code v = 16 * (v >> 4) + (v & 15), both terms as E4M3.
-                        uint32_t hi[4], lo[4];
+                        // INT8 v -> f16 1152 + v: bytes (v ^ 0x80) under 0x64.
+                        uint32_t hv[8];
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
-                            const uint32_t x = w[4 * u + q];
-                            float fh[4], fl[4];
-#pragma unroll
-                            for (int e = 0; e < 4; e++) {
-                                const int v = static_cast<int>(static_cast<int8_t>(x >> (8 * e)));
-                                fh[e] = static_cast<float>((v >> 4) * 16);
-                                fl[e] = static_cast<float>(v & 15);
-                            }
-                            hi[q] = encode4(0, fh[0], fh[1], fh[2], fh[3]);
-                            lo[q] = encode4(0, fl[0], fl[1], fl[2], fl[3]);
+                            const uint32_t xb = w[4 * u + q] ^ 0x80808080u;
+                            hv[2 * q] = __byte_perm(xb, 0x64646464u, 0x4140);
+                            hv[2 * q + 1] = __byte_perm(xb, 0x64646464u, 0x4342);
                         }
-                        sts128(dst, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-                        sts128(dst + Lay::kSplitBytes, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+#pragma unroll
+                        for (int hh = 0; hh < 2; hh++) {
+                            const int ua = 2 * (b * (B / 16) + u) + hh;
+                            const int chunk = ua / 8, uc = ua % 8;
+                            sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
+                                   make_uint4(hv[4 * hh], hv[4 * hh + 1], hv[4 * hh + 2], hv[4 * hh + 3]));
+                        }
                     }
                 }
             }
@@ -389,6 +433,15 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 tmem_ld_wait();
                 const int e0 = 32 * c;                     // first element (column) of the chunk
                 const int b = (B == 64) ? e0 / 64 : 0;     // block within the row (B = 64)
+                if constexpr (A16) {                       // remove the f16 bias 1152 of the codes
+                    if (!rotate) {
+#pragma unroll
+                        for (int h = 0; h < 32; h++)
+                            r[h] = __float_as_uint(__uint_as_float(r[h]) - 1152.0f);
+                    } else if (e0 % B == 0) {
+                        r[0] = __float_as_uint(__uint_as_float(r[0]) - 1152.0f * B);
+                    }
+                }
                 const float f = fb[b];
                 const float2 f2 = make_float2(f, f);
                 const int row = (B == 64) ? 2 * m + b : m; // y row within the tile
@@ -438,12 +491,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
 }
 
-template <int B, int RS, int AS, int NOUT, int SPLIT>
+template <int B, int RS, int AS, int NOUT, int A16>
 struct TcDecompressConfig {
-    using Lay = TcDecompressLayout<B, RS, AS, NOUT, SPLIT>;
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT, A16>;
     static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
     static_assert(Lay::kRawBytes % 16 == 0, "raw stage alignment");
-    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, RS, AS, NOUT, SPLIT>); }
+    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, RS, AS, NOUT, A16>); }
     static KernelInfo info()
     {
         return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), kDThreads, Lay::kTileBlocks, 0};
@@ -460,15 +513,15 @@ struct TcDecompressConfig {
 #define TACO_DTC256_CFG 221
 #endif
 // Per block size, three digits: raw stages, A stages, output tiles.
-using DecompressTc64 = TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 1>;
+using DecompressTc64 = TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0>;
 using DecompressTc128 =
-    TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10, 1>;
+    TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10, 0>;
 using DecompressTc256 =
-    TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10, 1>;
-// INT8 codes (two E4M3 terms per code: A stages twice as large).
-using DecompressI8x64 = TcDecompressConfig<64, 3, 2, 2, 2>;
-using DecompressI8x128 = TcDecompressConfig<128, 3, 2, 2, 2>;
-using DecompressI8x256 = TcDecompressConfig<256, 2, 1, 1, 2>;
+    TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10, 0>;
+// INT8 codes (f16 operands: A stages and H twice as large).
+using DecompressI8x64 = TcDecompressConfig<64, 3, 2, 2, 1>;
+using DecompressI8x128 = TcDecompressConfig<128, 3, 2, 2, 1>;
+using DecompressI8x256 = TcDecompressConfig<256, 1, 1, 1, 1>;
 
 }  // namespace
 

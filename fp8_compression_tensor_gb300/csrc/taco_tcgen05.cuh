@@ -106,6 +106,16 @@ __host__ __device__ constexpr uint32_t mma_idesc_e4m3_f32(int M, int N)
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor of tcgen05.mma.kind::f16 with F16 A and B (format 0).
+__host__ __device__ constexpr uint32_t mma_idesc_f16_f32(int M, int N)
+{
+    return (1u << 4)                                   // D format: F32
+           | (0u << 7)                                 // A format: F16
+           | (0u << 10)                                // B format: F16
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Same with E5M2 A and B (format 1 of .kind::f8f6f4).
 __host__ __device__ constexpr uint32_t mma_idesc_e5m2_f32(int M, int N)
 {
@@ -119,7 +129,8 @@ __host__ __device__ constexpr uint32_t mma_idesc_e5m2_f32(int M, int N)
 constexpr uint32_t kMmaNegateA = 1u << 13;   // instruction-descriptor bit: negate A
 
 // D[tmem] = A * B^T (+ D if accumulate): A is M x K, B is N x K, both from
-// shared-memory descriptors.  Issued by one thread.
+// shared-memory descriptors, 16-bit operands (BF16 or F16 per the
+// instruction descriptor, K = 16).  Issued by one thread.
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate)
 {
