@@ -38,11 +38,19 @@ bool block_supported(int block)
     return block == 32 || block == 64 || block == 128 || block == 256 || block == 512;
 }
 
-// Blocks 64, 128 and 256 run on the tensor-core kernels, 32 and 512 on the
-// warp-per-block codec (the shard reduce takes every block size).
+// Blocks 64 .. 512 run on the tensor-core kernels (512 as four rows of 128
+// elements per block), 32 on the lane-per-block codec; the shard reduce takes
+// every block size.
 bool tensor_core_block(int block)
 {
-    return block == 64 || block == 128 || block == 256;
+    return block == 64 || block == 128 || block == 256 || block == 512;
+}
+
+// Row length of the tensor-core kernels' view of the tensor: the block, or
+// 128 for B = 512 (four rows per block).
+int view_row_elems(int block)
+{
+    return block == 512 ? 128 : block;
 }
 
 taco_status_t cuda_fail(cudaError_t e)
@@ -212,7 +220,8 @@ taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, in
     if (ntiles > INT32_MAX)
         return TACO_ERR_BAD_SHAPE;
     alignas(64) CUtensorMap map;
-    cudaError_t e = encode_block_rows_map(&map, x_bf16, nblocks, block);
+    const int re = view_row_elems(block);
+    cudaError_t e = encode_block_rows_map(&map, x_bf16, nblocks * (block / re), re);
     if (e != cudaSuccess)
         return cuda_fail(e);
     const int grid = static_cast<int>(ntiles);
@@ -254,7 +263,9 @@ taco_status_t decompress_impl(const void *packed_in, int64_t rows, int64_t hidde
     if (ntiles > INT32_MAX)
         return TACO_ERR_BAD_SHAPE;
     alignas(64) CUtensorMap map;
-    cudaError_t e = encode_block_rows_map(&map, y_bf16_out, nblocks, block, ki.tile_blocks);
+    const int re = view_row_elems(block), rows_per_block = block / re;
+    cudaError_t e = encode_block_rows_map(&map, y_bf16_out, nblocks * rows_per_block, re,
+                                          ki.tile_blocks * rows_per_block);
     if (e != cudaSuccess)
         return cuda_fail(e);
     const int grid = static_cast<int>(ntiles);

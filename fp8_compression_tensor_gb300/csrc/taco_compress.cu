@@ -62,17 +62,23 @@ __host__ __device__ constexpr int tc_threads(int groups) { return 64 + kEpiThrea
 template <int B, int STAGES, int EPG, int NBG>
 struct TcCompressLayout {
     static constexpr int NOUT = EPG * NBG;                         // record-tile buffers
-    static constexpr int kN = B <= 128 ? B : 128;                  // MMA N = order of the Hadamard matrix used
-    static constexpr int kHalves = B / kN;                         // 2 for B = 256 (Kronecker split)
+    // B = 512: each block is four A rows of 128 elements (quarters).
+    static constexpr bool kQuad = B == 512;
+    static constexpr int kRowElems = kQuad ? 128 : B;              // elements of an A row
+    static constexpr int kRowsPerBlock = kQuad ? 4 : 1;
+    static constexpr int kTileBlocks = kTcRows / kRowsPerBlock;    // blocks per tile
+    static constexpr int kN = kRowElems <= 128 ? kRowElems : 128;  // MMA N = order of the Hadamard matrix used
+    static constexpr int kHalves = kRowElems / kN;                 // 2 for B = 256 (Kronecker split)
     static constexpr int kKSteps = kN / 16;                        // MMAs (K = 16) per product with H_N
-    static constexpr int kChunks = B / 64;                         // 128-byte K chunks of a row
+    static constexpr int kChunks = kRowElems / 64;                 // 128-byte K chunks of a row
     static constexpr int kChunkBytesA = kTcRows * 128;             // one chunk of the A tile
-    static constexpr int kStageBytes = kTcRows * B * 2;            // one A tile
+    static constexpr int kStageBytes = kTcRows * kRowElems * 2;    // one A tile
     static constexpr int kChunkBytesH = kN * 128;                  // one chunk of H_N
     static constexpr int kHBytes = kN * kN * 2;
     static constexpr int kRec = B + 8;
-    static constexpr int kOutBytes = kTcRows * kRec;               // one record tile (multiple of 16)
-    static constexpr int kTmemCols = 2 * B;                        // two accumulators of B columns
+    static constexpr int kOutBytes = kTileBlocks * kRec;           // one record tile (multiple of 16)
+    static constexpr int kAccCols = kRowElems;                     // TMEM columns of one accumulator
+    static constexpr int kTmemCols = 2 * kAccCols;                 // two accumulators
     // Offsets from the 1024-byte aligned base.
     static constexpr int kOffA = 0;
     static constexpr int kOffH = kOffA + STAGES * kStageBytes;
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                 if (!mbar_wait_bounded_thread(full_bar(s), (i / STAGES) & 1, fault, kFaultCompress))
                     break;
                 tc_fence_after_sync();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * B);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * Lay::kAccCols);
                 const uint32_t a_stage = a0 + s * Lay::kStageBytes;
                 if constexpr (Lay::kHalves == 1) {
 #pragma unroll
@@ -285,9 +291,14 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
         const int grp = (warp - 2) / 4;                 // epilogue group
         const int et = threadIdx.x - 64 - kEpiThreads * grp;   // 0..127 within the group
         const int q = warp & 3;                         // TMEM lane quarter of this warp
-        const int row = 32 * q + lane;                  // accumulator row = block within the tile
+        const int row = 32 * q + lane;                  // accumulator row
+        const int blk = row / Lay::kRowsPerBlock;       // block within the tile
+        const int quarter = row % Lay::kRowsPerBlock;   // B = 512: which 128 elements of the block
         const bool store_warp = ((warp - 2) & 3) == 0;  // first warp of the group issues the stores
-        const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
+        const float rB = (B == 64)    ? 0.125f
+                         : (B == 128) ? 0.0883883476483184405f
+                         : (B == 256) ? 0.0625f
+                                      : 0.0441941738241592203f;   // 1/sqrt(B) in binary32
         for (int kt = 0;; kt++) {                   // kt: tiles this group has handled
             const int i = EPG * kt + grp;               // the CTA's item counter
             const int64_t t = sched.tile_warp(i);
@@ -297,27 +308,65 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             if (!mbar_wait_bounded(acc_full_bar(acc), (i >> 1) & 1, fault, kFaultCompress))
                 break;
             tc_fence_after_sync();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * B);
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * Lay::kAccCols);
 
             // Pass 1: energy (Parseval) and max|y|.
             float2 e2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             float ymax = 0.f;
+            // B = 512: H_512 = H_4 (x) H_128; the MMA gave H_128 of each quarter,
+            // the 4 quarters' rows sit in 4 neighbouring lanes, and a butterfly
+            // over lanes (xor 1, xor 2) finishes the rotation; the rotated
+            // quarter stays in registers for pass 2.
+            float yq[Lay::kQuad ? 128 : 1];
+            if constexpr (Lay::kQuad) {
+                const float sgn1 = (quarter & 1) ? -1.0f : 1.0f, sgn2 = (quarter & 2) ? -1.0f : 1.0f;
 #pragma unroll
-            for (int c = 0; c < B / 32; c++) {
-                uint32_t r[32];
-                tmem_ld32(taddr + 32 * c, r);
-                tmem_ld_wait();
+                for (int c = 0; c < 4; c++) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + 32 * c, r);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const float2 y = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                    e2[(j >> 1) & 3] = fma2(y, y, e2[(j >> 1) & 3]);
-                    ymax = max3(ymax, fabsf(y.x), fabsf(y.y));
+                    for (int j = 0; j < 32; j++) {
+                        float v = __uint_as_float(r[j]);
+                        if (rotate) {   // lower lane a + b, upper lane a - b, as one fma each
+                            v = fmaf(sgn1, v, __shfl_xor_sync(kFullMask, v, 1));
+                            v = fmaf(sgn2, v, __shfl_xor_sync(kFullMask, v, 2));
+                        }
+                        yq[32 * c + j] = v;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float2 y = make_float2(yq[32 * c + j], yq[32 * c + j + 1]);
+                        e2[(j >> 1) & 3] = fma2(y, y, e2[(j >> 1) & 3]);
+                        ymax = max3(ymax, fabsf(y.x), fabsf(y.y));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < B / 32; c++) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + 32 * c, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float2 y = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                        e2[(j >> 1) & 3] = fma2(y, y, e2[(j >> 1) & 3]);
+                        ymax = max3(ymax, fabsf(y.x), fabsf(y.y));
+                    }
                 }
             }
             const float2 e01 = add2(e2[0], e2[1]), e23 = add2(e2[2], e2[3]);
             const float2 ee = add2(e01, e23);
-            const float m = (ee.x + ee.y) * (1.0f / (static_cast<float>(B) * B));
+            float etot = ee.x + ee.y;
+            if constexpr (Lay::kQuad) {   // the block's four quarters
+                etot += __shfl_xor_sync(kFullMask, etot, 1);
+                etot += __shfl_xor_sync(kFullMask, etot, 2);
+                ymax = fmaxf(ymax, __shfl_xor_sync(kFullMask, ymax, 1));
+                ymax = fmaxf(ymax, __shfl_xor_sync(kFullMask, ymax, 2));
+            }
+            const float m = etot * (1.0f / (static_cast<float>(B) * B));
             const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(m + kEps)) : 1.0f;
             const float rr = rotate ? rB : 1.0f;
             const float qmax = code_qmax(scheme.code);
@@ -342,15 +391,22 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                 if (!mbar_wait_bounded(out_free_bar(ob), ((kt / NBG) - 1) & 1, fault, kFaultCompress))
                     break;
             }
-            const uint32_t rec = sbase + Lay::kOffOut + ob * Lay::kOutBytes + row * Lay::kRec;
+            const uint32_t rec_block = sbase + Lay::kOffOut + ob * Lay::kOutBytes + blk * Lay::kRec;
+            const uint32_t rec = rec_block + quarter * 128;
 
             // Pass 2: codes (Eq. 10) two per cvt, 32 per chunk.
             const float2 k2 = make_float2(k, k);
 #pragma unroll
-            for (int c = 0; c < B / 32; c++) {
+            for (int c = 0; c < Lay::kAccCols / 32; c++) {
                 uint32_t r[32];
-                tmem_ld32(taddr + 32 * c, r);
-                tmem_ld_wait();
+                if constexpr (Lay::kQuad) {
+#pragma unroll
+                    for (int j = 0; j < 32; j++)
+                        r[j] = __float_as_uint(yq[32 * c + j]);
+                } else {
+                    tmem_ld32(taddr + 32 * c, r);
+                    tmem_ld_wait();
+                }
                 uint32_t cw[8];
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
@@ -374,13 +430,15 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             if (lane == 0)
                 mbar_arrive(acc_empty_bar(acc));
 
-            sts64(rec + B, __float_as_uint(alpha), __float_as_uint(s));
+            if (quarter == 0)
+                sts64(rec_block + B, __float_as_uint(alpha), __float_as_uint(s));
             fence_proxy_async_smem();
             mbar_arrive(rec_done_bar(ob));
 
-            // The group's first warp (lane 0) stores the tile's records once all 128 are written.
-            const int64_t blk0 = t * kTcRows;
-            const int nvalid = static_cast<int>(nblocks - blk0 < kTcRows ? nblocks - blk0 : kTcRows);
+            // The group's first warp (lane 0) stores the tile's records once all are written.
+            constexpr int TB = Lay::kTileBlocks;
+            const int64_t blk0 = t * TB;
+            const int nvalid = static_cast<int>(nblocks - blk0 < TB ? nblocks - blk0 : TB);
             const int neven = nvalid & ~1;
             if (store_warp) {
                 if (!mbar_wait_bounded(rec_done_bar(ob), (kt / NBG) & 1, fault, kFaultCompress))
@@ -391,9 +449,9 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                     bulk_commit();
                 }
             }
-            if ((nvalid & 1) && row == nvalid - 1) {
-                uint8_t *dst = packed + (blk0 + row) * Lay::kRec;
-                const uint8_t *src = base + Lay::kOffOut + ob * Lay::kOutBytes + row * Lay::kRec;
+            if ((nvalid & 1) && blk == nvalid - 1 && quarter == 0) {
+                uint8_t *dst = packed + (blk0 + blk) * Lay::kRec;
+                const uint8_t *src = base + Lay::kOffOut + ob * Lay::kOutBytes + blk * Lay::kRec;
                 for (int o = 0; o < Lay::kRec; o += 8)
                     *reinterpret_cast<uint2 *>(dst + o) = *reinterpret_cast<const uint2 *>(src + o);
             }
@@ -418,7 +476,7 @@ struct TcCompressConfig {
     static void *fn() { return reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG>); }
     static KernelInfo info()
     {
-        return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), kTcRows, 0};
+        return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), Lay::kTileBlocks, 0};
     }
 };
 
@@ -431,10 +489,14 @@ struct TcCompressConfig {
 #ifndef TACO_TC256_CFG
 #define TACO_TC256_CFG 211
 #endif
+#ifndef TACO_TC512_CFG
+#define TACO_TC512_CFG 421
+#endif
 // Per block size, three digits: A stages, epilogue groups, buffers per group.
 using CompressTc64 = TcCompressConfig<64, TACO_TC64_CFG / 100, TACO_TC64_CFG / 10 % 10, TACO_TC64_CFG % 10>;
 using CompressTc128 = TcCompressConfig<128, TACO_TC128_CFG / 100, TACO_TC128_CFG / 10 % 10, TACO_TC128_CFG % 10>;
 using CompressTc256 = TcCompressConfig<256, TACO_TC256_CFG / 100, TACO_TC256_CFG / 10 % 10, TACO_TC256_CFG % 10>;
+using CompressTc512 = TcCompressConfig<512, TACO_TC512_CFG / 100, TACO_TC512_CFG / 10 % 10, TACO_TC512_CFG % 10>;
 
 }  // namespace
 
@@ -444,6 +506,7 @@ KernelInfo compress_kernel_info(int block)
     case 64: return CompressTc64::info();
     case 128: return CompressTc128::info();
     case 256: return CompressTc256::info();
+    case 512: return CompressTc512::info();
     default: return KernelInfo{};
     }
 }

@@ -55,9 +55,13 @@ constexpr int kGroup = 128;        // threads of the transposer / epilogue group
 
 template <int B, int RS, int AS, int NOUT, int A16>
 struct TcDecompressLayout {
+    // B = 512: each block is four A rows of 128 codes (quarters).
+    static constexpr bool kQuad = B == 512;
     static constexpr int kBlocksPerRow = B == 64 ? 2 : 1;
-    static constexpr int kTileBlocks = kDRows * kBlocksPerRow;
-    static constexpr int kRowCodes = B * kBlocksPerRow;            // 128 or 256
+    static constexpr int kRowsPerBlock = kQuad ? 4 : 1;
+    static constexpr int kTileBlocks = kDRows * kBlocksPerRow / kRowsPerBlock;
+    static constexpr int kPartCodes = kQuad ? 128 : B;             // codes of one block (part) in a row
+    static constexpr int kRowCodes = kPartCodes * kBlocksPerRow;   // 128 or 256
     static constexpr int kElem = A16 ? 2 : 1;                      // bytes per code in the A operand
     static constexpr int kAChunks = kRowCodes * kElem / 128;       // 128-byte chunks of an A row
     static constexpr int kInHalves = B == 256 ? 2 : 1;             // 128-code halves of a block
@@ -70,8 +74,8 @@ struct TcDecompressLayout {
     static constexpr int kAChunkBytes = kDRows * 128;
     static constexpr int kHChunkBytes = 128 * 128;                 // 128 rows of H, 128 bytes of K
     static constexpr int kHBytes = kChunksPerHalf * kHChunkBytes;
-    static constexpr int kOutRows = kTileBlocks;                   // rows of y per tile
-    static constexpr int kOutChunks = B == 64 ? 1 : B / 64;        // 64-element chunks of a y row
+    static constexpr int kOutRows = kQuad ? kDRows : kTileBlocks;  // rows of the y view per tile
+    static constexpr int kOutChunks = B == 64 ? 1 : kPartCodes / 64;   // 64-element chunks of a y row
     static constexpr int kOutChunkBytes = kOutRows * 128;
     static constexpr int kOutBytes = kOutChunks * kOutChunkBytes;
     static constexpr int FS = AS + 2;                              // factor slots
@@ -323,7 +327,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
     } else if (warp < 6) {
         // ---- transposers (warps 2..5): one MMA row per thread ---------------
         const int m = threadIdx.x - 64;    // 0..127
-        const float rB = (B == 64) ? 0.125f : (B == 128) ? 0.0883883476483184405f : 0.0625f;
+        const float rB = (B == 64)    ? 0.125f
+                         : (B == 128) ? 0.0883883476483184405f
+                         : (B == 256) ? 0.0625f
+                                      : 0.0441941738241592203f;   // 1/sqrt(B) in binary32
         const float rr = rotate ? rB : 1.0f;
         for (int i = 0;; i++) {
             const int64_t t = sched.tile_warp(i);
@@ -340,16 +347,19 @@ __global__ void __launch_bounds__(kDThreads, 1)
             const uint32_t a_row = sbase + Lay::kOffA + j * Lay::kAStageBytes + m * 128;
 #pragma unroll
             for (int b = 0; b < Lay::kBlocksPerRow; b++) {
-                const int bl = m * Lay::kBlocksPerRow + b;    // block within the tile
-                uint32_t w[B / 4];
+                constexpr int PC = Lay::kPartCodes;
+                const int bl = (m * Lay::kBlocksPerRow + b) / Lay::kRowsPerBlock;   // block within the tile
+                const int part = m % Lay::kRowsPerBlock;                             // B = 512: quarter
+                uint32_t w[PC / 4];
                 float f = 0.f;
                 if (bl < nvalid) {
                     const bool from_global = (nvalid & 1) && bl == nvalid - 1;   // not in the bulk copy
                     const uint8_t *rg = packed + (blk0 + bl) * Lay::kRec;
                     const uint32_t rs = raw + bl * Lay::kRec;
 #pragma unroll
-                    for (int q = 0; q < B / 8; q++) {
-                        const uint2 v = from_global ? *reinterpret_cast<const uint2 *>(rg + 8 * q) : lds64(rs + 8 * q);
+                    for (int q = 0; q < PC / 8; q++) {
+                        const int o = part * PC + 8 * q;
+                        const uint2 v = from_global ? *reinterpret_cast<const uint2 *>(rg + o) : lds64(rs + o);
                         w[2 * q] = v.x;
                         w[2 * q + 1] = v.y;
                     }
@@ -357,15 +367,16 @@ __global__ void __launch_bounds__(kDThreads, 1)
                     f = __fdiv_rn(__fmul_rn(__uint_as_float(meta.y), rr), __uint_as_float(meta.x));
                 } else {
 #pragma unroll
-                    for (int q = 0; q < B / 4; q++)
+                    for (int q = 0; q < PC / 4; q++)
                         w[q] = 0u;
                 }
-                factors[fs * Lay::kTileBlocks + bl] = f;
+                if (part == 0)
+                    factors[fs * Lay::kTileBlocks + bl] = f;
                 // Codes to the swizzled A row: 16 codes per 16-byte unit (8 in f16).
 #pragma unroll
-                for (int u = 0; u < B / 16; u++) {
+                for (int u = 0; u < PC / 16; u++) {
                     if constexpr (!A16) {
-                        const int ua = b * (B / 16) + u;          // unit index along the A row
+                        const int ua = b * (PC / 16) + u;         // unit index along the A row
                         const int chunk = ua / 8, uc = ua % 8;
                         sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
                                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]));
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
                         }
 #pragma unroll
                         for (int hh = 0; hh < 2; hh++) {
-                            const int ua = 2 * (b * (B / 16) + u) + hh;
+                            const int ua = 2 * (b * (PC / 16) + u) + hh;
                             const int chunk = ua / 8, uc = ua % 8;
                             sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
                                    make_uint4(hv[4 * hh], hv[4 * hh + 1], hv[4 * hh + 2], hv[4 * hh + 3]));
@@ -414,7 +425,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
             float fb[Lay::kBlocksPerRow];
 #pragma unroll
             for (int b = 0; b < Lay::kBlocksPerRow; b++)
-                fb[b] = factors[fs * Lay::kTileBlocks + m * Lay::kBlocksPerRow + b];
+                fb[b] = factors[fs * Lay::kTileBlocks + (m * Lay::kBlocksPerRow + b) / Lay::kRowsPerBlock];
             if (i >= NOUT) {
                 if (et == 0) {
                     bulk_wait_read<NOUT - 1>();
@@ -434,12 +445,25 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 const int e0 = 32 * c;                     // first element (column) of the chunk
                 const int b = (B == 64) ? e0 / 64 : 0;     // block within the row (B = 64)
                 if constexpr (A16) {                       // remove the f16 bias 1152 of the codes
+                    constexpr int kBiasCols = Lay::kQuad ? 128 : B;   // the length H was applied over
                     if (!rotate) {
 #pragma unroll
                         for (int h = 0; h < 32; h++)
                             r[h] = __float_as_uint(__uint_as_float(r[h]) - 1152.0f);
-                    } else if (e0 % B == 0) {
-                        r[0] = __float_as_uint(__uint_as_float(r[0]) - 1152.0f * B);
+                    } else if (e0 % kBiasCols == 0) {
+                        r[0] = __float_as_uint(__uint_as_float(r[0]) - 1152.0f * kBiasCols);
+                    }
+                }
+                if constexpr (Lay::kQuad) {               // H_512 = H_4 (x) H_128: finish across the quarters' lanes
+                    if (rotate) {   // lower lane a + b, upper lane a - b, as one fma each
+                        const float sgn1 = (m & 1) ? -1.0f : 1.0f, sgn2 = (m & 2) ? -1.0f : 1.0f;
+#pragma unroll
+                        for (int h = 0; h < 32; h++) {
+                            float v = __uint_as_float(r[h]);
+                            v = fmaf(sgn1, v, __shfl_xor_sync(kFullMask, v, 1));
+                            v = fmaf(sgn2, v, __shfl_xor_sync(kFullMask, v, 2));
+                            r[h] = __float_as_uint(v);
+                        }
                     }
                 }
                 const float f = fb[b];
@@ -512,16 +536,22 @@ struct TcDecompressConfig {
 #ifndef TACO_DTC256_CFG
 #define TACO_DTC256_CFG 221
 #endif
+#ifndef TACO_DTC512_CFG
+#define TACO_DTC512_CFG 322
+#endif
 // Per block size, three digits: raw stages, A stages, output tiles.
 using DecompressTc64 = TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0>;
 using DecompressTc128 =
     TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10, 0>;
 using DecompressTc256 =
     TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10, 0>;
+using DecompressTc512 =
+    TcDecompressConfig<512, TACO_DTC512_CFG / 100, TACO_DTC512_CFG / 10 % 10, TACO_DTC512_CFG % 10, 0>;
 // INT8 codes (f16 operands: A stages and H twice as large).
 using DecompressI8x64 = TcDecompressConfig<64, 3, 2, 2, 1>;
 using DecompressI8x128 = TcDecompressConfig<128, 3, 2, 2, 1>;
 using DecompressI8x256 = TcDecompressConfig<256, 1, 1, 1, 1>;
+using DecompressI8x512 = TcDecompressConfig<512, 3, 2, 2, 1>;
 
 }  // namespace
 
@@ -532,6 +562,7 @@ KernelInfo decompress_kernel_info(int block, int code)
         case 64: return DecompressI8x64::info();
         case 128: return DecompressI8x128::info();
         case 256: return DecompressI8x256::info();
+        case 512: return DecompressI8x512::info();
         default: return KernelInfo{};
         }
     }
@@ -539,6 +570,7 @@ KernelInfo decompress_kernel_info(int block, int code)
     case 64: return DecompressTc64::info();
     case 128: return DecompressTc128::info();
     case 256: return DecompressTc256::info();
+    case 512: return DecompressTc512::info();
     default: return KernelInfo{};
     }
 }

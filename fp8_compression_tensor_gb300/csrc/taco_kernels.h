@@ -60,8 +60,8 @@ cudaError_t launch_compress(int block, Scheme scheme, const void *tmap, void *pa
 cudaError_t launch_decompress(int block, Scheme scheme, const void *tmap_y, const void *packed, int64_t nblocks,
                               uint32_t *fault, int grid, cudaStream_t stream);
 
-// CUDA-core codec for blocks 32 (a lane per block) and 512 (a warp per block);
-// fn == nullptr otherwise.  tile_blocks = blocks per CTA.
+// CUDA-core codec for block 32 (a lane per block); fn == nullptr otherwise.
+// tile_blocks = blocks per CTA.
 KernelInfo warp_codec_info(int block, bool compress);
 cudaError_t launch_warp_compress(int block, Scheme scheme, const void *x, void *packed, int64_t nblocks, int grid,
                                  cudaStream_t stream);

@@ -1,15 +1,12 @@
-// taco_warp_codec.cu -- compress and decompress for the block sizes of the
-// paper's block-size ablation that the tensor-core kernels do not take
-// (B = 32 and B = 512; "TACO: Efficient Communication Compression of
-// Intermediate Tensors for Scalable Tensor-Parallel LLM Training", Section
-// 5.3.3, Table 2), on the CUDA cores, for GB300 (sm_103a).
+// taco_warp_codec.cu -- compress and decompress for B = 32, the smallest
+// block of the paper's block-size ablation ("TACO: Efficient Communication
+// Compression of Intermediate Tensors for Scalable Tensor-Parallel LLM
+// Training", Section 5.3.3, Table 2), on the CUDA cores, for GB300 (sm_103a).
 //
-// B = 512: one warp per block, lane l holding the 16 consecutive elements
-// [16 l, 16 l + 16).  The Walsh-Hadamard butterfly (a, b) -> (a + b, a - b)
-// runs in registers for strides 1..8 and across lanes (xor-shuffles of the
-// lane index) for strides 16..256, which gives H_B y in Sylvester order;
-// energy and maximum are warp reductions.  B = 32: one lane per block, the
-// whole butterfly, energy and maximum in registers (a warp per block would
+// One lane per block: the whole Walsh-Hadamard butterfly (a, b) -> (a + b,
+// a - b) at strides 1..16, which gives H_32 y in Sylvester order, and the
+// block's energy and maximum stay in registers (a 32-element block is too
+// short for a tensor-core tile row of 128 bytes, and a warp per block would
 // spend every per-block scalar on 32 elements only).  Every scheme of the
 // tensor-core kernels is supported (variants and code formats; see
 // taco_compress.cu), with the same arithmetic shortcuts: the rotation is
@@ -21,181 +18,11 @@
 namespace taco {
 namespace {
 
-constexpr int kWarpThreads = 256;   // 8 blocks in flight per CTA
-
-template <int E>
-__device__ __forceinline__ void fwht_warp(float (&v)[E], int lane)
-{
-    // Strides 1 .. E/2 inside the lane.
-#pragma unroll
-    for (int h = 1; h < E; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < E; i++) {
-            if ((i & h) == 0) {
-                const float a = v[i], b = v[i + h];
-                v[i] = a + b;
-                v[i + h] = a - b;
-            }
-        }
-    }
-    // Strides E .. 16 E across lanes: the lane whose bit is clear keeps a + b.
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < E; i++) {
-            const float o = __shfl_xor_sync(kFullMask, v[i], m);
-            v[i] = upper ? (o - v[i]) : (v[i] + o);
-        }
-    }
-}
-
-__device__ __forceinline__ float warp_sum(float x)
-{
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1)
-        x += __shfl_xor_sync(kFullMask, x, m);
-    return x;
-}
-
-__device__ __forceinline__ float warp_max(float x)
-{
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1)
-        x = fmaxf(x, __shfl_xor_sync(kFullMask, x, m));
-    return x;
-}
+constexpr int kWarpThreads = 256;   // blocks per CTA and pass
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h)
 {
     return __uint_as_float(h << 16);
-}
-
-// Value of one code byte of a format (exact).
-__device__ __forceinline__ float code_value(int code, uint32_t byte)
-{
-    if (code == 0)
-        return e4m3x2_to_float2(byte & 0xffu).x;
-    if (code == 1)
-        return e5m2x2_to_float2(byte & 0xffu).x;
-    return static_cast<float>(static_cast<int8_t>(byte));
-}
-
-template <int B>
-__global__ void __launch_bounds__(kWarpThreads) taco_warp_compress_kernel(const uint16_t *__restrict__ x,
-                                                                          uint8_t *__restrict__ packed,
-                                                                          int64_t nblocks, const Scheme scheme)
-{
-    constexpr int E = B / 32;
-    constexpr int kRec = B + 8;
-    grid_launch_dependents();
-    grid_dependency_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kWarpThreads / 32);
-    const bool rotate = scheme.variant != 2;
-    const bool adaptive = scheme.variant == 0 || scheme.variant == 3;
-    const bool dual_scale = scheme.variant != 3;
-    static_assert(B == 512, "the warp-per-block kernels serve B = 512");
-    const float rB = 0.0441941738241592203f;   // 1/sqrt(512) in binary32
-    const float rr = rotate ? rB : 1.0f;
-    const float qmax = code_qmax(scheme.code);
-
-    for (int64_t k = (static_cast<int64_t>(blockIdx.x) * kWarpThreads + threadIdx.x) / 32; k < nblocks;
-         k += warps) {
-        float v[E];
-        const uint16_t *src = x + k * B + lane * E;
-#pragma unroll
-        for (int q = 0; q < E / 8; q++) {   // 16-byte loads (lane slices start at 32-byte multiples)
-            const uint4 w = *reinterpret_cast<const uint4 *>(src + 8 * q);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                v[8 * q + 2 * j] = bf16_bits_to_float(ws[j] & 0xffffu);
-                v[8 * q + 2 * j + 1] = bf16_bits_to_float(ws[j] >> 16);
-            }
-        }
-        float e = 0.f;
-#pragma unroll
-        for (int i = 0; i < E; i++)
-            e = fmaf(v[i], v[i], e);
-        e = warp_sum(e);
-        if (rotate)
-            fwht_warp<E>(v, lane);
-        float ymax = 0.f;
-#pragma unroll
-        for (int i = 0; i < E; i++)
-            ymax = fmaxf(ymax, fabsf(v[i]));
-        ymax = warp_max(ymax);
-
-        const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(e * (1.0f / B) + kEps)) : 1.0f;
-        float s = 0.f, kq = 0.f;
-        if (!dual_scale) {
-            s = 1.0f;
-            kq = __fmul_rn(alpha, rr);
-        } else if (ymax > 0.f) {
-            s = __fdiv_rn(__fmul_rn(__fmul_rn(alpha, ymax), rr), qmax);
-            kq = __fdiv_rn(qmax, ymax);
-        }
-        uint8_t *rec = packed + k * kRec;
-        uint32_t cw[E / 4];
-#pragma unroll
-        for (int j = 0; j < E / 4; j++)
-            cw[j] = ymax > 0.f ? encode4(scheme.code, v[4 * j] * kq, v[4 * j + 1] * kq, v[4 * j + 2] * kq,
-                                         v[4 * j + 3] * kq)
-                               : 0u;
-        // Records start at multiples of B + 8 bytes (8-byte aligned).
-#pragma unroll
-        for (int j = 0; j < E / 8; j++)
-            *reinterpret_cast<uint2 *>(rec + lane * E + 8 * j) = make_uint2(cw[2 * j], cw[2 * j + 1]);
-        if (lane == 0)
-            *reinterpret_cast<uint2 *>(rec + B) = make_uint2(__float_as_uint(alpha), __float_as_uint(s));
-    }
-}
-
-template <int B>
-__global__ void __launch_bounds__(kWarpThreads) taco_warp_decompress_kernel(const uint8_t *__restrict__ packed,
-                                                                            uint16_t *__restrict__ y,
-                                                                            int64_t nblocks, const Scheme scheme)
-{
-    constexpr int E = B / 32;
-    constexpr int kRec = B + 8;
-    grid_launch_dependents();
-    grid_dependency_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kWarpThreads / 32);
-    const bool rotate = scheme.variant != 2;
-    static_assert(B == 512, "the warp-per-block kernels serve B = 512");
-    const float rB = 0.0441941738241592203f;
-    const float rr = rotate ? rB : 1.0f;
-
-    for (int64_t k = (static_cast<int64_t>(blockIdx.x) * kWarpThreads + threadIdx.x) / 32; k < nblocks;
-         k += warps) {
-        const uint8_t *rec = packed + k * kRec;
-        const uint2 meta = *reinterpret_cast<const uint2 *>(rec + B);
-        const float f = __fdiv_rn(__fmul_rn(__uint_as_float(meta.y), rr), __uint_as_float(meta.x));
-        float v[E];
-#pragma unroll
-        for (int j = 0; j < E / 8; j++) {
-            const uint2 w = *reinterpret_cast<const uint2 *>(rec + lane * E + 8 * j);
-            const uint32_t ws[2] = {w.x, w.y};
-#pragma unroll
-            for (int h = 0; h < 2; h++)
-#pragma unroll
-                for (int b = 0; b < 4; b++)
-                    v[8 * j + 4 * h + b] = code_value(scheme.code, (ws[h] >> (8 * b)) & 0xffu);
-        }
-        if (rotate)
-            fwht_warp<E>(v, lane);
-        uint16_t *dst = y + k * B + lane * E;
-#pragma unroll
-        for (int q = 0; q < E / 8; q++) {
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; j++)
-                o[j] = float2_to_bf16x2(v[8 * q + 2 * j] * f, v[8 * q + 2 * j + 1] * f);
-            *reinterpret_cast<uint4 *>(dst + 8 * q) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    }
 }
 
 // In-register Walsh-Hadamard transform of n values (strides 1 .. n/2).
@@ -326,14 +153,6 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_decompress_kernel(cons
     }
 }
 
-template <int B>
-KernelInfo warp_info(bool compress)
-{
-    void *fn = compress ? reinterpret_cast<void *>(&taco_warp_compress_kernel<B>)
-                        : reinterpret_cast<void *>(&taco_warp_decompress_kernel<B>);
-    return KernelInfo{fn, 0, kWarpThreads, kWarpThreads / 32, kWarpThreads / 32};
-}
-
 KernelInfo lane_info(bool compress)
 {
     void *fn = compress ? reinterpret_cast<void *>(&taco_lane_compress_kernel)
@@ -345,11 +164,7 @@ KernelInfo lane_info(bool compress)
 
 KernelInfo warp_codec_info(int block, bool compress)
 {
-    switch (block) {
-    case 32: return lane_info(compress);
-    case 512: return warp_info<512>(compress);
-    default: return KernelInfo{};
-    }
+    return block == 32 ? lane_info(compress) : KernelInfo{};
 }
 
 cudaError_t launch_warp_compress(int block, Scheme scheme, const void *x, void *packed, int64_t nblocks, int grid,

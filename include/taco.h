@@ -34,8 +34,8 @@
  *   - rows == 0 or hidden == 0 is an empty tensor: TACO_OK, nothing launched,
  *     pointers may be NULL.
  *   - Supported blocks: 32, 64, 128, 256, 512 (TACO_ERR_UNSUPPORTED_BLOCK
- *     otherwise; Section 5.3.3 ablates these sizes).  64, 128 and 256 run on
- *     the tensor cores, 32 and 512 on a warp-per-block CUDA-core codec.
+ *     otherwise; Section 5.3.3 ablates these sizes).  64 to 512 run on the
+ *     tensor cores, 32 on a lane-per-block CUDA-core codec.
  *   - Inputs must be finite with |x| < 2^56; beyond that the FP32 block
  *     energy of Eq. (6) can overflow and the output is unspecified.
  *   - Kernels that wait on the copy engine give up after about one second,
