@@ -85,6 +85,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.taco_decompress_ex.restype = i32
         lib.taco_reduce_shards_ex.argtypes = [ctypes.POINTER(vp), i32, i64, i64, optp, vp, vp]
         lib.taco_reduce_shards_ex.restype = i32
+        lib.taco_selftest_wait_timeout.argtypes = [vp]
+        lib.taco_selftest_wait_timeout.restype = i32
         lib.taco_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.taco_device_status.restype = i32
         lib.taco_status_string.argtypes = [i32]

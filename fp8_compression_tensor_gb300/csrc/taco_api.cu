@@ -383,6 +383,16 @@ taco_status_t taco_reduce_shards_ex(const void *const *packed_shards, int num_sh
     return reduce_impl(packed_shards, num_shards, rows, hidden, options->block, scheme, packed_out, stream);
 }
 
+taco_status_t taco_selftest_wait_timeout(taco_stream_t stream)
+{
+    DeviceState *dev = nullptr;
+    const taco_status_t st = device_state(&dev);
+    if (st != TACO_OK)
+        return st;
+    const cudaError_t e = launch_wait_selftest(dev->fault, 2000000ull, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TACO_OK : cuda_fail(e);
+}
+
 taco_status_t taco_device_status(taco_stream_t stream, uint32_t *flags_out)
 {
     DeviceState *dev = nullptr;

@@ -21,6 +21,7 @@ constexpr float kQmax = 448.0f;
 constexpr uint32_t kFaultCompress = 1u;
 constexpr uint32_t kFaultDecompress = 2u;
 constexpr uint32_t kFaultReduce = 4u;
+constexpr uint32_t kFaultSelfTest = 8u;   // the wait-timeout self-test (taco_selftest_wait_timeout)
 
 // A wait on the copy engine gives up after this long (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

@@ -68,6 +68,10 @@ cudaError_t launch_warp_compress(int block, Scheme scheme, const void *x, void *
 cudaError_t launch_warp_decompress(int block, Scheme scheme, const void *packed, void *y, int64_t nblocks, int grid,
                                    cudaStream_t stream);
 
+// One CTA whose wait on a barrier nothing completes gives up after limit_ns
+// and sets the self-test fault bit.
+cudaError_t launch_wait_selftest(uint32_t *fault, uint64_t limit_ns, cudaStream_t stream);
+
 constexpr int kMaxShards = 16;
 
 struct ReduceArgs {

@@ -235,16 +235,16 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Single-thread bounded wait for phase `parity` of `bar` (kWaitLimitNs);
-// sets `fault_bit` and returns false on a timeout.
+// Single-thread bounded wait for phase `parity` of `bar` (limit_ns, by
+// default kWaitLimitNs); sets `fault_bit` and returns false on a timeout.
 __device__ __forceinline__ bool mbar_wait_bounded_thread(uint32_t bar, uint32_t parity, uint32_t *fault,
-                                                         uint32_t fault_bit)
+                                                         uint32_t fault_bit, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(fault, fault_bit);
             return false;
         }

@@ -169,11 +169,21 @@ TACO_API taco_status_t taco_reduce_shards_ex(const void *const *packed_shards, i
 /*
  * Synchronises `stream`, then reads and clears the current device's fault
  * flags (bit 0: compress, bit 1: decompress, bit 2: shard reduce gave up
- * waiting for a copy or a tile assignment).
+ * waiting for a copy or a tile assignment; bit 3: the self-test below).
  * *flags_out (may be NULL) receives them.  Returns TACO_ERR_DEVICE_FAULT if any
  * flag was set, TACO_ERR_CUDA if a CUDA call failed, TACO_OK otherwise.
  */
 TACO_API taco_status_t taco_device_status(taco_stream_t stream, uint32_t *flags_out);
+
+/*
+ * Self-test of the fault path (no counterpart in the paper): launches one CTA
+ * on `stream` whose bounded wait on an mbarrier that nothing completes runs
+ * out after about 2 ms; it then sets bit 3 of the device fault flags and
+ * exits, exactly as every kernel does when a wait gives up.  A following
+ * taco_device_status() returns TACO_ERR_DEVICE_FAULT with that bit (and
+ * clears it).  Nothing faults, traps or hangs.  Returns TACO_OK once launched.
+ */
+TACO_API taco_status_t taco_selftest_wait_timeout(taco_stream_t stream);
 
 /* Static, human-readable name of a status. */
 TACO_API const char *taco_status_string(taco_status_t status);
