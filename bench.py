@@ -334,14 +334,49 @@ def run_taco(args, rank, world):
 
     scheme = {"variant": args.variant, "code": args.code}
 
-    def op_compress(r):
-        taco.compress(xs[r], block, out=packs[r], stream=stream, **scheme)
+    def op_compress(r, st=None):
+        taco.compress(xs[r], block, out=packs[r], stream=st or stream, **scheme)
 
-    def op_reduce(r):
-        taco.reduce_shards(segs[r], seg_rows, hidden, block, out=reds[r], stream=stream, **scheme)
+    def op_reduce(r, st=None):
+        taco.reduce_shards(segs[r], seg_rows, hidden, block, out=reds[r], stream=st or stream, **scheme)
 
-    def op_decompress(r):
-        taco.decompress(packs[r], rows, hidden, block, out=ys[r], stream=stream, **scheme)
+    def op_decompress(r, st=None):
+        taco.decompress(packs[r], rows, hidden, block, out=ys[r], stream=st or stream, **scheme)
+
+    # The cycle of R steps as a graph with one branch per kernel kind and an
+    # edge only where data flows (compress -> reduce / decompress of the same
+    # set, and a set's next compress after the reads of its records): the
+    # three kernels of a step work on different buffer sets (micro-batches),
+    # so one kernel's tail overlaps the next kernel's start.
+    branch = {"C": torch.cuda.Stream(dev), "R": torch.cuda.Stream(dev), "D": torch.cuda.Stream(dev)}
+
+    def cycle_with_data_edges():
+        ops = []
+        for k in range(R):
+            ops += [("C", k % R), ("R", (k - 2) % R), ("D", (k - 3) % R)]
+        for st in branch.values():
+            st.wait_stream(stream)
+        last_write, readers = {}, {}
+        for kind, r in ops:
+            st = branch[kind]
+            reads = [("x", r)] if kind == "C" else [("packed", r)]
+            writes = [("packed", r)] if kind == "C" else [("reduced", r)] if kind == "R" else [("y", r)]
+            for buf in reads + writes:
+                if buf in last_write:
+                    st.wait_event(last_write[buf])
+            for buf in writes:
+                for e in readers.get(buf, []):
+                    st.wait_event(e)
+            {"C": op_compress, "R": op_reduce, "D": op_decompress}[kind](r, st)
+            done = torch.cuda.Event()
+            done.record(st)
+            for buf in reads:
+                readers.setdefault(buf, []).append(done)
+            for buf in writes:
+                last_write[buf] = done
+                readers[buf] = []
+        for st in branch.values():
+            stream.wait_stream(st)
 
     def step(k):
         op_compress(k % R)
@@ -366,7 +401,7 @@ def run_taco(args, rank, world):
             step(k)
         stream.synchronize()
         step_graphs = [capture(lambda k=k: step(k)) for k in range(R)]
-        cycle_graph = capture(lambda: [step(k) for k in range(R)])   # R steps, sets 0..R-1 once each
+        cycle_graph = capture(cycle_with_data_edges)   # R steps, sets 0..R-1 once each
         solo_graphs = {name: capture(lambda fn=fn: [fn(r) for r in range(R)])
                        for name, fn in (("compress", op_compress), ("reduce", op_reduce),
                                         ("decompress", op_decompress))}
@@ -580,7 +615,9 @@ def run_taco(args, rank, world):
                    "bytes_per_step": "6N: 2N compressed + 2N logical bf16 of the reduced segments + 2N decompressed",
                    "l2": (f"no flush; inputs larger than L2: {R} rotating buffer sets of {set_bytes / 1e6:.1f} MB "
                           f"(L2 {l2 / 1e6:.0f} MB); step k compresses set k, reduces set k-2, decompresses "
-                          f"set k-3; graph replays (one graph per R steps), one CUDA-event pair around the K steps"),
+                          f"set k-3; graph replays (one graph per R steps, a branch per kernel kind with edges "
+                          f"only for data dependencies, so kernels of different sets overlap at their "
+                          f"boundaries), one CUDA-event pair around the K steps"),
                    "buffer_sets": R,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops,
