@@ -50,10 +50,11 @@ namespace taco {
 namespace {
 
 constexpr int kDRows = 128;        // MMA rows per tile
-constexpr int kDThreads = 320;     // 10 warps
+// Threads: loader, MMA, 4 transposer warps and EPG groups of 4 epilogue warps.
+__host__ __device__ constexpr int dthreads(int epg) { return 192 + 128 * epg; }
 constexpr int kGroup = 128;        // threads of the transposer / epilogue groups
 
-template <int B, int RS, int AS, int NOUT, int A16>
+template <int B, int RS, int AS, int NOUT, int A16, int EPG>
 struct TcDecompressLayout {
     // B = 512: each block is four A rows of 128 codes (quarters).
     static constexpr bool kQuad = B == 512;
@@ -79,6 +80,7 @@ struct TcDecompressLayout {
     static constexpr int kOutChunkBytes = kOutRows * 128;
     static constexpr int kOutBytes = kOutChunks * kOutChunkBytes;
     static constexpr int FS = AS + 2;                              // factor slots
+    static_assert(EPG == 1 || (FS % 2 == 0 && NOUT % 2 == 0), "two epilogue groups take alternate tiles");
     // Offsets from the 1024-byte aligned base.
     static constexpr int kOffA = 0;
     static constexpr int kOffH = kOffA + AS * kAStageBytes;
@@ -89,7 +91,7 @@ struct TcDecompressLayout {
     // barrier of item i - RS, when the epilogue has read items up to
     // i - RS - AS - 2: a published-tile slot is reused only after every
     // reader is done with it.
-    static_assert(kTileRing >= RS + AS + 3, "published-tile slot reused too early");
+    static_assert(kTileRing >= RS + AS + 2 + EPG, "published-tile slot reused too early");
     static constexpr int kOffSched = kOffFac + FS * kTileBlocks * 4;   // 16-byte aligned
     static_assert(kOffSched % 16 == 0, "cancel responses need 16-byte alignment");
     static constexpr int kOffBar = kOffSched + kSchedBytes;
@@ -162,13 +164,14 @@ __device__ void write_hadamard_f16_sw128(uint8_t *h, bool rotate)
     }
 }
 
-template <int B, int RS, int AS, int NOUT, int A16>
-__global__ void __launch_bounds__(kDThreads, 1)
+template <int B, int RS, int AS, int NOUT, int A16, int EPG>
+__global__ void __launch_bounds__(dthreads(EPG), 1)
     taco_decompress_kernel(const __grid_constant__ CUtensorMap tmap_y, const uint8_t *__restrict__ packed,
                               int64_t nblocks, uint32_t *__restrict__ fault, const Scheme scheme)
 {
-    using Lay = TcDecompressLayout<B, RS, AS, NOUT, A16>;
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT, A16, EPG>;
     constexpr int FS = Lay::FS;
+    constexpr int NBG = NOUT / EPG;   // output tiles per epilogue group
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -255,13 +258,13 @@ __global__ void __launch_bounds__(kDThreads, 1)
             for (;; i++) {
                 const int64_t t = sched.response(i);
                 if (t < 0) {
-                    sched.publish_end(i, 1);
+                    sched.publish_end(i, EPG);
                     break;
                 }
                 sched.request(++requested);      // no failure seen yet: keep kSchedAhead in flight
                 const int s = i % RS;
                 if (i >= RS && !mbar_wait_bounded_thread(raw_empty(s), ((i / RS) - 1) & 1, fault, kFaultDecompress)) {
-                    sched.publish_end(i, 1);
+                    sched.publish_end(i, EPG);
                     break;
                 }
                 sched.publish(i, t);
@@ -408,15 +411,18 @@ __global__ void __launch_bounds__(kDThreads, 1)
             }
         }
     } else {
-        // ---- epilogue (warps 6..9): one MMA row per thread ------------------
-        const int et = threadIdx.x - 192;          // 0..127
+        // ---- epilogue (warps 6.., EPG groups of 4): one MMA row per thread ---
+        // Group g takes the tiles i with i % EPG == g.
+        const int grp = (warp - 6) / 4;
+        const int et = threadIdx.x - 192 - kGroup * grp;   // 0..127 within the group
         const int q = warp & 3;
         const int m = 32 * q + lane;               // accumulator row
-        for (int i = 0;; i++) {
+        for (int kt = 0;; kt++) {                  // kt: tiles this group has handled
+            const int i = EPG * kt + grp;
             const int64_t t = sched.tile_warp(i);
             if (t < 0)
                 break;
-            const int acc = i & 1, fs = i % FS, ob = i % NOUT;
+            const int acc = i & 1, fs = i % FS, ob = grp * NBG + kt % NBG;
             if (!mbar_wait_bounded(acc_full(acc), (i >> 1) & 1, fault, kFaultDecompress))
                 break;
             if (!mbar_wait_bounded(fac_full(fs), (i / FS) & 1, fault, kFaultDecompress))
@@ -426,12 +432,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
 #pragma unroll
             for (int b = 0; b < Lay::kBlocksPerRow; b++)
                 fb[b] = factors[fs * Lay::kTileBlocks + (m * Lay::kBlocksPerRow + b) / Lay::kRowsPerBlock];
-            if (i >= NOUT) {
+            if (kt >= NBG) {
                 if (et == 0) {
-                    bulk_wait_read<NOUT - 1>();
+                    bulk_wait_read<NBG - 1>();
                     mbar_arrive(out_free(ob));
                 }
-                if (!mbar_wait_bounded(out_free(ob), ((i / NOUT) - 1) & 1, fault, kFaultDecompress))
+                if (!mbar_wait_bounded(out_free(ob), ((kt / NBG) - 1) & 1, fault, kFaultDecompress))
                     break;
             }
             const uint32_t out = sbase + Lay::kOffOut + ob * Lay::kOutBytes;
@@ -491,8 +497,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 mbar_arrive(acc_empty(acc));
             fence_proxy_async_smem();
             mbar_arrive(out_done(ob));
-            if (warp == 6) {
-                if (!mbar_wait_bounded(out_done(ob), (i / NOUT) & 1, fault, kFaultDecompress))
+            if (warp == 6 + 4 * grp) {   // the group's first warp stores the tile
+                if (!mbar_wait_bounded(out_done(ob), (kt / NBG) & 1, fault, kFaultDecompress))
                     break;
                 if (lane == 0) {
                     const int32_t y0 = static_cast<int32_t>(t * Lay::kOutRows);
@@ -515,15 +521,15 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
 }
 
-template <int B, int RS, int AS, int NOUT, int A16>
+template <int B, int RS, int AS, int NOUT, int A16, int EPG = 1>
 struct TcDecompressConfig {
-    using Lay = TcDecompressLayout<B, RS, AS, NOUT, A16>;
+    using Lay = TcDecompressLayout<B, RS, AS, NOUT, A16, EPG>;
     static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
     static_assert(Lay::kRawBytes % 16 == 0, "raw stage alignment");
-    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, RS, AS, NOUT, A16>); }
+    static void *fn() { return reinterpret_cast<void *>(&taco_decompress_kernel<B, RS, AS, NOUT, A16, EPG>); }
     static KernelInfo info()
     {
-        return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), kDThreads, Lay::kTileBlocks, 0};
+        return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), dthreads(EPG), Lay::kTileBlocks, 0};
     }
 };
 
@@ -540,13 +546,28 @@ struct TcDecompressConfig {
 #define TACO_DTC512_CFG 322
 #endif
 // Per block size, three digits: raw stages, A stages, output tiles.
-using DecompressTc64 = TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0>;
+#ifndef TACO_DEPG64
+#define TACO_DEPG64 1
+#endif
+#ifndef TACO_DEPG128
+#define TACO_DEPG128 1
+#endif
+#ifndef TACO_DEPG256
+#define TACO_DEPG256 1
+#endif
+#ifndef TACO_DEPG512
+#define TACO_DEPG512 2
+#endif
+// EPG: epilogue groups (2 where the epilogue is the bottleneck: B = 512's
+// butterfly across the quarters' lanes).
+using DecompressTc64 =
+    TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0, TACO_DEPG64>;
 using DecompressTc128 =
-    TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10, 0>;
+    TcDecompressConfig<128, TACO_DTC128_CFG / 100, TACO_DTC128_CFG / 10 % 10, TACO_DTC128_CFG % 10, 0, TACO_DEPG128>;
 using DecompressTc256 =
-    TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10, 0>;
+    TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10, 0, TACO_DEPG256>;
 using DecompressTc512 =
-    TcDecompressConfig<512, TACO_DTC512_CFG / 100, TACO_DTC512_CFG / 10 % 10, TACO_DTC512_CFG % 10, 0>;
+    TcDecompressConfig<512, TACO_DTC512_CFG / 100, TACO_DTC512_CFG / 10 % 10, TACO_DTC512_CFG % 10, 0, TACO_DEPG512>;
 // INT8 codes (f16 operands: A stages and H twice as large).
 using DecompressI8x64 = TcDecompressConfig<64, 3, 2, 2, 1>;
 using DecompressI8x128 = TcDecompressConfig<128, 3, 2, 2, 1>;
