@@ -26,7 +26,14 @@
 namespace taco {
 
 constexpr int kSchedSlots = 16;   // cancel-response slots
-constexpr int kSchedAhead = 4;    // cancel requests in flight
+#ifndef TACO_SCHED_AHEAD
+#define TACO_SCHED_AHEAD 1
+#endif
+// Cancel requests in flight.  One is enough to hide the round trip behind a
+// tile's loads; with more, the CTAs that ask first claim most of the tiles of
+// a small grid before the others have asked once (0.2-0.4 us slower per
+// launch at 33.5 M elements).
+constexpr int kSchedAhead = TACO_SCHED_AHEAD;
 constexpr int kTileRing = 16;     // published-tile slots
 
 // Shared-memory bytes: responses (16 B each, 16-byte aligned first), tiles
