@@ -17,11 +17,12 @@
 //   warp 0  TMA producer: 2-D tiled loads (128-byte swizzle) of the tile into a
 //           ring of STAGES shared-memory stages;
 //   warp 1  allocates tensor memory and issues the B/16 tcgen05.mma of a tile
-//           (M = 128, N = B, K = B, BF16 in, FP32 out) into one of two
-//           accumulators, then commits to the stage's "empty" and the
-//           accumulator's "full" barriers;
-//   warps 2.. epilogue, one or two groups of 4 warps (group g takes every
-//           EPG-th tile, so two tiles' epilogues can overlap): each thread
+//           (M = 128, N = B, K = B, BF16 in, FP32 out) into one of two to
+//           four accumulators (tile i into accumulator i mod their number),
+//           then commits to the stage's "empty" and the accumulator's "full"
+//           barriers;
+//   warps 2.. epilogue, EPG groups of 4 warps (group g takes every EPG-th
+//           tile, so EPG tiles' epilogues can overlap): each thread
 //           owns one row (one block) of the
 //           accumulator in its TMEM lane: pass 1 reads it for the energy (by
 //           Parseval, sum_j y_j^2 = B sum_j G_j^2) and the maximum, pass 2
@@ -78,7 +79,10 @@ struct TcCompressLayout {
     static constexpr int kRec = B + 8;
     static constexpr int kOutBytes = kTileBlocks * kRec;           // one record tile (multiple of 16)
     static constexpr int kAccCols = kRowElems;                     // TMEM columns of one accumulator
-    static constexpr int kTmemCols = 2 * kAccCols;                 // two accumulators
+    // Accumulators in tensor memory (512 columns): up to four, so that more
+    // than two epilogue groups can hold one each while the MMA fills the next.
+    static constexpr int kNumAcc = 4 * kAccCols <= 512 ? 4 : 2;
+    static constexpr int kTmemCols = kNumAcc * kAccCols;
     // Offsets from the 1024-byte aligned base.
     static constexpr int kOffA = 0;
     static constexpr int kOffH = kOffA + STAGES * kStageBytes;
@@ -91,7 +95,7 @@ struct TcCompressLayout {
     static constexpr int kOffSched = kOffOut + NOUT * kOutBytes;   // 16-byte aligned
     static_assert(kOffSched % 16 == 0, "cancel responses need 16-byte alignment");
     static constexpr int kOffBar = kOffSched + kSchedBytes;        // 8-byte aligned
-    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * NOUT;
+    static constexpr int kNumBars = 2 * STAGES + 2 * kNumAcc + 2 * NOUT;
     static constexpr int kOffTmem = kOffBar + 8 * kNumBars;
     static constexpr int kBytes = kOffTmem + 16;
     static constexpr int kSmem = kBytes + 1024;                    // slack for 1024-byte alignment
@@ -140,10 +144,11 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     const uint32_t bar0 = sbase + Lay::kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    constexpr int NACC = Lay::kNumAcc;
     auto acc_full_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-    auto acc_empty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-    auto out_free_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
-    auto rec_done_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + NOUT + b); };
+    auto acc_empty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + NACC + a); };
+    auto out_free_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 * NACC + b); };
+    auto rec_done_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 * NACC + NOUT + b); };
     const TileSched sched{sbase + Lay::kOffSched, fault, kFaultCompress};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
 
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int a = 0; a < 2; a++) {
+        for (int a = 0; a < NACC; a++) {
             mbar_init(acc_full_bar(a), 1);
             mbar_init(acc_empty_bar(a), kEpiThreads / 32);   // the 4 warps of the group reading it
         }
@@ -236,8 +241,8 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             for (;; i++) {
                 if (sched.tile_thread(i) < 0)
                     break;
-                const int s = i % STAGES, acc = i & 1;
-                if (i >= 2 && !mbar_wait_bounded_thread(acc_empty_bar(acc), ((i >> 1) - 1) & 1, fault,
+                const int s = i % STAGES, acc = i % NACC;
+                if (i >= NACC && !mbar_wait_bounded_thread(acc_empty_bar(acc), ((i / NACC) - 1) & 1, fault,
                                                         kFaultCompress))
                     break;
                 if (!mbar_wait_bounded_thread(full_bar(s), (i / STAGES) & 1, fault, kFaultCompress))
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             }
             // All MMAs issued must finish before tensor memory is freed.
             if (i > 0)
-                mbar_wait_bounded_thread(acc_full_bar((i - 1) & 1), ((i - 1) >> 1) & 1, fault, kFaultCompress);
+                mbar_wait_bounded_thread(acc_full_bar((i - 1) % NACC), ((i - 1) / NACC) & 1, fault, kFaultCompress);
         }
     } else {
         // ---- epilogue (warps 2 .. 2+4*EPG-1) --------------------------------
@@ -304,8 +309,8 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             const int64_t t = sched.tile_warp(i);
             if (t < 0)
                 break;
-            const int acc = i & 1;
-            if (!mbar_wait_bounded(acc_full_bar(acc), (i >> 1) & 1, fault, kFaultCompress))
+            const int acc = i % NACC;
+            if (!mbar_wait_bounded(acc_full_bar(acc), (i / NACC) & 1, fault, kFaultCompress))
                 break;
             tc_fence_after_sync();
             const uint32_t taddr =
@@ -456,8 +461,11 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                     *reinterpret_cast<uint2 *>(dst + o) = *reinterpret_cast<const uint2 *>(src + o);
             }
         }
+        // The shared-memory sources of this thread's stores must be read
+        // before the CTA exits; the writes themselves complete before the
+        // grid does.
         if (et == 0)
-            bulk_wait_all<0>();
+            bulk_wait_read<0>();
     }
 
     // ---- tear-down -------------------------------------------------------
@@ -481,10 +489,10 @@ struct TcCompressConfig {
 };
 
 #ifndef TACO_TC64_CFG
-#define TACO_TC64_CFG 821
+#define TACO_TC64_CFG 641
 #endif
 #ifndef TACO_TC128_CFG
-#define TACO_TC128_CFG 421
+#define TACO_TC128_CFG 331
 #endif
 #ifndef TACO_TC256_CFG
 #define TACO_TC256_CFG 211

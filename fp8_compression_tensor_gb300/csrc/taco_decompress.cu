@@ -509,8 +509,11 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                 }
             }
         }
+        // The shared-memory sources of this thread's stores must be read
+        // before the CTA exits; the writes themselves complete before the
+        // grid does.
         if (et == 0)
-            bulk_wait_all<0>();
+            bulk_wait_read<0>();
     }
 
     tc_fence_before_sync();
