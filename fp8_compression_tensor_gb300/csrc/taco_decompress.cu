@@ -553,7 +553,7 @@ struct TcDecompressConfig {
 #define TACO_DEPG64 1
 #endif
 #ifndef TACO_DEPG128
-#define TACO_DEPG128 1
+#define TACO_DEPG128 2
 #endif
 #ifndef TACO_DEPG256
 #define TACO_DEPG256 1
@@ -561,8 +561,9 @@ struct TcDecompressConfig {
 #ifndef TACO_DEPG512
 #define TACO_DEPG512 2
 #endif
-// EPG: epilogue groups (2 where the epilogue is the bottleneck: B = 512's
-// butterfly across the quarters' lanes).
+// EPG: epilogue groups (2 where the epilogue limits: B = 512's butterfly
+// across the quarters' lanes; B = 128, where two tiles' epilogues in flight
+// shorten each launch's tail).
 using DecompressTc64 =
     TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0, TACO_DEPG64>;
 using DecompressTc128 =
