@@ -190,6 +190,31 @@ __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b)
 }
 
 // ---------------------------------------------------------------------------
+// Packed FP32x2 arithmetic (one instruction for two lanes of data)
+// ---------------------------------------------------------------------------
+
+// Packed add written as PTX (one instruction for two lanes of data).
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
 // Number formats
 // ---------------------------------------------------------------------------
 
@@ -216,6 +241,36 @@ __device__ __forceinline__ float code_qmax(int code)
     return code == 0 ? 448.0f : code == 1 ? 57344.0f : 127.0f;
 }
 
+// INT8 codes of four values (first in the low byte), rounded to the nearest
+// integer, ties to even, for |u| < 2^22: u + 1.5 * 2^23 lies in [2^23, 2^24),
+// where FP32 values are spaced by 1, so the FP32 add rounds u to an integer
+// (nearest, ties to even) and the low byte of the sum's bits is that integer
+// modulo 256, its two's-complement byte.
+constexpr float kInt8Magic = 12582912.0f;   // 1.5 * 2^23
+__device__ __forceinline__ uint32_t int8x4_from_float(float a, float b, float c, float d)
+{
+    const float2 m = make_float2(kInt8Magic, kInt8Magic);
+    const float2 x = add2(make_float2(a, b), m), y = add2(make_float2(c, d), m);
+    const uint32_t lo = __byte_perm(__float_as_uint(x.x), __float_as_uint(x.y), 0x0040);
+    const uint32_t hi = __byte_perm(__float_as_uint(y.x), __float_as_uint(y.y), 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
+}
+
+// Values of four INT8 codes (exact): the byte v ^ 0x80 = v + 128 under the
+// exponent byte 0x4B is the FP32 value 2^23 + v + 128, and subtracting
+// 2^23 + 128 is exact.
+__device__ __forceinline__ void int8x4_to_float(uint32_t x, float2 &q0, float2 &q1)
+{
+    const uint32_t u = x ^ 0x80808080u;
+    const float2 off = make_float2(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
+    q0 = add2(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))),
+              off);
+    q1 = add2(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))),
+              off);
+}
+
 // Codes of four values, first value in the low byte.  INT8 rounds to the
 // nearest integer, ties to even; the callers keep |u| <= 127 (u = Q_max y /
 // max|y| rounds to at most 127, and a direct cast has |u| <= sqrt(B) <= 16).
@@ -225,11 +280,7 @@ __device__ __forceinline__ uint32_t encode4(int code, float a, float b, float c,
         return e4m3x2_from_float2(a, b) | (e4m3x2_from_float2(c, d) << 16);
     if (code == 1)
         return e5m2x2_from_float2(a, b) | (e5m2x2_from_float2(c, d) << 16);
-    const uint32_t ia = static_cast<uint32_t>(__float2int_rn(a)) & 0xffu;
-    const uint32_t ib = static_cast<uint32_t>(__float2int_rn(b)) & 0xffu;
-    const uint32_t ic = static_cast<uint32_t>(__float2int_rn(c)) & 0xffu;
-    const uint32_t id = static_cast<uint32_t>(__float2int_rn(d)) & 0xffu;
-    return ia | (ib << 8) | (ic << 16) | (id << 24);
+    return int8x4_from_float(a, b, c, d);
 }
 
 // Cvt_FP32 (Eq. 11) of the two E4M3 codes in the low 16 bits of `pair`
@@ -262,31 +313,6 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi)
 {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// ---------------------------------------------------------------------------
-// Packed FP32x2 arithmetic (one instruction for two lanes of data)
-// ---------------------------------------------------------------------------
-
-// Packed add written as PTX (one instruction for two lanes of data).
-__device__ __forceinline__ float2 add2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-
-__device__ __forceinline__ float max3(float a, float b, float c)
-{
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
 

@@ -88,9 +88,7 @@ __device__ __forceinline__ void decode4(uint32_t x, float2 &q0, float2 &q1)
         q0 = e5m2x2_to_float2(x & 0xffffu);
         q1 = e5m2x2_to_float2(x >> 16);
     } else {
-        q0 = make_float2(static_cast<float>(static_cast<int8_t>(x)), static_cast<float>(static_cast<int8_t>(x >> 8)));
-        q1 = make_float2(static_cast<float>(static_cast<int8_t>(x >> 16)),
-                         static_cast<float>(static_cast<int8_t>(x >> 24)));
+        int8x4_to_float(x, q0, q1);
     }
 }
 

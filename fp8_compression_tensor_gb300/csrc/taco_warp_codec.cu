@@ -125,9 +125,12 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_decompress_kernel(cons
 #pragma unroll
             for (int h = 0; h < 2; h++) {
                 if (scheme.code == 2) {
-#pragma unroll
-                    for (int b = 0; b < 4; b++)
-                        v[8 * j + 4 * h + b] = static_cast<float>(static_cast<int8_t>(ws[h] >> (8 * b)));
+                    float2 lo, hi;
+                    int8x4_to_float(ws[h], lo, hi);
+                    v[8 * j + 4 * h] = lo.x;
+                    v[8 * j + 4 * h + 1] = lo.y;
+                    v[8 * j + 4 * h + 2] = hi.x;
+                    v[8 * j + 4 * h + 3] = hi.y;
                 } else {
                     const float2 lo = scheme.code == 0 ? e4m3x2_to_float2(ws[h] & 0xffffu)
                                                        : e5m2x2_to_float2(ws[h] & 0xffffu);
