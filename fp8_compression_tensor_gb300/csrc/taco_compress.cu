@@ -324,14 +324,16 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             // the 4 quarters' rows sit in 4 neighbouring lanes, and a butterfly
             // over lanes (xor 1, xor 2) finishes the rotation; the rotated
             // quarter stays in registers for pass 2.
-            float yq[Lay::kQuad ? 128 : 1];
+            // The rotated quarter goes back into its TMEM columns (pass 2
+            // reads it from there, as for the other block sizes).
             if constexpr (Lay::kQuad) {
                 const float sgn1 = (quarter & 1) ? -1.0f : 1.0f, sgn2 = (quarter & 2) ? -1.0f : 1.0f;
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < 4; c++) {
                     uint32_t r[32];
                     tmem_ld32(taddr + 32 * c, r);
                     tmem_ld_wait();
+                    tmem_regs_ready(r);
 #pragma unroll
                     for (int j = 0; j < 32; j++) {
                         float v = __uint_as_float(r[j]);
@@ -339,15 +341,18 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                             v = fmaf(sgn1, v, __shfl_xor_sync(kFullMask, v, 1));
                             v = fmaf(sgn2, v, __shfl_xor_sync(kFullMask, v, 2));
                         }
-                        yq[32 * c + j] = v;
+                        r[j] = __float_as_uint(v);
                     }
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
-                        const float2 y = make_float2(yq[32 * c + j], yq[32 * c + j + 1]);
+                        const float2 y = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
                         e2[(j >> 1) & 3] = fma2(y, y, e2[(j >> 1) & 3]);
                         ymax = max3(ymax, fabsf(y.x), fabsf(y.y));
                     }
+                    if (rotate)
+                        tmem_st32(taddr + 32 * c, r);
                 }
+                tmem_st_wait();
             } else {
 #pragma unroll
                 for (int c = 0; c < B / 32; c++) {
@@ -404,14 +409,8 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
 #pragma unroll
             for (int c = 0; c < Lay::kAccCols / 32; c++) {
                 uint32_t r[32];
-                if constexpr (Lay::kQuad) {
-#pragma unroll
-                    for (int j = 0; j < 32; j++)
-                        r[j] = __float_as_uint(yq[32 * c + j]);
-                } else {
-                    tmem_ld32(taddr + 32 * c, r);
-                    tmem_ld_wait();
-                }
+                tmem_ld32(taddr + 32 * c, r);
+                tmem_ld_wait();
                 uint32_t cw[8];
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
@@ -498,7 +497,7 @@ struct TcCompressConfig {
 #define TACO_TC256_CFG 211
 #endif
 #ifndef TACO_TC512_CFG
-#define TACO_TC512_CFG 421
+#define TACO_TC512_CFG 341
 #endif
 // Per block size, three digits: A stages, epilogue groups, buffers per group.
 using CompressTc64 = TcCompressConfig<64, TACO_TC64_CFG / 100, TACO_TC64_CFG / 10 % 10, TACO_TC64_CFG % 10>;

@@ -16,11 +16,13 @@
 //   warp 0    bulk-copies each tile of records (contiguous, B + 8 bytes each)
 //             into a ring of raw stages;
 //   warp 1    allocates tensor memory and issues the MMAs of a tile into one
-//             of two accumulators (M = 128 rows, N = 128, K = 32 per MMA);
+//             of two to four accumulators (tile i into accumulator i mod
+//             their number; M = 128 rows, N = 128, K = 32 per MMA);
 //   warps 2-5 "transposers": each thread takes one MMA row, copies its codes
 //             from the record into the 128-byte swizzled K-major A layout,
 //             and writes the block's factor s / sqrt(B) / alpha;
-//   warps 6-9 epilogue: each thread reads its row of the accumulator from
+//   warps 6.. epilogue, EPG groups of 4 warps taking alternate tiles: each
+//             thread reads its row of the accumulator from
 //             TMEM, scales it by the factor, converts two values per cvt to
 //             bf16 into a swizzled output tile, which one thread writes with
 //             2-D TMA stores (rows past the tensor's end are not written).
@@ -79,8 +81,15 @@ struct TcDecompressLayout {
     static constexpr int kOutChunks = B == 64 ? 1 : kPartCodes / 64;   // 64-element chunks of a y row
     static constexpr int kOutChunkBytes = kOutRows * 128;
     static constexpr int kOutBytes = kOutChunks * kOutChunkBytes;
-    static constexpr int FS = AS + 2;                              // factor slots
-    static_assert(EPG == 1 || (FS % 2 == 0 && NOUT % 2 == 0), "two epilogue groups take alternate tiles");
+    // Accumulators in tensor memory (512 columns): up to four, so that more
+    // than two epilogue groups can hold one each while the MMA fills the next.
+    static constexpr int kNumAcc = 4 * kAccCols <= 512 ? 4 : 2;
+    // Factor slots: the transposer writes item i's factors after the MMA of
+    // item i - AS, which needed item i - AS - kNumAcc's accumulator back from
+    // the epilogue (which had read that item's factors): AS + kNumAcc slots
+    // are never overwritten before they are read.
+    static constexpr int FS = AS + kNumAcc;
+    static_assert(NOUT % EPG == 0, "every epilogue group owns NOUT / EPG output tiles");
     // Offsets from the 1024-byte aligned base.
     static constexpr int kOffA = 0;
     static constexpr int kOffH = kOffA + AS * kAStageBytes;
@@ -91,15 +100,15 @@ struct TcDecompressLayout {
     // barrier of item i - RS, when the epilogue has read items up to
     // i - RS - AS - 2: a published-tile slot is reused only after every
     // reader is done with it.
-    static_assert(kTileRing >= RS + AS + 2 + EPG, "published-tile slot reused too early");
+    static_assert(kTileRing >= RS + AS + kNumAcc + EPG, "published-tile slot reused too early");
     static constexpr int kOffSched = kOffFac + FS * kTileBlocks * 4;   // 16-byte aligned
     static_assert(kOffSched % 16 == 0, "cancel responses need 16-byte alignment");
     static constexpr int kOffBar = kOffSched + kSchedBytes;
-    static constexpr int kNumBars = 2 * RS + 2 * AS + 4 + 2 * NOUT + FS;
+    static constexpr int kNumBars = 2 * RS + 2 * AS + 2 * kNumAcc + 2 * NOUT + FS;
     static constexpr int kOffTmem = kOffBar + 8 * kNumBars;
     static constexpr int kBytes = kOffTmem + 16;
     static constexpr int kSmem = kBytes + 1024;
-    static constexpr int kTmemCols = 2 * kAccCols;
+    static constexpr int kTmemCols = kNumAcc * kAccCols;
 };
 
 // The MMA's B operand, K-major, 128-byte swizzle, in E4M3 (+1 = 0x38,
@@ -181,11 +190,12 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
     auto raw_empty = [&](int s) { return bar0 + 8u * (RS + s); };
     auto a_full = [&](int j) { return bar0 + 8u * (2 * RS + j); };
     auto a_empty = [&](int j) { return bar0 + 8u * (2 * RS + AS + j); };
+    constexpr int NACC = Lay::kNumAcc;
     auto acc_full = [&](int a) { return bar0 + 8u * (2 * RS + 2 * AS + a); };
-    auto acc_empty = [&](int a) { return bar0 + 8u * (2 * RS + 2 * AS + 2 + a); };
-    auto out_free = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + b); };
-    auto out_done = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + NOUT + b); };
-    auto fac_full = [&](int f) { return bar0 + 8u * (2 * RS + 2 * AS + 4 + 2 * NOUT + f); };
+    auto acc_empty = [&](int a) { return bar0 + 8u * (2 * RS + 2 * AS + NACC + a); };
+    auto out_free = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 2 * NACC + b); };
+    auto out_done = [&](int b) { return bar0 + 8u * (2 * RS + 2 * AS + 2 * NACC + NOUT + b); };
+    auto fac_full = [&](int f) { return bar0 + 8u * (2 * RS + 2 * AS + 2 * NACC + 2 * NOUT + f); };
     const TileSched sched{sbase + Lay::kOffSched, fault, kFaultDecompress};
     float *factors = reinterpret_cast<float *>(base + Lay::kOffFac);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + Lay::kOffTmem);
@@ -203,7 +213,7 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
             mbar_init(a_full(j), kGroup / 32);
             mbar_init(a_empty(j), 1);
         }
-        for (int a = 0; a < 2; a++) {
+        for (int a = 0; a < NACC; a++) {
             mbar_init(acc_full(a), 1);
             mbar_init(acc_empty(a), kGroup / 32);
         }
@@ -288,9 +298,9 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
             for (;; i++) {
                 if (sched.tile_thread(i) < 0)
                     break;
-                const int j = i % AS, acc = i & 1;
-                if (i >= 2 &&
-                    !mbar_wait_bounded_thread(acc_empty(acc), ((i >> 1) - 1) & 1, fault, kFaultDecompress))
+                const int j = i % AS, acc = i % NACC;
+                if (i >= NACC &&
+                    !mbar_wait_bounded_thread(acc_empty(acc), ((i / NACC) - 1) & 1, fault, kFaultDecompress))
                     break;
                 if (!mbar_wait_bounded_thread(a_full(j), (i / AS) & 1, fault, kFaultDecompress))
                     break;
@@ -325,7 +335,7 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                 tc_commit(acc_full(acc));
             }
             if (i > 0)
-                mbar_wait_bounded_thread(acc_full((i - 1) & 1), ((i - 1) >> 1) & 1, fault, kFaultDecompress);
+                mbar_wait_bounded_thread(acc_full((i - 1) % NACC), ((i - 1) / NACC) & 1, fault, kFaultDecompress);
         }
     } else if (warp < 6) {
         // ---- transposers (warps 2..5): one MMA row per thread ---------------
@@ -422,8 +432,8 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
             const int64_t t = sched.tile_warp(i);
             if (t < 0)
                 break;
-            const int acc = i & 1, fs = i % FS, ob = grp * NBG + kt % NBG;
-            if (!mbar_wait_bounded(acc_full(acc), (i >> 1) & 1, fault, kFaultDecompress))
+            const int acc = i % NACC, fs = i % FS, ob = grp * NBG + kt % NBG;
+            if (!mbar_wait_bounded(acc_full(acc), (i / NACC) & 1, fault, kFaultDecompress))
                 break;
             if (!mbar_wait_bounded(fac_full(fs), (i / FS) & 1, fault, kFaultDecompress))
                 break;
@@ -546,7 +556,7 @@ struct TcDecompressConfig {
 #define TACO_DTC256_CFG 221
 #endif
 #ifndef TACO_DTC512_CFG
-#define TACO_DTC512_CFG 322
+#define TACO_DTC512_CFG 323
 #endif
 // Per block size, three digits: raw stages, A stages, output tiles.
 #ifndef TACO_DEPG64
@@ -559,11 +569,11 @@ struct TcDecompressConfig {
 #define TACO_DEPG256 1
 #endif
 #ifndef TACO_DEPG512
-#define TACO_DEPG512 2
+#define TACO_DEPG512 3
 #endif
-// EPG: epilogue groups (2 where the epilogue limits: B = 512's butterfly
-// across the quarters' lanes; B = 128, where two tiles' epilogues in flight
-// shorten each launch's tail).
+// EPG: epilogue groups (3 for B = 512, whose epilogue limits with the
+// butterfly across the quarters' lanes; 2 for B = 128, where two tiles'
+// epilogues in flight shorten each launch's tail).
 using DecompressTc64 =
     TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0, TACO_DEPG64>;
 using DecompressTc128 =
