@@ -47,10 +47,10 @@ bool tensor_core_block(int block)
 }
 
 // Row length of the tensor-core kernels' view of the tensor: the block, or
-// 128 for B = 512 (four rows per block).
+// 128 for B = 256 and 512 (two or four rows per block).
 int view_row_elems(int block)
 {
-    return block == 512 ? 128 : block;
+    return block > 128 ? 128 : block;
 }
 
 taco_status_t cuda_fail(cudaError_t e)

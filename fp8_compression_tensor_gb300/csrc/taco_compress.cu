@@ -6,9 +6,12 @@
 // 128 blocks as the rows of G (128 x B, bf16), Y = G H_B^T = G H_B (H_B is
 // symmetric) holds y_k = H_B G_k in row k.  The products G_kj * (+-1) are exact
 // and the tensor core accumulates in FP32, so Y is the unnormalised rotation
-// of Eq. (8) up to FP32 summation order.
+// of Eq. (8) up to FP32 summation order.  Blocks of 256 and 512 elements are
+// 2 or 4 rows of 128 (tiles of 64 or 32 blocks): the MMA applies H_128 to each
+// part and a butterfly across the parts' neighbouring TMEM lanes applies the
+// H_2 or H_4 factor of H_B = H_2 (x) H_128 or H_4 (x) H_128.
 //
-// Scheduling: one CTA per tile of 128 blocks, one CTA per SM resident; a
+// Scheduling: one CTA per tile of 128 rows, one CTA per SM resident; a
 // running CTA takes its own tile, then the tiles of CTAs it cancels before
 // they start (cluster launch control, taco_sched.cuh), so CTAs that get more
 // memory bandwidth take more tiles and all SMs finish together.
@@ -16,14 +19,14 @@
 // Roles in a CTA, one tile at a time:
 //   warp 0  TMA producer: 2-D tiled loads (128-byte swizzle) of the tile into a
 //           ring of STAGES shared-memory stages;
-//   warp 1  allocates tensor memory and issues the B/16 tcgen05.mma of a tile
-//           (M = 128, N = B, K = B, BF16 in, FP32 out) into one of two to
+//   warp 1  allocates tensor memory and issues the tcgen05.mma of a tile
+//           (M = 128, N = K = row length, BF16 in, FP32 out) into one of two to
 //           four accumulators (tile i into accumulator i mod their number),
 //           then commits to the stage's "empty" and the accumulator's "full"
 //           barriers;
 //   warps 2.. epilogue, EPG groups of 4 warps (group g takes every EPG-th
 //           tile, so EPG tiles' epilogues can overlap): each thread
-//           owns one row (one block) of the
+//           owns one row (one block or part) of the
 //           accumulator in its TMEM lane: pass 1 reads it for the energy (by
 //           Parseval, sum_j y_j^2 = B sum_j G_j^2) and the maximum, pass 2
 //           reads it again and converts y * (Q_max / max|y|) to E4M3 two
@@ -53,7 +56,7 @@ namespace {
 
 
 constexpr int kTcRows = 128;       // blocks per tile = MMA M = TMEM lanes
-constexpr int kEpiThreads = 128;   // threads of one epilogue group (4 warps, one per TMEM lane quarter)
+constexpr int kEpiThreads = 128;   // threads of one epilogue group (4 warps, one per TMEM lane part)
 
 __host__ __device__ constexpr int tc_threads(int groups) { return 64 + kEpiThreads * groups; }
 
@@ -63,13 +66,13 @@ __host__ __device__ constexpr int tc_threads(int groups) { return 64 + kEpiThrea
 template <int B, int STAGES, int EPG, int NBG>
 struct TcCompressLayout {
     static constexpr int NOUT = EPG * NBG;                         // record-tile buffers
-    // B = 512: each block is four A rows of 128 elements (quarters).
-    static constexpr bool kQuad = B == 512;
-    static constexpr int kRowElems = kQuad ? 128 : B;              // elements of an A row
-    static constexpr int kRowsPerBlock = kQuad ? 4 : 1;
+    // B = 256 and 512: each block is B / 128 A rows of 128 elements (its
+    // parts), in neighbouring rows of the tile.
+    static constexpr bool kSplit = B > 128;
+    static constexpr int kRowElems = kSplit ? 128 : B;             // elements of an A row
+    static constexpr int kRowsPerBlock = kSplit ? B / 128 : 1;
     static constexpr int kTileBlocks = kTcRows / kRowsPerBlock;    // blocks per tile
-    static constexpr int kN = kRowElems <= 128 ? kRowElems : 128;  // MMA N = order of the Hadamard matrix used
-    static constexpr int kHalves = kRowElems / kN;                 // 2 for B = 256 (Kronecker split)
+    static constexpr int kN = kRowElems;                           // MMA N = order of the Hadamard matrix used
     static constexpr int kKSteps = kN / 16;                        // MMAs (K = 16) per product with H_N
     static constexpr int kChunks = kRowElems / 64;                 // 128-byte K chunks of a row
     static constexpr int kChunkBytesA = kTcRows * 128;             // one chunk of the A tile
@@ -250,39 +253,12 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * Lay::kAccCols);
                 const uint32_t a_stage = a0 + s * Lay::kStageBytes;
-                if constexpr (Lay::kHalves == 1) {
 #pragma unroll
-                    for (int kk = 0; kk < Lay::kKSteps; kk++) {
-                        const uint32_t koff = (kk & 3) * 32;   // 16 bf16 = 32 bytes along K
-                        const uint64_t ad = sw128_kmajor_desc(a_stage + (kk >> 2) * Lay::kChunkBytesA + koff);
-                        const uint64_t bd = sw128_kmajor_desc(h0 + (kk >> 2) * Lay::kChunkBytesH + koff);
-                        tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
-                    }
-                } else {
-                    // B = 256 with H_256 = [[H, H], [H, -H]] (H = H_128): the
-                    // columns [0, 128) get H g0 + H g1 and [128, 256) get
-                    // H g0 - H g1, where g0 / g1 are the block's two halves
-                    // (A chunks 0-1 / 2-3); the minus is the negate-A bit.
-                    // Without rotation (identity) half h gets g_h only.
-#pragma unroll
-                    for (int out_half = 0; out_half < 2; out_half++) {
-#pragma unroll
-                        for (int in_half = 0; in_half < 2; in_half++) {
-                            if (!rotate && in_half != out_half)
-                                continue;
-                            const uint32_t id =
-                                (rotate && out_half == 1 && in_half == 1) ? (idesc | kMmaNegateA) : idesc;
-                            const bool first = rotate ? in_half == 0 : true;
-#pragma unroll
-                            for (int kk = 0; kk < Lay::kKSteps; kk++) {
-                                const uint32_t koff = (kk & 3) * 32;
-                                const uint64_t ad = sw128_kmajor_desc(
-                                    a_stage + (2 * in_half + (kk >> 2)) * Lay::kChunkBytesA + koff);
-                                const uint64_t bd = sw128_kmajor_desc(h0 + (kk >> 2) * Lay::kChunkBytesH + koff);
-                                tc_mma_bf16(d + out_half * 128, ad, bd, id, (first && kk == 0) ? 0u : 1u);
-                            }
-                        }
-                    }
+                for (int kk = 0; kk < Lay::kKSteps; kk++) {
+                    const uint32_t koff = (kk & 3) * 32;   // 16 bf16 = 32 bytes along K
+                    const uint64_t ad = sw128_kmajor_desc(a_stage + (kk >> 2) * Lay::kChunkBytesA + koff);
+                    const uint64_t bd = sw128_kmajor_desc(h0 + (kk >> 2) * Lay::kChunkBytesH + koff);
+                    tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(empty_bar(s));
                 tc_commit(acc_full_bar(acc));
@@ -295,10 +271,10 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
         // ---- epilogue (warps 2 .. 2+4*EPG-1) --------------------------------
         const int grp = (warp - 2) / 4;                 // epilogue group
         const int et = threadIdx.x - 64 - kEpiThreads * grp;   // 0..127 within the group
-        const int q = warp & 3;                         // TMEM lane quarter of this warp
+        const int q = warp & 3;                         // TMEM lane part of this warp
         const int row = 32 * q + lane;                  // accumulator row
         const int blk = row / Lay::kRowsPerBlock;       // block within the tile
-        const int quarter = row % Lay::kRowsPerBlock;   // B = 512: which 128 elements of the block
+        const int part = row % Lay::kRowsPerBlock;      // B = 256 / 512: which 128 elements of the block
         const bool store_warp = ((warp - 2) & 3) == 0;  // first warp of the group issues the stores
         const float rB = (B == 64)    ? 0.125f
                          : (B == 128) ? 0.0883883476483184405f
@@ -320,14 +296,14 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             float2 e2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             float ymax = 0.f;
-            // B = 512: H_512 = H_4 (x) H_128; the MMA gave H_128 of each quarter,
-            // the 4 quarters' rows sit in 4 neighbouring lanes, and a butterfly
-            // over lanes (xor 1, xor 2) finishes the rotation; the rotated
-            // quarter stays in registers for pass 2.
-            // The rotated quarter goes back into its TMEM columns (pass 2
-            // reads it from there, as for the other block sizes).
-            if constexpr (Lay::kQuad) {
-                const float sgn1 = (quarter & 1) ? -1.0f : 1.0f, sgn2 = (quarter & 2) ? -1.0f : 1.0f;
+            // B = 256 / 512: H_B = H_2 (x) H_128 / H_4 (x) H_128 (Sylvester
+            // order); the MMA gave H_128 of each part, the parts' rows sit in
+            // neighbouring lanes, and a butterfly over lanes (xor 1; and xor 2
+            // for four parts) finishes the rotation.  The rotated part goes
+            // back into its TMEM columns; pass 2 reads it from there, as for
+            // the other block sizes.
+            if constexpr (Lay::kSplit) {
+                const float sgn1 = (part & 1) ? -1.0f : 1.0f, sgn2 = (part & 2) ? -1.0f : 1.0f;
 #pragma unroll 1
                 for (int c = 0; c < 4; c++) {
                     uint32_t r[32];
@@ -339,7 +315,8 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                         float v = __uint_as_float(r[j]);
                         if (rotate) {   // lower lane a + b, upper lane a - b, as one fma each
                             v = fmaf(sgn1, v, __shfl_xor_sync(kFullMask, v, 1));
-                            v = fmaf(sgn2, v, __shfl_xor_sync(kFullMask, v, 2));
+                            if constexpr (Lay::kRowsPerBlock == 4)
+                                v = fmaf(sgn2, v, __shfl_xor_sync(kFullMask, v, 2));
                         }
                         r[j] = __float_as_uint(v);
                     }
@@ -370,11 +347,10 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             const float2 e01 = add2(e2[0], e2[1]), e23 = add2(e2[2], e2[3]);
             const float2 ee = add2(e01, e23);
             float etot = ee.x + ee.y;
-            if constexpr (Lay::kQuad) {   // the block's four quarters
-                etot += __shfl_xor_sync(kFullMask, etot, 1);
-                etot += __shfl_xor_sync(kFullMask, etot, 2);
-                ymax = fmaxf(ymax, __shfl_xor_sync(kFullMask, ymax, 1));
-                ymax = fmaxf(ymax, __shfl_xor_sync(kFullMask, ymax, 2));
+#pragma unroll
+            for (int d = 1; d < Lay::kRowsPerBlock; d <<= 1) {   // over the block's parts
+                etot += __shfl_xor_sync(kFullMask, etot, d);
+                ymax = fmaxf(ymax, __shfl_xor_sync(kFullMask, ymax, d));
             }
             const float m = etot * (1.0f / (static_cast<float>(B) * B));
             const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(m + kEps)) : 1.0f;
@@ -402,7 +378,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                     break;
             }
             const uint32_t rec_block = sbase + Lay::kOffOut + ob * Lay::kOutBytes + blk * Lay::kRec;
-            const uint32_t rec = rec_block + quarter * 128;
+            const uint32_t rec = rec_block + part * 128;
 
             // Pass 2: codes (Eq. 10) two per cvt, 32 per chunk.
             const float2 k2 = make_float2(k, k);
@@ -434,7 +410,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             if (lane == 0)
                 mbar_arrive(acc_empty_bar(acc));
 
-            if (quarter == 0)
+            if (part == 0)
                 sts64(rec_block + B, __float_as_uint(alpha), __float_as_uint(s));
             fence_proxy_async_smem();
             mbar_arrive(rec_done_bar(ob));
@@ -453,7 +429,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                     bulk_commit();
                 }
             }
-            if ((nvalid & 1) && blk == nvalid - 1 && quarter == 0) {
+            if ((nvalid & 1) && blk == nvalid - 1 && part == 0) {
                 uint8_t *dst = packed + (blk0 + blk) * Lay::kRec;
                 const uint8_t *src = base + Lay::kOffOut + ob * Lay::kOutBytes + blk * Lay::kRec;
                 for (int o = 0; o < Lay::kRec; o += 8)
@@ -494,7 +470,7 @@ struct TcCompressConfig {
 #define TACO_TC128_CFG 331
 #endif
 #ifndef TACO_TC256_CFG
-#define TACO_TC256_CFG 211
+#define TACO_TC256_CFG 331
 #endif
 #ifndef TACO_TC512_CFG
 #define TACO_TC512_CFG 341

@@ -26,9 +26,10 @@
 //             TMEM, scales it by the factor, converts two values per cvt to
 //             bf16 into a swizzled output tile, which one thread writes with
 //             2-D TMA stores (rows past the tensor's end are not written).
-// Block sizes: 128 (one block per row, H_128), 256 (one block per row, two
-// 128-code halves; H_256 = [[H, H], [H, -H]] with the negate-A bit), and 64
-// (two blocks per row, H = diag(H_64, H_64)).
+// Block sizes: 128 (one block per row, H_128), 64 (two blocks per row,
+// H = diag(H_64, H_64)), 256 and 512 (two or four rows of 128 codes per
+// block, H_128 on each and a butterfly across the parts' neighbouring TMEM
+// lanes for the H_2 or H_4 factor of H_B).
 //
 // Ablations (Scheme): E5M2 codes are the MMA's operand as E5M2 (H in E5M2);
 // INT8 codes (A16: the 8-bit integer MMA kind does not exist on sm_103a) go
@@ -58,26 +59,24 @@ constexpr int kGroup = 128;        // threads of the transposer / epilogue group
 
 template <int B, int RS, int AS, int NOUT, int A16, int EPG>
 struct TcDecompressLayout {
-    // B = 512: each block is four A rows of 128 codes (quarters).
-    static constexpr bool kQuad = B == 512;
+    // B = 256 and 512: each block is B / 128 A rows of 128 codes (its parts),
+    // in neighbouring rows of the tile.
+    static constexpr bool kSplit = B > 128;
     static constexpr int kBlocksPerRow = B == 64 ? 2 : 1;
-    static constexpr int kRowsPerBlock = kQuad ? 4 : 1;
+    static constexpr int kRowsPerBlock = kSplit ? B / 128 : 1;
     static constexpr int kTileBlocks = kDRows * kBlocksPerRow / kRowsPerBlock;
-    static constexpr int kPartCodes = kQuad ? 128 : B;             // codes of one block (part) in a row
+    static constexpr int kPartCodes = kSplit ? 128 : B;            // codes of one block (part) in a row
     static constexpr int kRowCodes = kPartCodes * kBlocksPerRow;   // 128 or 256
     static constexpr int kElem = A16 ? 2 : 1;                      // bytes per code in the A operand
     static constexpr int kAChunks = kRowCodes * kElem / 128;       // 128-byte chunks of an A row
-    static constexpr int kInHalves = B == 256 ? 2 : 1;             // 128-code halves of a block
-    static constexpr int kChunksPerHalf = kAChunks / kInHalves;    // = H's K chunks
-    static constexpr int kHalves = B == 256 ? 2 : 1;
-    static constexpr int kAccCols = 128 * kHalves;                 // TMEM columns per tile
+    static constexpr int kAccCols = 128;                           // TMEM columns per tile
     static constexpr int kRec = B + 8;
     static constexpr int kRawBytes = kTileBlocks * kRec;
     static constexpr int kAStageBytes = kDRows * kRowCodes * kElem;
     static constexpr int kAChunkBytes = kDRows * 128;
     static constexpr int kHChunkBytes = 128 * 128;                 // 128 rows of H, 128 bytes of K
-    static constexpr int kHBytes = kChunksPerHalf * kHChunkBytes;
-    static constexpr int kOutRows = kQuad ? kDRows : kTileBlocks;  // rows of the y view per tile
+    static constexpr int kHBytes = kAChunks * kHChunkBytes;        // K chunks of H = those of an A row
+    static constexpr int kOutRows = kSplit ? kDRows : kTileBlocks; // rows of the y view per tile
     static constexpr int kOutChunks = B == 64 ? 1 : kPartCodes / 64;   // 64-element chunks of a y row
     static constexpr int kOutChunkBytes = kOutRows * 128;
     static constexpr int kOutBytes = kOutChunks * kOutChunkBytes;
@@ -308,27 +307,16 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * Lay::kAccCols);
                 const uint32_t a_st = sbase + Lay::kOffA + j * Lay::kAStageBytes;
 #pragma unroll
-                for (int oh = 0; oh < Lay::kHalves; oh++) {
-                    bool first = true;
+                for (int c = 0; c < Lay::kAChunks; c++) {
 #pragma unroll
-                    for (int ih = 0; ih < Lay::kInHalves; ih++) {
-                        if (!rotate && Lay::kHalves == 2 && ih != oh)
-                            continue;   // identity: output half h takes input half h only
-                        const uint32_t id = (rotate && oh == 1 && ih == 1) ? (idesc | kMmaNegateA) : idesc;
-#pragma unroll
-                        for (int c = 0; c < Lay::kChunksPerHalf; c++) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; kk++) {   // 32 bytes of K per MMA
-                                const uint64_t ad = sw128_kmajor_desc(
-                                    a_st + (ih * Lay::kChunksPerHalf + c) * Lay::kAChunkBytes + 32 * kk);
-                                const uint64_t bd = sw128_kmajor_desc(h0 + c * Lay::kHChunkBytes + 32 * kk);
-                                if constexpr (A16)
-                                    tc_mma_bf16(d + 128 * oh, ad, bd, id, (first && kk == 0) ? 0u : 1u);
-                                else
-                                    tc_mma_f8(d + 128 * oh, ad, bd, id, (first && kk == 0) ? 0u : 1u);
-                                first = false;
-                            }
-                        }
+                    for (int kk = 0; kk < 4; kk++) {   // 32 bytes of K per MMA
+                        const uint64_t ad = sw128_kmajor_desc(a_st + c * Lay::kAChunkBytes + 32 * kk);
+                        const uint64_t bd = sw128_kmajor_desc(h0 + c * Lay::kHChunkBytes + 32 * kk);
+                        const uint32_t accumulate = (c == 0 && kk == 0) ? 0u : 1u;
+                        if constexpr (A16)
+                            tc_mma_bf16(d, ad, bd, idesc, accumulate);
+                        else
+                            tc_mma_f8(d, ad, bd, idesc, accumulate);
                     }
                 }
                 tc_commit(a_empty(j));
@@ -362,7 +350,7 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
             for (int b = 0; b < Lay::kBlocksPerRow; b++) {
                 constexpr int PC = Lay::kPartCodes;
                 const int bl = (m * Lay::kBlocksPerRow + b) / Lay::kRowsPerBlock;   // block within the tile
-                const int part = m % Lay::kRowsPerBlock;                             // B = 512: quarter
+                const int part = m % Lay::kRowsPerBlock;                             // B = 256 / 512: part
                 uint32_t w[PC / 4];
                 float f = 0.f;
                 if (bl < nvalid) {
@@ -461,7 +449,7 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                 const int e0 = 32 * c;                     // first element (column) of the chunk
                 const int b = (B == 64) ? e0 / 64 : 0;     // block within the row (B = 64)
                 if constexpr (A16) {                       // remove the f16 bias 1152 of the codes
-                    constexpr int kBiasCols = Lay::kQuad ? 128 : B;   // the length H was applied over
+                    constexpr int kBiasCols = Lay::kPartCodes;   // the length H was applied over
                     if (!rotate) {
 #pragma unroll
                         for (int h = 0; h < 32; h++)
@@ -470,14 +458,15 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                         r[0] = __float_as_uint(__uint_as_float(r[0]) - 1152.0f * kBiasCols);
                     }
                 }
-                if constexpr (Lay::kQuad) {               // H_512 = H_4 (x) H_128: finish across the quarters' lanes
+                if constexpr (Lay::kSplit) {   // H_B = H_2 / H_4 (x) H_128: finish across the parts' lanes
                     if (rotate) {   // lower lane a + b, upper lane a - b, as one fma each
                         const float sgn1 = (m & 1) ? -1.0f : 1.0f, sgn2 = (m & 2) ? -1.0f : 1.0f;
 #pragma unroll
                         for (int h = 0; h < 32; h++) {
                             float v = __uint_as_float(r[h]);
                             v = fmaf(sgn1, v, __shfl_xor_sync(kFullMask, v, 1));
-                            v = fmaf(sgn2, v, __shfl_xor_sync(kFullMask, v, 2));
+                            if constexpr (Lay::kRowsPerBlock == 4)
+                                v = fmaf(sgn2, v, __shfl_xor_sync(kFullMask, v, 2));
                             r[h] = __float_as_uint(v);
                         }
                     }
@@ -553,7 +542,7 @@ struct TcDecompressConfig {
 #define TACO_DTC128_CFG 322
 #endif
 #ifndef TACO_DTC256_CFG
-#define TACO_DTC256_CFG 221
+#define TACO_DTC256_CFG 323
 #endif
 #ifndef TACO_DTC512_CFG
 #define TACO_DTC512_CFG 323
@@ -566,13 +555,13 @@ struct TcDecompressConfig {
 #define TACO_DEPG128 2
 #endif
 #ifndef TACO_DEPG256
-#define TACO_DEPG256 1
+#define TACO_DEPG256 3
 #endif
 #ifndef TACO_DEPG512
 #define TACO_DEPG512 3
 #endif
-// EPG: epilogue groups (3 for B = 512, whose epilogue limits with the
-// butterfly across the quarters' lanes; 2 for B = 128, where two tiles'
+// EPG: epilogue groups (3 for B = 256 and 512, whose epilogues carry the
+// butterfly across the parts' lanes; 2 for B = 128, where two tiles'
 // epilogues in flight shorten each launch's tail).
 using DecompressTc64 =
     TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0, TACO_DEPG64>;
@@ -585,7 +574,7 @@ using DecompressTc512 =
 // INT8 codes (f16 operands: A stages and H twice as large).
 using DecompressI8x64 = TcDecompressConfig<64, 3, 2, 2, 1>;
 using DecompressI8x128 = TcDecompressConfig<128, 3, 2, 2, 1>;
-using DecompressI8x256 = TcDecompressConfig<256, 1, 1, 1, 1>;
+using DecompressI8x256 = TcDecompressConfig<256, 3, 2, 2, 1>;
 using DecompressI8x512 = TcDecompressConfig<512, 3, 2, 2, 1>;
 
 }  // namespace

@@ -159,7 +159,6 @@ __host__ __device__ constexpr uint32_t mma_idesc_e5m2_f32(int M, int N)
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-constexpr uint32_t kMmaNegateA = 1u << 13;   // instruction-descriptor bit: negate A
 
 // D[tmem] = A * B^T (+ D if accumulate): A is M x K, B is N x K, both from
 // shared-memory descriptors, 16-bit operands (BF16 or F16 per the
