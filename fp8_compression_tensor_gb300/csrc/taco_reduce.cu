@@ -12,11 +12,12 @@
 //
 // Data movement.  A tile is T consecutive blocks (T = 4096 / B); its records
 // are contiguous in every shard, T * (B + 8) bytes (a multiple of 16: T is
-// even).  A loader thread bulk-copies the tile's P record runs into one stage
-// of a shared-memory ring (as many stages of P runs as fit in kRingBytes) and
-// a group of 8 consumer warps decodes them from shared memory (three groups
-// take turns, so three tiles are decoded at once): B/16 consecutive threads of
-// a group share a block, each owns 16 elements.  Energy and maximum are reduced across
+// even).  The loader warp bulk-copies the tile's P record runs (lane p the
+// run of shard p) into one stage of a shared-memory ring (as many stages of
+// P runs as fit in kRingBytes) and a group of 8 consumer warps decodes them
+// from shared memory (three groups take turns, so three tiles are decoded at
+// once): B/16 consecutive threads of a group share a block, each owns 16
+// elements.  Energy and maximum are reduced across
 // the block's threads with xor-shuffles (every thread ends with the same bits),
 // and every thread stores its 16 codes directly (8-byte stores).
 //
@@ -169,42 +170,52 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     cta_barrier();
 
     if (warp == kGroups * kConsumers / 32) {
-        // ---- loader --------------------------------------------------------
-        if (lane == 0) {
-            auto issue_tile = [&](int i, int64_t t) {
-                const int s = i % nst;
-                const int nvalid = tile_valid(t);
-                const uint32_t run = static_cast<uint32_t>(nvalid & ~1) * kRec;   // multiple of 16
+        // ---- loader: lane 0 runs the tile scheduler and the stage barriers,
+        // lane p issues the bulk copy of shard p (the copies of a tile go out
+        // at once instead of one after another from one thread).
+        auto issue_tile = [&](int i, int64_t t) {   // whole warp
+            const int s = i % nst;
+            const int nvalid = tile_valid(t);
+            const uint32_t run = static_cast<uint32_t>(nvalid & ~1) * kRec;   // multiple of 16
+            if (lane == 0)
                 mbar_arrive_expect_tx(full_bar(s), run * static_cast<uint32_t>(P));
-                if (run > 0) {
-                    const uint32_t dst = sbase + Lay::kOffRing + s * stage_bytes;
-                    for (int p = 0; p < P; p++)
-                        bulk_load(dst + p * Lay::kRunBytes, shard_ptr[p] + t * T * kRec, run, full_bar(s));
-                }
-            };
+            __syncwarp();
+            if (run > 0 && lane < P)
+                bulk_load(sbase + Lay::kOffRing + s * stage_bytes + lane * Lay::kRunBytes,
+                          shard_ptr[lane] + t * T * kRec, run, full_bar(s));
+        };
+        int requested = kSchedAhead;    // requests 1 .. requested issued (lane 0)
+        if (lane == 0) {
             for (int j = 1; j <= kSchedAhead; j++)
                 sched.request(j);
             sched.publish(0, blockIdx.x);
-            issue_tile(0, blockIdx.x);
-            int i = 1;                       // items 0 .. i-1 have been loaded
-            int requested = kSchedAhead;     // requests 1 .. requested issued
-            for (;; i++) {
-                const int64_t t = sched.response(i);
-                if (t < 0) {
-                    sched.publish_end(i, kGroups);
-                    break;
+        }
+        issue_tile(0, blockIdx.x);
+        int i = 1;                       // items 0 .. i-1 have been loaded
+        for (;; i++) {
+            int64_t t = -1;
+            if (lane == 0) {
+                t = sched.response(i);
+                if (t >= 0) {
+                    sched.request(++requested);  // no failure seen yet: keep kSchedAhead in flight
+                    const int s = i % nst;
+                    if (i >= nst &&
+                        !mbar_wait_bounded_thread(empty_bar(s), ((i / nst) - 1) & 1, fault, kFaultReduce))
+                        t = -1;
                 }
-                sched.request(++requested);  // no failure seen yet: keep kSchedAhead in flight
-                const int s = i % nst;
-                if (i >= nst && !mbar_wait_bounded_thread(empty_bar(s), ((i / nst) - 1) & 1, fault, kFaultReduce)) {
+                if (t < 0)
                     sched.publish_end(i, kGroups);
-                    break;
-                }
-                sched.publish(i, t);
-                issue_tile(i, t);
+                else
+                    sched.publish(i, t);
             }
-            // Responses still in flight and copies this thread issued must
-            // land before the CTA can exit.
+            t = __shfl_sync(kFullMask, t, 0);
+            if (t < 0)
+                break;
+            issue_tile(i, t);
+        }
+        // Responses still in flight and the tile copies must land before the
+        // CTA can exit.
+        if (lane == 0) {
             sched.drain(i, requested);
             for (int j = i - nst > 0 ? i - nst : 0; j < i; j++)
                 mbar_wait_bounded_thread(full_bar(j % nst), (j / nst) & 1, fault, kFaultReduce);
