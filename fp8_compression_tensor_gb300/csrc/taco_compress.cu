@@ -190,6 +190,15 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     if (threadIdx.x == 0) {
         for (int j = 1; j <= kSchedAhead; j++)
             sched.request(j);
+        // While the previous kernel drains: its own tile and, as a guess at
+        // the tiles of the next rounds, those one and more SM counts further on.
+        for (int k = 0; k < kL2PrefetchCompress; k++) {
+            const uint32_t t = blockIdx.x + k * num_sms();
+            if (t < gridDim.x)
+#pragma unroll
+                for (int c = 0; c < Lay::kChunks; c++)
+                    tma_prefetch_2d(&tmap_x, 64 * c, static_cast<int32_t>(t * kTcRows));
+        }
         grid_dependency_wait();   // the input may come from the previous kernel
         sched.publish(0, blockIdx.x);
         issue_tile(0, blockIdx.x);

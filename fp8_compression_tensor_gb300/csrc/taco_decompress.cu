@@ -240,6 +240,18 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
     if (threadIdx.x == 0) {
         for (int j = 1; j <= kSchedAhead; j++)
             sched.request(j);
+        // While the previous kernel drains: the records of its own tile and,
+        // as a guess at the next rounds' tiles, one and more SM counts further on.
+        for (int k = 0; k < kL2PrefetchDecompress; k++) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(k) * num_sms();
+            if (t < gridDim.x) {
+                const int64_t blk0 = t * Lay::kTileBlocks;
+                const int64_t nv = nblocks - blk0 < Lay::kTileBlocks ? nblocks - blk0 : Lay::kTileBlocks;
+                const uint32_t bytes = static_cast<uint32_t>(nv & ~1) * Lay::kRec;   // multiple of 16
+                if (bytes > 0)
+                    bulk_prefetch_l2(packed + blk0 * Lay::kRec, bytes);
+            }
+        }
         grid_dependency_wait();   // the input may come from the previous kernel
         sched.publish(0, blockIdx.x);
         issue_tile(0, blockIdx.x);

@@ -117,6 +117,24 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Hint: fetch [src, src + bytes) from HBM into L2 (size a multiple of 16,
+// src 16-byte aligned).  Nothing reaches the SM and L2 is the device's point
+// of coherence for global memory, so a prefetch can never make a later load
+// return stale data: a kernel may issue it before grid_dependency_wait() to
+// overlap the first DRAM round trip with the previous kernel's tail.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Number of SMs of the device (an upper bound on the SM ids).
+__device__ __forceinline__ uint32_t num_sms()
+{
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%nsmid;" : "=r"(n));
+    return n;
+}
+
 // Bulk copy shared -> global, tracked by this thread's bulk async-groups.
 __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
 {

@@ -166,6 +166,18 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     }
     if (threadIdx.x < kMaxShards)
         shard_ptr[threadIdx.x] = args.shards[threadIdx.x];
+    if (warp == kGroups * kConsumers / 32 && lane < P) {
+        // While the previous kernel drains: this CTA's tile of shard `lane`
+        // and, as a guess at the next rounds' tiles, one and more SM counts on.
+        for (int k = 0; k < kL2PrefetchReduce; k++) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(k) * num_sms();
+            if (t < gridDim.x) {
+                const uint32_t run = static_cast<uint32_t>(tile_valid(t) & ~1) * kRec;   // multiple of 16
+                if (run > 0)
+                    bulk_prefetch_l2(args.shards[lane] + t * T * kRec, run);
+            }
+        }
+    }
     grid_dependency_wait();   // the shards may come from the previous kernel
     cta_barrier();
 

@@ -35,6 +35,21 @@ constexpr int kSchedSlots = 16;   // cancel-response slots
 // launch at 33.5 M elements).
 constexpr int kSchedAhead = TACO_SCHED_AHEAD;
 constexpr int kTileRing = 16;     // published-tile slots
+#ifndef TACO_L2_PREFETCH_COMPRESS
+#define TACO_L2_PREFETCH_COMPRESS 3
+#endif
+#ifndef TACO_L2_PREFETCH_DECOMPRESS
+#define TACO_L2_PREFETCH_DECOMPRESS 2
+#endif
+#ifndef TACO_L2_PREFETCH_REDUCE
+#define TACO_L2_PREFETCH_REDUCE 2
+#endif
+// Tiles whose input a CTA prefetches into L2 before its dependency wait, per
+// kernel: its own, then (a guess at what it or its neighbours take next) those
+// one, two, ... SM counts further on.
+constexpr int kL2PrefetchCompress = TACO_L2_PREFETCH_COMPRESS;
+constexpr int kL2PrefetchDecompress = TACO_L2_PREFETCH_DECOMPRESS;
+constexpr int kL2PrefetchReduce = TACO_L2_PREFETCH_REDUCE;
 
 // Shared-memory bytes: responses (16 B each, 16-byte aligned first), tiles
 // (8 B each) and the two sets of mbarriers.

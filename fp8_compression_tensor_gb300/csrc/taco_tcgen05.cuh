@@ -242,6 +242,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// Hint: fetch the box at (x, y) from HBM into L2 (same coordinate rules as
+// tma_load_2d; see bulk_prefetch_l2 for why it may precede the dependency wait).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled bulk tensor store of a shared-memory box to (x, y); elements
 // outside the tensor are not written.  Tracked by bulk async-groups.
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t x, int32_t y, uint32_t src)
