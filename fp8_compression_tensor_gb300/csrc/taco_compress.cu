@@ -107,12 +107,17 @@ struct TcCompressLayout {
 // Writes H_B (+-1 in bf16, Sylvester order; the identity when `rotate` is
 // false) into shared memory as the K-major B operand in the 128-byte swizzled
 // layout: chunk c holds columns [64c, 64c+64); row n of a chunk is 128 bytes
-// whose 16-byte unit u sits at unit u ^ (n % 8).
+// whose 16-byte unit u sits at unit u ^ (n % 8).  Written by the threads of
+// warps 1 and up, before their dependency wait: warp 0's thread 0 issues the
+// first loads right after that wait and would otherwise hold the CTA's set-up
+// barrier for its share (about 0.5 us for one thread alone).
 template <int B>
 __device__ void write_hadamard_sw128(uint8_t *h, bool rotate)
 {
     constexpr int kUnits = B * (B / 8);    // 16-byte units of H
-    for (int idx = threadIdx.x; idx < kUnits; idx += blockDim.x) {
+    if (threadIdx.x < 32)
+        return;
+    for (int idx = threadIdx.x - 32; idx < kUnits; idx += blockDim.x - 32) {
         const int n = idx / (B / 8);
         const int u_all = idx % (B / 8);   // unit index along K over the whole row
         const int c = u_all / 8, u = u_all % 8;

@@ -112,12 +112,17 @@ struct TcDecompressLayout {
 
 // The MMA's B operand, K-major, 128-byte swizzle, in E4M3 (+1 = 0x38,
 // -1 = 0xB8) or E5M2 (+1 = 0x3C, -1 = 0xBC): H_128 for B = 128 / 256,
-// diag(H_64, H_64) for B = 64, the identity when `rotate` is false.
+// diag(H_64, H_64) for B = 64, the identity when `rotate` is false.  Written
+// by the threads of warps 1 and up, before their dependency wait: warp 0's
+// thread 0 issues the first loads right after that wait and would otherwise
+// hold the CTA's set-up barrier for its share.
 template <int B>
 __device__ void write_hadamard_f8_sw128(uint8_t *h, bool e5m2, bool rotate)
 {
     const uint32_t plus = e5m2 ? 0x3Cu : 0x38u, minus = e5m2 ? 0xBCu : 0xB8u;
-    for (int idx = threadIdx.x; idx < 128 * 8; idx += blockDim.x) {
+    if (threadIdx.x < 32)
+        return;
+    for (int idx = threadIdx.x - 32; idx < 128 * 8; idx += blockDim.x - 32) {
         const int n = idx / 8, u = idx % 8;
         uint32_t w[4];
 #pragma unroll
@@ -142,11 +147,13 @@ __device__ void write_hadamard_f8_sw128(uint8_t *h, bool e5m2, bool rotate)
 }
 
 // The same in f16 (+1 = 0x3C00, -1 = 0xBC00): two 128-byte K chunks of 64
-// columns each.
+// columns each, written by the same threads.
 template <int B>
 __device__ void write_hadamard_f16_sw128(uint8_t *h, bool rotate)
 {
-    for (int idx = threadIdx.x; idx < 128 * 16; idx += blockDim.x) {
+    if (threadIdx.x < 32)
+        return;
+    for (int idx = threadIdx.x - 32; idx < 128 * 16; idx += blockDim.x - 32) {
         const int n = idx / 16, ua = idx % 16;   // row, 16-byte unit along K (8 columns)
         const int c = ua / 8, u = ua % 8;
         uint32_t w[4];
