@@ -49,12 +49,19 @@ namespace {
 #ifndef TACO_REDUCE_GROUPS
 #define TACO_REDUCE_GROUPS 3
 #endif
-constexpr int kConsumers = 256;                 // threads of a consumer group: 8 warps, 16 elements each
+#ifndef TACO_REDUCE_CONSUMERS
+#define TACO_REDUCE_CONSUMERS 256
+#endif
+constexpr int kConsumers = TACO_REDUCE_CONSUMERS;   // threads of a consumer group, 16 elements each
 constexpr int kGroups = TACO_REDUCE_GROUPS;     // consumer groups; group g takes items i % kGroups == g
 constexpr int kRThreads = kGroups * kConsumers + 32;   // + the loader warp
 constexpr int kLaneCodes = 16;                  // codes (elements) per thread per shard
 constexpr int kRingBytes = TACO_REDUCE_RING_KB * 1024;
 constexpr int kMaxStages = 8;
+#ifndef TACO_REDUCE_SCHED_AHEAD
+#define TACO_REDUCE_SCHED_AHEAD TACO_SCHED_AHEAD
+#endif
+constexpr int kRSchedAhead = TACO_REDUCE_SCHED_AHEAD;   // cancel requests in flight
 // The loader publishes item i after the empty barrier of item i - nst, when
 // the consumers have read every item up to i - nst: a published-tile slot
 // (and the end marks of kGroups items) is reused only after its readers are done.
@@ -196,9 +203,9 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                 bulk_load(sbase + Lay::kOffRing + s * stage_bytes + lane * Lay::kRunBytes,
                           shard_ptr[lane] + t * T * kRec, run, full_bar(s));
         };
-        int requested = kSchedAhead;    // requests 1 .. requested issued (lane 0)
+        int requested = kRSchedAhead;   // requests 1 .. requested issued (lane 0)
         if (lane == 0) {
-            for (int j = 1; j <= kSchedAhead; j++)
+            for (int j = 1; j <= kRSchedAhead; j++)
                 sched.request(j);
             sched.publish(0, blockIdx.x);
         }
@@ -209,7 +216,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             if (lane == 0) {
                 t = sched.response(i);
                 if (t >= 0) {
-                    sched.request(++requested);  // no failure seen yet: keep kSchedAhead in flight
+                    sched.request(++requested);  // no failure seen yet: keep kRSchedAhead in flight
                     const int s = i % nst;
                     if (i >= nst &&
                         !mbar_wait_bounded_thread(empty_bar(s), ((i / nst) - 1) & 1, fault, kFaultReduce))
