@@ -86,14 +86,39 @@ def parse_args():
 # Helpers
 # ---------------------------------------------------------------------------
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and blank space, so that editing a
+    comment does not invalidate DRAM counters taken on the same code."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c == '"':                        # string literal (PTX text): kept verbatim
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash(rel: str) -> str:
+    """Hash of a kernel's code (its .cu file and the shared headers), comments excluded."""
     h = hashlib.sha256()
     for p in (rel, "fp8_compression_tensor_gb300/csrc/taco_device.cuh",
               "fp8_compression_tensor_gb300/csrc/taco_tcgen05.cuh",
               "fp8_compression_tensor_gb300/csrc/taco_sched.cuh",
               "fp8_compression_tensor_gb300/csrc/taco_kernels.h"):
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,5 +1,5 @@
-// taco_compress.cu -- TACO's fused sender-side kernel (Algorithm 1, lines
-// 4-16; Eqs. 5-10) with the Hadamard rotation on the 5th-generation tensor
+// taco_compress.cu -- TACO's fused sender-side kernel (Algorithm 1, its
+// compression loop; Eqs. 5-10) with the Hadamard rotation on the 5th-generation tensor
 // cores (tcgen05), for GB300 (sm_103a).
 //
 // The rotation of a whole tile of blocks is a dense product: with the tile's

@@ -1,5 +1,5 @@
-// taco_decompress.cu -- TACO's fused receiver-side kernel (Algorithm 1,
-// lines 19-24; Eqs. 11-13; the paper's fused_ash_decompress_kernel) with the
+// taco_decompress.cu -- TACO's fused receiver-side kernel (Algorithm 1, its
+// decompression loop; Eqs. 11-13; the paper's fused_ash_decompress_kernel) with the
 // inverse rotation on the tensor cores (tcgen05), for GB300 (sm_103a).
 //
 // For a tile of blocks, the E4M3 codes of each block form one row of A and

@@ -104,7 +104,7 @@ typedef struct taco_options {
 TACO_API int64_t taco_compressed_bytes(int64_t rows, int64_t hidden, int block);
 
 /*
- * Sender side, Algorithm 1 lines 4-16 (Eqs. 5-10), one fused kernel: for every
+ * Sender side, Algorithm 1's compression loop (Eqs. 5-10), one fused kernel: for every
  * block G_k of x, sigma_k = sqrt(mean(G_k^2) + eps) (Eq. 6), alpha_k = tau/sigma_k
  * (Eq. 7), Z_k = (1/sqrt B) H_B (alpha_k G_k) (Eq. 8), s_k = max|Z_k| / Q_max
  * (Eq. 9), q_k = Cvt_FP8(Z_k / s_k) (Eq. 10); writes the record (q_k, alpha_k, s_k).
@@ -117,7 +117,7 @@ TACO_API taco_status_t taco_compress(const void *x_bf16, int64_t rows, int64_t h
                             void *packed_out, taco_stream_t stream);
 
 /*
- * Receiver side, Algorithm 1 lines 19-24 (Eqs. 11-13), the fused decompress
+ * Receiver side, Algorithm 1's decompression loop (Eqs. 11-13), the fused decompress
  * kernel (Section 4.1, "fused_ash_decompress_kernel"): Zhat_k = Cvt_FP32(q_k) s_k,
  * Ghat_k = (1/sqrt B) H_B Zhat_k, G'_k = Ghat_k / alpha_k, rounded to bf16
  * (nearest even).

@@ -318,7 +318,7 @@ static int block_ok(int B)
 }
 
 /* ------------------------------------------------------------------ */
-/* Sender: Algorithm 1, lines 4-16                                     */
+/* Sender: Algorithm 1 (its compression loop), Eqs. (5)-(10)          */
 /* ------------------------------------------------------------------ */
 
 static void compress_block(const float *G, int B, int variant, int code, uint8_t *rec)
@@ -376,7 +376,7 @@ static void compress_block(const float *G, int B, int variant, int code, uint8_t
 }
 
 /* ------------------------------------------------------------------ */
-/* Receiver: Algorithm 1, lines 19-24; Eqs. (11)-(13)                  */
+/* Receiver: Algorithm 1 (its decompression loop), Eqs. (11)-(13)     */
 /* ------------------------------------------------------------------ */
 
 static void decompress_block(const uint8_t *rec, int B, int variant, int code, float *out)

@@ -1,7 +1,7 @@
 """Parity helpers shared by the GPU tests, the smoke check and the benchmark:
 compare packed records and reconstructions against the CPU oracle.
 
-The tolerances are the ones the compression operator is judged by:
+The tolerances are the ones the compression operator is held to:
   - alpha_k and s_k agree to 1e-6 relative (s_k = 0 blocks exactly);
   - E4M3 codes are identical except in at most 1e-4 of the elements, and
     those differ by exactly one E4M3 step (+0 / -0 count as equal values and
