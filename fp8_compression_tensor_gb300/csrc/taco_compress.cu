@@ -481,7 +481,7 @@ struct TcCompressConfig {
 #define TACO_TC64_CFG 641
 #endif
 #ifndef TACO_TC128_CFG
-#define TACO_TC128_CFG 331
+#define TACO_TC128_CFG 431
 #endif
 #ifndef TACO_TC256_CFG
 #define TACO_TC256_CFG 331

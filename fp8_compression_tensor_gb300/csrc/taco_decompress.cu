@@ -558,7 +558,7 @@ struct TcDecompressConfig {
 #define TACO_DTC64_CFG 322
 #endif
 #ifndef TACO_DTC128_CFG
-#define TACO_DTC128_CFG 322
+#define TACO_DTC128_CFG 622
 #endif
 #ifndef TACO_DTC256_CFG
 #define TACO_DTC256_CFG 323
