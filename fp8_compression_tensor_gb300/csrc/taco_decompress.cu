@@ -590,9 +590,14 @@ using DecompressTc256 =
     TcDecompressConfig<256, TACO_DTC256_CFG / 100, TACO_DTC256_CFG / 10 % 10, TACO_DTC256_CFG % 10, 0, TACO_DEPG256>;
 using DecompressTc512 =
     TcDecompressConfig<512, TACO_DTC512_CFG / 100, TACO_DTC512_CFG / 10 % 10, TACO_DTC512_CFG % 10, 0, TACO_DEPG512>;
-// INT8 codes (f16 operands: A stages and H twice as large).
+// INT8 codes (f16 operands: A stages and H twice as large).  B = 128, four
+// digits: raw stages, A stages, output tiles, epilogue groups.
+#ifndef TACO_DI8_128_CFG
+#define TACO_DI8_128_CFG 3222
+#endif
 using DecompressI8x64 = TcDecompressConfig<64, 3, 2, 2, 1>;
-using DecompressI8x128 = TcDecompressConfig<128, 3, 2, 2, 1>;
+using DecompressI8x128 = TcDecompressConfig<128, TACO_DI8_128_CFG / 1000, TACO_DI8_128_CFG / 100 % 10,
+                                            TACO_DI8_128_CFG / 10 % 10, 1, TACO_DI8_128_CFG % 10>;
 using DecompressI8x256 = TcDecompressConfig<256, 3, 2, 2, 1>;
 using DecompressI8x512 = TcDecompressConfig<512, 3, 2, 2, 1>;
 
