@@ -303,10 +303,9 @@ __device__ __forceinline__ uint32_t encode4(int code, float a, float b, float c,
 
 // Cvt_FP32 (Eq. 11) of the two E4M3 codes in the low 16 bits of `pair`
 // (exact): low byte -> .x, high byte -> .y.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair)
+// The two f16 values of a word as floats (exact), low half first.
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h2)
 {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
     float lo, hi;
     asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
         : "=f"(lo), "=f"(hi)
@@ -314,16 +313,18 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair)
     return make_float2(lo, hi);
 }
 
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
+    return f16x2_to_float2(h2);
+}
+
 // The two E5M2 codes in the low 16 bits of `pair` as floats (exact).
 __device__ __forceinline__ float2 e5m2x2_to_float2(uint32_t pair)
 {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(pair)));
-    float lo, hi;
-    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h2));
-    return make_float2(lo, hi);
+    // An E5M2 code is the high byte of the f16 of the same value.
+    return f16x2_to_float2(__byte_perm(pair, 0u, 0x1404));
 }
 
 // Two floats -> two bf16 (round to nearest even) packed in a word, lo first.

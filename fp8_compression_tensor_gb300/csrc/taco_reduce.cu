@@ -93,8 +93,10 @@ __device__ __forceinline__ void decode4(uint32_t x, float2 &q0, float2 &q1)
         q0 = e4m3x2_to_float2(x & 0xffffu);
         q1 = e4m3x2_to_float2(x >> 16);
     } else if constexpr (CODE == 1) {
-        q0 = e5m2x2_to_float2(x & 0xffffu);
-        q1 = e5m2x2_to_float2(x >> 16);
+        // An E5M2 code is the high byte of the f16 of the same value
+        // (subnormals and signs included): byte permutes build both f16 pairs.
+        q0 = f16x2_to_float2(__byte_perm(x, 0u, 0x1404));
+        q1 = f16x2_to_float2(__byte_perm(x, 0u, 0x3424));
     } else {
         int8x4_to_float(x, q0, q1);
     }
@@ -365,12 +367,19 @@ KernelInfo info_for_block(int block)
 
 KernelInfo reduce_kernel_info(int block, int code, int num_shards)
 {
-    // The method's own case (E4M3, 8 shards) has kernels with the shard loop unrolled.
-    if (TACO_REDUCE_FIXED_P8 && code == 0 && num_shards == 8) {
-        switch (block) {
+    // The method's shard count (8) has kernels with the shard loop unrolled,
+    // for every code format and the blocks of the paper's main configurations.
+    if (TACO_REDUCE_FIXED_P8 && num_shards == 8) {
+        switch (code * 1000 + block) {
         case 64: return info<64, 0, 8>();
         case 128: return info<128, 0, 8>();
         case 256: return info<256, 0, 8>();
+        case 1064: return info<64, 1, 8>();
+        case 1128: return info<128, 1, 8>();
+        case 1256: return info<256, 1, 8>();
+        case 2064: return info<64, 2, 8>();
+        case 2128: return info<128, 2, 8>();
+        case 2256: return info<256, 2, 8>();
         default: break;
         }
     }

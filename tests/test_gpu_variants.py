@@ -96,6 +96,25 @@ def test_reduce(taco, B, variant, code):
 
 
 @pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("variant", [0, 1, 3])
+@pytest.mark.parametrize("B", [64, 128, 256])
+def test_reduce_eight_shards(taco, B, variant, code):
+    # Eight shards run the kernels with the shard loop unrolled; odd block
+    # counts at B = 256 leave a record outside the tile copies.
+    rows, hidden, P = 97, 1280, 8
+    shards = [oracle.compress(workloads.generate("student_t_channels", rows, hidden, 40 + p), B, variant, code)
+              for p in range(P)]
+    n = rows * hidden
+    ref = oracle.reduce_shards(shards, n, B, variant, code)
+    got = taco.reduce_shards([torch.from_numpy(s).cuda() for s in shards], rows, hidden, B,
+                             variant=variant, code=code).cpu().numpy()
+    u = reduce_exact_u(shards, B, variant, code)
+    ties = near_midpoint(u, code=code) | noise_zone(u, B)
+    compare_records(got, ref, B, ambiguous=ties, code=code)
+    assert taco.device_status() == 0
+
+
+@pytest.mark.parametrize("code", CODES)
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_special_blocks(taco, variant, code):
     """All-zero, single-spike and constant blocks, and a shard with its
