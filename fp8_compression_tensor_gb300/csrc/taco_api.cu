@@ -90,7 +90,7 @@ void init_device(DeviceState &st)
         }
         for (int code = 0; code < 3 && e == cudaSuccess; code++)
             e = init_kernel(reduce_kernel_info(blocks[i], code, 1), &st.ctas_per_sm);
-        for (int code = 0; code < 3 && e == cudaSuccess && tensor_core_block(blocks[i]); code++)
+        for (int code = 0; code < 3 && e == cudaSuccess; code++)
             e = init_kernel(reduce_kernel_info(blocks[i], code, 8), &st.ctas_per_sm);
     }
     st.init_error = e;

@@ -350,15 +350,15 @@ KernelInfo info()
                       kRThreads, ReduceLayout<B>::kT, kRThreads / 32};
 }
 
-template <int CODE>
+template <int CODE, int PFIX = 0>
 KernelInfo info_for_block(int block)
 {
     switch (block) {
-    case 32: return info<32, CODE>();
-    case 64: return info<64, CODE>();
-    case 128: return info<128, CODE>();
-    case 256: return info<256, CODE>();
-    case 512: return info<512, CODE>();
+    case 32: return info<32, CODE, PFIX>();
+    case 64: return info<64, CODE, PFIX>();
+    case 128: return info<128, CODE, PFIX>();
+    case 256: return info<256, CODE, PFIX>();
+    case 512: return info<512, CODE, PFIX>();
     default: return KernelInfo{};
     }
 }
@@ -368,19 +368,13 @@ KernelInfo info_for_block(int block)
 KernelInfo reduce_kernel_info(int block, int code, int num_shards)
 {
     // The method's shard count (8) has kernels with the shard loop unrolled,
-    // for every code format and the blocks of the paper's main configurations.
+    // for every code format and block size.
     if (TACO_REDUCE_FIXED_P8 && num_shards == 8) {
-        switch (code * 1000 + block) {
-        case 64: return info<64, 0, 8>();
-        case 128: return info<128, 0, 8>();
-        case 256: return info<256, 0, 8>();
-        case 1064: return info<64, 1, 8>();
-        case 1128: return info<128, 1, 8>();
-        case 1256: return info<256, 1, 8>();
-        case 2064: return info<64, 2, 8>();
-        case 2128: return info<128, 2, 8>();
-        case 2256: return info<256, 2, 8>();
-        default: break;
+        switch (code) {
+        case 0: return info_for_block<0, 8>(block);
+        case 1: return info_for_block<1, 8>(block);
+        case 2: return info_for_block<2, 8>(block);
+        default: return KernelInfo{};
         }
     }
     switch (code) {

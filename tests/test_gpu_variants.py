@@ -97,11 +97,11 @@ def test_reduce(taco, B, variant, code):
 
 @pytest.mark.parametrize("code", CODES)
 @pytest.mark.parametrize("variant", [0, 1, 3])
-@pytest.mark.parametrize("B", [64, 128, 256])
+@pytest.mark.parametrize("B", BLOCKS)
 def test_reduce_eight_shards(taco, B, variant, code):
     # Eight shards run the kernels with the shard loop unrolled; odd block
-    # counts at B = 256 leave a record outside the tile copies.
-    rows, hidden, P = 97, 1280, 8
+    # counts (B = 512) leave a record outside the tile copies.
+    rows, hidden, P = 97, 1536, 8
     shards = [oracle.compress(workloads.generate("student_t_channels", rows, hidden, 40 + p), B, variant, code)
               for p in range(P)]
     n = rows * hidden
