@@ -176,6 +176,13 @@ taco_status_t check_shape(int64_t rows, int64_t hidden, int block, int64_t *n, i
     return TACO_OK;
 }
 
+// The tensor-core kernels address a tensor as rows of view_row_elems(block)
+// elements with 32-bit TMA coordinates: at most INT32_MAX such rows.
+taco_status_t check_view_rows(int64_t n, int block)
+{
+    return tensor_core_block(block) && n / view_row_elems(block) > INT32_MAX ? TACO_ERR_BAD_SHAPE : TACO_OK;
+}
+
 taco_status_t check_options(const taco_options_t *opt, Scheme *scheme)
 {
     if (!opt)
@@ -192,6 +199,8 @@ taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, in
 {
     int64_t n = 0, bytes = 0;
     taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
+    if (st == TACO_OK)
+        st = check_view_rows(n, block);
     if (st != TACO_OK || n == 0)
         return st;
     if (!x_bf16 || !packed_out)
@@ -235,6 +244,8 @@ taco_status_t decompress_impl(const void *packed_in, int64_t rows, int64_t hidde
 {
     int64_t n = 0, bytes = 0;
     taco_status_t st = check_shape(rows, hidden, block, &n, &bytes);
+    if (st == TACO_OK)
+        st = check_view_rows(n, block);
     if (st != TACO_OK || n == 0)
         return st;
     if (!packed_in || !y_bf16_out)

@@ -63,7 +63,9 @@ typedef struct CUstream_st *taco_stream_t;
 typedef enum taco_status {
     TACO_OK = 0,
     TACO_ERR_NULL_POINTER = 1,      /* a required pointer is NULL */
-    TACO_ERR_BAD_SHAPE = 2,         /* rows < 0, hidden < 0, hidden % block != 0, or size overflow */
+    TACO_ERR_BAD_SHAPE = 2,         /* rows < 0, hidden < 0, hidden % block != 0, size overflow, or
+                                       (compress / decompress, blocks 64-512) more than 2^31 - 1 rows
+                                       of min(block, 128) elements */
     TACO_ERR_UNSUPPORTED_BLOCK = 3, /* block not in {32, 64, 128, 256, 512} */
     TACO_ERR_MISALIGNED = 4,        /* a device pointer is not 16-byte aligned */
     TACO_ERR_BAD_SHARDS = 5,        /* num_shards < 1 or > TACO_MAX_SHARDS */

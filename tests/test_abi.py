@@ -53,6 +53,14 @@ def test_host_side_queries(lib):
     assert lib.taco_compress(None, 4, 128, 128, None, None) == 1
     assert lib.taco_compress(16, 4, 128, 128, 2, None) == 4
     assert lib.taco_compress(0, 0, 128, 128, 0, None) == 0
+    # Blocks 64-512 address the tensor with 32-bit row coordinates (rows of
+    # min(B, 128) elements); block 32 has no such limit.
+    for fn in (lib.taco_compress, lib.taco_decompress):
+        assert fn(None, 1 << 31, 64, 64, None, None) == 2
+        assert fn(None, (1 << 31) - 1, 64, 64, None, None) == 1
+        assert fn(None, 1 << 30, 512, 256, None, None) == 2
+        assert fn(None, (1 << 30) - 1, 256, 256, None, None) == 1
+        assert fn(None, 1 << 31, 64, 32, None, None) == 1
     ptrs = (ctypes.c_void_p * 1)(16)
     assert lib.taco_reduce_shards(ptrs, 0, 4, 128, 128, 32, None) == 5
     assert lib.taco_reduce_shards(ptrs, 17, 4, 128, 128, 32, None) == 5
