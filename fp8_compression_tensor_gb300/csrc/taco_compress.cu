@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
         }
         for (int b = 0; b < NOUT; b++) {
             mbar_init(out_free_bar(b), 1);
-            mbar_init(rec_done_bar(b), kEpiThreads);
+            mbar_init(rec_done_bar(b), kEpiThreads / 32);
         }
         sched.init();
         fence_mbar_init();
@@ -427,7 +427,9 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             if (part == 0)
                 sts64(rec_block + B, __float_as_uint(alpha), __float_as_uint(s));
             fence_proxy_async_smem();
-            mbar_arrive(rec_done_bar(ob));
+            __syncwarp();                               // one arrival per warp covers its lanes' writes
+            if (lane == 0)
+                mbar_arrive(rec_done_bar(ob));
 
             // The group's first warp (lane 0) stores the tile's records once all are written.
             constexpr int TB = Lay::kTileBlocks;

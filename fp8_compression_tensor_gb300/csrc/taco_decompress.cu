@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
         }
         for (int b = 0; b < NOUT; b++) {
             mbar_init(out_free(b), 1);
-            mbar_init(out_done(b), kGroup);
+            mbar_init(out_done(b), kGroup / 32);
         }
         for (int f = 0; f < FS; f++)
             mbar_init(fac_full(f), kGroup / 32);
@@ -370,6 +370,12 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                 constexpr int PC = Lay::kPartCodes;
                 const int bl = (m * Lay::kBlocksPerRow + b) / Lay::kRowsPerBlock;   // block within the tile
                 const int part = m % Lay::kRowsPerBlock;                             // B = 256 / 512: part
+                // B = 512: the four parts of a record lie 128 bytes apart, on
+                // the same banks, so part p reads its 8-byte pieces starting at
+                // piece 4p (register pair q holds piece (q + 4p) mod 16) and
+                // stores unit u at (u + 2p) mod 8: two wavefronts per read.
+                constexpr bool kRot = Lay::kRowsPerBlock == 4;
+                const int rot = kRot ? part : 0;
                 uint32_t w[PC / 4];
                 float f = 0.f;
                 if (bl < nvalid) {
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                     const uint32_t rs = raw + bl * Lay::kRec;
 #pragma unroll
                     for (int q = 0; q < PC / 8; q++) {
-                        const int o = part * PC + 8 * q;
+                        const int o = part * PC + 8 * ((q + 4 * rot) % (PC / 8));
                         const uint2 v = from_global ? *reinterpret_cast<const uint2 *>(rg + o) : lds64(rs + o);
                         w[2 * q] = v.x;
                         w[2 * q + 1] = v.y;
@@ -395,8 +401,9 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                 // Codes to the swizzled A row: 16 codes per 16-byte unit (8 in f16).
 #pragma unroll
                 for (int u = 0; u < PC / 16; u++) {
+                    const int ur = (u + 2 * rot) % (PC / 16);     // the unit register group u holds
                     if constexpr (!A16) {
-                        const int ua = b * (PC / 16) + u;         // unit index along the A row
+                        const int ua = b * (PC / 16) + ur;        // unit index along the A row
                         const int chunk = ua / 8, uc = ua % 8;
                         sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
                                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]));
@@ -411,7 +418,7 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                         }
 #pragma unroll
                         for (int hh = 0; hh < 2; hh++) {
-                            const int ua = 2 * (b * (PC / 16) + u) + hh;
+                            const int ua = 2 * (b * (PC / 16) + ur) + hh;
                             const int chunk = ua / 8, uc = ua % 8;
                             sts128(a_row + chunk * Lay::kAChunkBytes + ((uc ^ (m & 7)) * 16),
                                    make_uint4(hv[4 * hh], hv[4 * hh + 1], hv[4 * hh + 2], hv[4 * hh + 3]));
@@ -514,7 +521,9 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
             if (lane == 0)
                 mbar_arrive(acc_empty(acc));
             fence_proxy_async_smem();
-            mbar_arrive(out_done(ob));
+            __syncwarp();                               // one arrival per warp covers its lanes' writes
+            if (lane == 0)
+                mbar_arrive(out_done(ob));
             if (warp == 6 + 4 * grp) {   // the group's first warp stores the tile
                 if (!mbar_wait_bounded(out_done(ob), (kt / NBG) & 1, fault, kFaultDecompress))
                     break;
