@@ -17,7 +17,8 @@
 // P runs as fit in kRingBytes) and a group of 8 consumer warps decodes them
 // from shared memory (three groups take turns, so three tiles are decoded at
 // once): B/16 consecutive threads of a group share a block, each owns 16
-// elements.  Energy and maximum are reduced across
+// elements (TACO_REDUCE_LANE_CODES = 8 halves that where a block still fits a
+// warp; measured slower).  Energy and maximum are reduced across
 // the block's threads with xor-shuffles (every thread ends with the same bits),
 // and every thread stores its 16 codes directly (8-byte stores).
 //
@@ -55,7 +56,11 @@ namespace {
 constexpr int kConsumers = TACO_REDUCE_CONSUMERS;   // threads of a consumer group, 16 elements each
 constexpr int kGroups = TACO_REDUCE_GROUPS;     // consumer groups; group g takes items i % kGroups == g
 constexpr int kRThreads = kGroups * kConsumers + 32;   // + the loader warp
-constexpr int kLaneCodes = 16;                  // codes (elements) per thread per shard
+#ifndef TACO_REDUCE_LANE_CODES
+#define TACO_REDUCE_LANE_CODES 16
+#endif
+constexpr int kLaneCodes = TACO_REDUCE_LANE_CODES;   // codes (elements) per thread per shard
+static_assert(kLaneCodes == 8 || kLaneCodes == 16, "8 or 16 codes per thread");
 constexpr int kRingBytes = TACO_REDUCE_RING_KB * 1024;
 constexpr int kMaxStages = 8;
 #ifndef TACO_REDUCE_SCHED_AHEAD
@@ -69,8 +74,22 @@ static_assert(kTileRing >= kMaxStages + kGroups, "published-tile slot reused too
 
 template <int B>
 struct ReduceLayout {
-    static constexpr int kT = kConsumers * kLaneCodes / B;   // blocks per tile
-    static constexpr int kLpb = B / kLaneCodes;             // threads per block
+    // Codes per thread: kLaneCodes, or 16 where a block would span more than a
+    // warp (its energy and maximum are reduced with shuffles inside one warp).
+    static constexpr int kLC = B / kLaneCodes > 32 ? 16 : kLaneCodes;
+    static constexpr int kLW = kLC / 4;                      // 32-bit words of a thread's codes
+    // Blocks per tile: one per kLpb consumer threads, halved until two stages of
+    // kMaxShards record runs fit the ring (the threads beyond it stay idle).
+    static constexpr int tile_blocks()
+    {
+        int t = kConsumers * kLC / B;
+        while (t > 2 && 2 * kMaxShards * t * (B + 8) > kRingBytes)
+            t /= 2;
+        return t;
+    }
+    static constexpr int kT = tile_blocks();
+    static constexpr int kLpb = B / kLC;                     // threads per block
+    static_assert(kLpb <= 32 && 32 % kLpb == 0, "a block's threads lie in one warp");
     static constexpr int kRec = B + 8;
     static constexpr int kRunBytes = kT * kRec;             // one shard's records of a tile
     static_assert(kT % 2 == 0 && kRunBytes % 16 == 0, "bulk copies need 16-byte multiples");
@@ -102,15 +121,14 @@ __device__ __forceinline__ void decode4(uint32_t x, float2 &q0, float2 &q1)
     }
 }
 
-// w[0..15] += q[0..15] * f for the 16 codes in `c`, each product rounded on its
-// own before the add (so that a shard and its negation cancel exactly, as in
-// an FP32 sum of decoded shards).
-template <int CODE>
-__device__ __forceinline__ void accumulate_shard(float (&w)[kLaneCodes], uint4 c, float f)
+// w[k] += q[k] * f for the thread's codes in `words`, each product rounded on
+// its own before the add (so that a shard and its negation cancel exactly, as
+// in an FP32 sum of decoded shards).
+template <int CODE, int LW>
+__device__ __forceinline__ void accumulate_shard(float (&w)[4 * LW], const uint32_t (&words)[LW], float f)
 {
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
+    for (int k = 0; k < LW; k++) {
         float2 q0, q1;
         decode4<CODE>(words[k], q0, q1);
         // Scalar products (never contracted), packed sums.
@@ -137,6 +155,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     using Lay = ReduceLayout<B>;
     constexpr int T = Lay::kT;
     constexpr int kRec = Lay::kRec;
+    constexpr int LC = Lay::kLC, LW = Lay::kLW;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *base = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
@@ -242,11 +261,11 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                 mbar_wait_bounded_thread(full_bar(j % nst), (j / nst) & 1, fault, kFaultReduce);
         }
     } else {
-        // ---- consumers: 16 elements of one block per thread -----------------
+        // ---- consumers: Lay::kLC elements of one block per thread ------------
         const int grp = threadIdx.x / kConsumers;
         const int c = threadIdx.x % kConsumers;
         const int bl = c / Lay::kLpb;        // block within the tile
-        const int part = c % Lay::kLpb;      // 16-element part of the block
+        const int part = c % Lay::kLpb;      // Lay::kLC-element part of the block
         for (int i = grp;; i += kGroups) {
             const int64_t t = sched.tile_warp(i);
             if (t < 0)
@@ -261,30 +280,40 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             const uint32_t rec_s = sbase + Lay::kOffRing + s * stage_bytes + bl * kRec;
 
             // W = sum_p q_p * (s_p / alpha_p) in shard order.
-            float w[kLaneCodes];
+            float w[LC];
 #pragma unroll
-            for (int k = 0; k < kLaneCodes; k++)
+            for (int k = 0; k < LC; k++)
                 w[k] = 0.f;
             // s_p / alpha_p below is within 2 ulp (alpha_p <= 1e15 is far from
             // the range where the fast quotient underflows).
             if (active && !from_global) {
-                const uint32_t r0 = rec_s + kLaneCodes * part;
+                const uint32_t r0 = rec_s + LC * part;
 #pragma unroll(PFIX > 0 ? PFIX : 1)
                 for (int p = 0; p < P; p++) {
                     const uint32_t r = r0 + p * Lay::kRunBytes;
-                    const uint2 a = lds64(r), b = lds64(r + 8);
-                    const uint2 meta = lds64(r - kLaneCodes * part + B);
-                    accumulate_shard<CODE>(w, make_uint4(a.x, a.y, b.x, b.y),
-                                     __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
+                    uint32_t words[LW];
+#pragma unroll
+                    for (int h = 0; h < LW / 2; h++) {
+                        const uint2 a = lds64(r + 8 * h);
+                        words[2 * h] = a.x;
+                        words[2 * h + 1] = a.y;
+                    }
+                    const uint2 meta = lds64(r - LC * part + B);
+                    accumulate_shard<CODE>(w, words, __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
                 }
             } else if (active) {
                 // The tile's odd last record is not in the bulk copies.
                 for (int p = 0; p < P; p++) {
                     const uint8_t *r = shard_ptr[p] + blk * kRec;
-                    const uint2 a = ldg_u2(r + kLaneCodes * part), b = ldg_u2(r + kLaneCodes * part + 8);
+                    uint32_t words[LW];
+#pragma unroll
+                    for (int h = 0; h < LW / 2; h++) {
+                        const uint2 a = ldg_u2(r + LC * part + 8 * h);
+                        words[2 * h] = a.x;
+                        words[2 * h + 1] = a.y;
+                    }
                     const uint2 meta = ldg_u2(r + B);
-                    accumulate_shard<CODE>(w, make_uint4(a.x, a.y, b.x, b.y),
-                                     __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
+                    accumulate_shard<CODE>(w, words, __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
                 }
             }
             // The stage is read: hand it back to the loader.
@@ -296,7 +325,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             float2 e2 = make_float2(0.f, 0.f);
             float wmax = 0.f;
 #pragma unroll
-            for (int k = 0; k < kLaneCodes; k += 2) {
+            for (int k = 0; k < LC; k += 2) {
                 const float2 wi = make_float2(w[k], w[k + 1]);
                 e2 = fma2(wi, wi, e2);
                 wmax = max3(wmax, fabsf(w[k]), fabsf(w[k + 1]));
@@ -319,23 +348,25 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                 sc = __fdiv_rn(__fmul_rn(alpha, wmax), qmax);
                 kq = __fdiv_rn(qmax, wmax);
             }
-            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            uint32_t o[LW];
+#pragma unroll
+            for (int j = 0; j < LW; j++)
+                o[j] = 0u;
             if (wmax > 0.f) {
                 const float2 k2 = make_float2(kq, kq);
-                uint32_t o[4];
 #pragma unroll
-                for (int j = 0; j < 4; j++) {
+                for (int j = 0; j < LW; j++) {
                     const float2 u0 = mul2(make_float2(w[4 * j], w[4 * j + 1]), k2);
                     const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
                     o[j] = encode4(CODE, u0.x, u0.y, u1.x, u1.y);
                 }
-                out = make_uint4(o[0], o[1], o[2], o[3]);
             }
             if (active) {
                 uint8_t *rec = args.out + blk * kRec;
-                // Records are 8-byte aligned: two 8-byte stores per thread.
-                *reinterpret_cast<uint2 *>(rec + kLaneCodes * part) = make_uint2(out.x, out.y);
-                *reinterpret_cast<uint2 *>(rec + kLaneCodes * part + 8) = make_uint2(out.z, out.w);
+                // Records are 8-byte aligned: 8-byte stores.
+#pragma unroll
+                for (int h = 0; h < LW / 2; h++)
+                    *reinterpret_cast<uint2 *>(rec + LC * part + 8 * h) = make_uint2(o[2 * h], o[2 * h + 1]);
                 if (part == 0)
                     *reinterpret_cast<uint2 *>(rec + B) = make_uint2(__float_as_uint(alpha), __float_as_uint(sc));
             }
