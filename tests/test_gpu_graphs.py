@@ -10,7 +10,9 @@ kernels are deterministic, so every check here is bit-exact:
   synchronisation between the calls;
 * compress -> shard reduce -> decompress captured in a CUDA graph and replayed
   on new input contents (the graph's kernels read the buffers, not captured
-  values) equals the eager calls on the same input.
+  values) equals the eager calls on the same input;
+* chains on three streams running at the same time equal each chain run
+  alone.
 """
 import numpy as np
 import pytest
@@ -112,4 +114,47 @@ def test_graph_replay_matches_eager(taco):
         graphed = snapshot()
         for name, a, b in zip(("packed", "reduced", "decompressed"), graphed, eager):
             assert np.array_equal(a, b), f"graph replay differs from the eager calls in {name} ({dist}, seed {seed})"
+    assert taco.device_status() == 0
+
+
+def test_concurrent_streams_match_sequential(taco):
+    """Calls on different streams may run at the same time on the GPU (each
+    grid schedules its own tiles); every output equals the one computed alone."""
+    rows, hidden, P = 4096, 2048, 4
+    seg_rows = rows // P
+    seg = taco.compressed_bytes(seg_rows, hidden, 128)
+    xs = [bf16_input(d, rows, hidden, seed=20 + i)
+          for i, d in enumerate(("student_t_channels", "laplace_outliers", "gaussian_sparse"))]
+    blocks = (128, 64, 256)
+
+    def chain(x, block, stream):
+        p = taco.compress(x, block, stream=stream)
+        y = taco.decompress(p, rows, hidden, block, stream=stream)
+        r = None
+        if block == 128:
+            r = taco.reduce_shards([p[i * seg:(i + 1) * seg] for i in range(P)], seg_rows, hidden, block,
+                                   stream=stream)
+        return p, y, r
+
+    def host(outs):
+        return [None if t is None else (t.cpu().numpy() if t.dtype == torch.uint8
+                                        else t.view(torch.int16).cpu().numpy()) for t in outs]
+
+    ref = []
+    for x, b in zip(xs, blocks):
+        ref.append(host(chain(x, b, torch.cuda.current_stream())))
+        torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in xs]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        outs = []
+        for x, b, s in zip(xs, blocks, streams):
+            with torch.cuda.stream(s):
+                outs.append(chain(x, b, s))
+        torch.cuda.synchronize()
+        for k, (o, r) in enumerate(zip(outs, ref)):
+            for name, a, b in zip(("packed", "decompressed", "reduced"), host(o), r):
+                assert (a is None) == (b is None)
+                if a is not None:
+                    assert np.array_equal(a, b), f"stream {k}: {name} differs from the call made alone"
     assert taco.device_status() == 0
