@@ -564,7 +564,7 @@ struct TcDecompressConfig {
 };
 
 #ifndef TACO_DTC64_CFG
-#define TACO_DTC64_CFG 322
+#define TACO_DTC64_CFG 422
 #endif
 #ifndef TACO_DTC128_CFG
 #define TACO_DTC128_CFG 622
@@ -577,7 +577,7 @@ struct TcDecompressConfig {
 #endif
 // Per block size, three digits: raw stages, A stages, output tiles.
 #ifndef TACO_DEPG64
-#define TACO_DEPG64 1
+#define TACO_DEPG64 2
 #endif
 #ifndef TACO_DEPG128
 #define TACO_DEPG128 2
@@ -589,7 +589,7 @@ struct TcDecompressConfig {
 #define TACO_DEPG512 3
 #endif
 // EPG: epilogue groups (3 for B = 256 and 512, whose epilogues carry the
-// butterfly across the parts' lanes; 2 for B = 128, where two tiles'
+// butterfly across the parts' lanes; 2 for B = 64 and 128, where two tiles'
 // epilogues in flight shorten each launch's tail).
 using DecompressTc64 =
     TcDecompressConfig<64, TACO_DTC64_CFG / 100, TACO_DTC64_CFG / 10 % 10, TACO_DTC64_CFG % 10, 0, TACO_DEPG64>;
