@@ -38,6 +38,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -217,6 +218,31 @@ class ClockSampler:
 # Oracle timing (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
+def oracle_build_info() -> str:
+    """Compiler and flags the oracle library is built with."""
+    import oracle
+    return "gcc " + " ".join(f for f in oracle.CFLAGS if f not in ("-fPIC", "-shared"))
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
 def oracle_step_time(x_bits: np.ndarray, block: int, shards: int, threads: int) -> float:
     """Wall time of one oracle step (compress, reduce of the P row-slices,
     decompress) over x_bits, split into block ranges across `threads`."""
@@ -316,7 +342,8 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "block": block,
                    "reduce_shards": shards, "sample_rows": rows},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model(), "compiler": oracle_build_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -615,11 +642,17 @@ def run_taco(args, rank, world):
         while sum(times) < budget:
             times.append(oracle_step_time(xs, block, P, threads))
         t_cpu = sum(times) / len(times)
+        # The same oracle on one core, on a sample of about 2 s.
+        rows1 = sample_rows_for(w, block, P, 1, 2.0)
+        t1 = oracle_step_time(x_host_bits[:rows1], block, P, 1)
         cpu = {"value": 6.0 * xs.size / t_cpu / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"rows [0, {srows}) of the {rows}x{hidden} tensor: {len(times)} oracle step(s) "
                          f"(compress, reduce of {P} row-slices, decompress), block ranges split over "
                          f"{threads} threads, mean time per step",
-               "seconds": sum(times)}
+               "seconds": sum(times),
+               "single_core": {"value": 6.0 * rows1 * hidden / t1 / 1e9, "unit": UNIT, "cores": 1,
+                               "sample": f"rows [0, {rows1}): one oracle step on one thread"},
+               "cpu_model": cpu_model(), "compiler": oracle_build_info()}
 
     line = {
         "metric": METRIC,

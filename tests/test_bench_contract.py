@@ -34,6 +34,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"] == "small_4096x1024"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["cpu_model"] and cb["compiler"].startswith("gcc -O2")
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
