@@ -490,21 +490,31 @@ def run_taco(args, rank, world):
     ms_step = max_over_ranks([ev0.elapsed_time(ev1) / K], device=dev)[0]
 
     # Each kernel alone: back-to-back launches over the rotating sets.
+    # Events split the replays into G groups: the mean over all launches, and
+    # the median and minimum of the groups' per-launch means.
     reps = max(4, min(250, (20 * K) // (R * 10)))
-    solo_ms = {}
+    G = min(10, reps)
+    reps = reps // G * G
+    solo_ms, solo_med, solo_min = {}, {}, {}
     with torch.cuda.stream(stream):
         for name, g in solo_graphs.items():
             for _ in range(2):
                 g.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(reps):
-                g.replay()
-            b.record(stream)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(G + 1)]
+            evs[0].record(stream)
+            for j in range(G):
+                for _ in range(reps // G):
+                    g.replay()
+                evs[j + 1].record(stream)
             stream.synchronize()
-            solo_ms[name] = a.elapsed_time(b) / (reps * R)
-    tot = max_over_ranks([solo_ms["compress"], solo_ms["reduce"], solo_ms["decompress"]], device=dev)
-    solo_ms = dict(zip(("compress", "reduce", "decompress"), tot))
+            per = [evs[j].elapsed_time(evs[j + 1]) / (reps // G * R) for j in range(G)]
+            solo_ms[name] = evs[0].elapsed_time(evs[G]) / (reps * R)
+            solo_med[name] = statistics.median(per)
+            solo_min[name] = min(per)
+    names = ("compress", "reduce", "decompress")
+    tot = max_over_ranks([solo_ms[k] for k in names] + [solo_med[k] for k in names] + [solo_min[k] for k in names],
+                         device=dev)
+    solo_ms, solo_med, solo_min = dict(zip(names, tot[0:3])), dict(zip(names, tot[3:6])), dict(zip(names, tot[6:9]))
 
     # Workloads of P seeded shards (the owner's step of the two-shot AllReduce
     # on full-size shards): the reduce of the P packed tensors, timed alone.
@@ -619,7 +629,8 @@ def run_taco(args, rank, world):
         ops[op] = {"ms": avg_ms[op], "bf16_gbs": 2 * n / t / 1e9,
                    "hbm_gbs": alg[op] / t / 1e9, "frac_of_measured_hbm": alg[op] / t / 1e9 / peak,
                    "frac_of_nominal_8tbs": alg[op] / t / 1e9 / 8000.0,
-                   "algorithmic_bytes": alg[op], "launches_timed": reps * R}
+                   "algorithmic_bytes": alg[op], "launches_timed": reps * R,
+                   "ms_median_of_groups": solo_med[op], "ms_min_of_groups": solo_min[op], "groups": G}
     dom = max(avg_ms, key=avg_ms.get)
     achieved = alg[dom] / (avg_ms[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
