@@ -32,18 +32,41 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h)
     return __uint_as_float(h << 16);
 }
 
+// Packed FP32x2 subtract (one issue for two IEEE subtractions).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // In-register Walsh-Hadamard transform of n values (strides 1 .. n/2).
+// Stride 1 pairs the two halves of a value pair and runs scalar; strides 2 ..
+// n/2 butterfly neighbouring pairs with packed FP32x2 adds and subtracts (the
+// same IEEE results per element, half the issue slots).
 template <int N>
 __device__ __forceinline__ void fwht_regs(float (&v)[N])
 {
 #pragma unroll
-    for (int h = 1; h < N; h <<= 1) {
+    for (int i = 0; i < N; i += 2) {
+        const float a = v[i], b = v[i + 1];
+        v[i] = a + b;
+        v[i + 1] = a - b;
+    }
 #pragma unroll
-        for (int i = 0; i < N; i++) {
+    for (int h = 2; h < N; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
             if ((i & h) == 0) {
-                const float a = v[i], b = v[i + h];
-                v[i] = a + b;
-                v[i + h] = a - b;
+                const float2 p = make_float2(v[i], v[i + 1]), q = make_float2(v[i + h], v[i + h + 1]);
+                const float2 s = add2(p, q), d = sub2(p, q);
+                v[i] = s.x;
+                v[i + 1] = s.y;
+                v[i + h] = d.x;
+                v[i + h + 1] = d.y;
             }
         }
     }
@@ -179,16 +202,20 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_compress_kernel(const 
                 }
             }
         }
-        float e = 0.f;
+        float2 e2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < B; i++)
-            e = fmaf(v[i], v[i], e);
+        for (int i = 0; i < B; i += 2) {
+            const float2 vi = make_float2(v[i], v[i + 1]);
+            e2[(i >> 1) & 1] = fma2(vi, vi, e2[(i >> 1) & 1]);
+        }
+        const float2 e01 = add2(e2[0], e2[1]);
+        const float e = e01.x + e01.y;
         if (rotate)
             fwht_regs<B>(v);
         float ymax = 0.f;
 #pragma unroll
-        for (int i = 0; i < B; i++)
-            ymax = fmaxf(ymax, fabsf(v[i]));
+        for (int i = 0; i < B; i += 2)
+            ymax = max3(ymax, fabsf(v[i]), fabsf(v[i + 1]));
         const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(e * (1.0f / B) + kEps)) : 1.0f;
         float s = 0.f, kq = 0.f;
         if (!dual_scale) {
@@ -199,11 +226,13 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_compress_kernel(const 
             kq = __fdiv_rn(qmax, ymax);
         }
         uint32_t cw[B / 4];
+        const float2 k2 = make_float2(kq, kq);
 #pragma unroll
-        for (int j = 0; j < B / 4; j++)
-            cw[j] = ymax > 0.f ? encode4(scheme.code, v[4 * j] * kq, v[4 * j + 1] * kq, v[4 * j + 2] * kq,
-                                         v[4 * j + 3] * kq)
-                               : 0u;
+        for (int j = 0; j < B / 4; j++) {
+            const float2 u0 = mul2(make_float2(v[4 * j], v[4 * j + 1]), k2);
+            const float2 u1 = mul2(make_float2(v[4 * j + 2], v[4 * j + 3]), k2);
+            cw[j] = ymax > 0.f ? encode4(scheme.code, u0.x, u0.y, u1.x, u1.y) : 0u;
+        }
         if (full) {
             // The warp's 32 records are 1280 contiguous bytes: stage, then store coalesced.
             __syncwarp();                         // the previous pass has read the buffer
@@ -299,8 +328,10 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_decompress_kernel(cons
         for (int q = 0; q < B / 8; q++) {
             uint32_t t[4];
 #pragma unroll
-            for (int j = 0; j < 4; j++)
-                t[j] = float2_to_bf16x2(v[8 * q + 2 * j] * f, v[8 * q + 2 * j + 1] * f);
+            for (int j = 0; j < 4; j++) {
+                const float2 g = mul2(make_float2(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]), make_float2(f, f));
+                t[j] = float2_to_bf16x2(g.x, g.y);
+            }
             o[q] = make_uint4(t[0], t[1], t[2], t[3]);
         }
         if (full) {
