@@ -30,7 +30,11 @@
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising.  TACO_OK means the
  *     kernel was launched.  Argument errors are found on the host before any
- *     launch and leave every output untouched.
+ *     launch and leave every output untouched.  Calls keep no state between
+ *     them, so calls on different streams (or threads) may run at the same
+ *     time on disjoint buffers; within a stream each kernel starts while the
+ *     previous one drains but reads its input only once that kernel is done.
+ *     The calls may be captured into CUDA graphs.
  *   - rows == 0 or hidden == 0 is an empty tensor: TACO_OK, nothing launched,
  *     pointers may be NULL.
  *   - Supported blocks: 32, 64, 128, 256, 512 (TACO_ERR_UNSUPPORTED_BLOCK
