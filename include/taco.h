@@ -34,7 +34,11 @@
  *     them, so calls on different streams (or threads) may run at the same
  *     time on disjoint buffers; within a stream each kernel starts while the
  *     previous one drains but reads its input only once that kernel is done.
- *     The calls may be captured into CUDA graphs.
+ *     The first call on a device does the library's one-time set-up for it
+ *     (kernel attributes, the fault flag's address); after that,
+ *     taco_compress, taco_decompress and taco_reduce_shards (and their _ex
+ *     forms) may be captured into CUDA graphs.  taco_device_status copies
+ *     synchronously and is not capturable.
  *   - rows == 0 or hidden == 0 is an empty tensor: TACO_OK, nothing launched,
  *     pointers may be NULL.
  *   - Supported blocks: 32, 64, 128, 256, 512 (TACO_ERR_UNSUPPORTED_BLOCK
