@@ -32,7 +32,8 @@
 //           reads it again and converts y * (Q_max / max|y|) to E4M3 two
 //           codes at a time into a shared-memory record tile, which one
 //           thread writes out with a bulk store.
-// H_B is written once per CTA into shared memory in the same swizzled layout.
+// H_B is written once per CTA into shared memory in the same swizzled layout,
+// by warps 1 and up while the CTA waits for the previous kernel.
 //
 // Scales: m = sum y^2 / B^2 (Eq. 6), alpha = tau / sqrt(m + eps) (Eq. 7),
 // s = alpha * max|y| * (1/sqrt B) / Q_max (Eq. 9), codes of y * (Q_max / max|y|)

@@ -21,7 +21,7 @@
 //   warps 2-5 "transposers": each thread takes one MMA row, copies its codes
 //             from the record into the 128-byte swizzled K-major A layout,
 //             and writes the block's factor s / sqrt(B) / alpha;
-//   warps 6.. epilogue, EPG groups of 4 warps taking alternate tiles: each
+//   warps 6.. epilogue, EPG groups of 4 warps taking rotating tiles: each
 //             thread reads its row of the accumulator from
 //             TMEM, scales it by the factor, converts two values per cvt to
 //             bf16 into a swizzled output tile, which one thread writes with

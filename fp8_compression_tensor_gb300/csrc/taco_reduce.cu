@@ -53,7 +53,7 @@ namespace {
 #ifndef TACO_REDUCE_CONSUMERS
 #define TACO_REDUCE_CONSUMERS 256
 #endif
-constexpr int kConsumers = TACO_REDUCE_CONSUMERS;   // threads of a consumer group, 16 elements each
+constexpr int kConsumers = TACO_REDUCE_CONSUMERS;   // threads of a consumer group
 constexpr int kGroups = TACO_REDUCE_GROUPS;     // consumer groups; group g takes items i % kGroups == g
 constexpr int kRThreads = kGroups * kConsumers + 32;   // + the loader warp
 #ifndef TACO_REDUCE_LANE_CODES
