@@ -16,8 +16,8 @@ only marshals arguments.  Build the library with
 """
 from ._binding import (CODES, LIBRARY_PATH, MAX_SHARDS, STATUS, SUPPORTED_BLOCKS, VARIANTS,  # noqa: F401
                        TacoError, compress, compressed_bytes, decompress, device_status, load_library, raw_call,
-                       reduce_shards)
+                       reduce_shards, selftest_encode_bits)
 
 __all__ = ["compress", "decompress", "reduce_shards", "compressed_bytes", "device_status", "load_library",
            "TacoError", "LIBRARY_PATH", "MAX_SHARDS", "SUPPORTED_BLOCKS", "STATUS", "VARIANTS", "CODES",
-           "raw_call"]
+           "raw_call", "selftest_encode_bits"]

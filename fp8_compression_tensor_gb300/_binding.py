@@ -87,6 +87,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.taco_reduce_shards_ex.restype = i32
         lib.taco_selftest_wait_timeout.argtypes = [vp]
         lib.taco_selftest_wait_timeout.restype = i32
+        lib.taco_selftest_encode_bits.argtypes = [i32, ctypes.c_uint32, i64, vp, vp]
+        lib.taco_selftest_encode_bits.restype = i32
         lib.taco_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.taco_device_status.restype = i32
         lib.taco_status_string.argtypes = [i32]
@@ -224,6 +226,19 @@ def reduce_shards(shards: Sequence[torch.Tensor], rows: int, hidden: int, block:
             rc = load_library().taco_reduce_shards_ex(ptrs, len(shards), rows, hidden, ctypes.byref(opt),
                                                       out.data_ptr(), _stream_handle(dev, stream))
     _check(rc, "taco_reduce_shards")
+    return out
+
+
+def selftest_encode_bits(code, first: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Self-test of the kernels' code conversion: fills the uint8 CUDA tensor
+    `out` with the codes of the float32 bit patterns first, first + 1, ...
+    (taco_selftest_encode_bits)."""
+    _check_cuda_tensor(out, torch.uint8, "out")
+    c = CODES[code] if isinstance(code, str) else int(code)
+    with torch.cuda.device(out.device):
+        rc = load_library().taco_selftest_encode_bits(c, first & 0xFFFFFFFF, out.numel(), out.data_ptr(),
+                                                      _stream_handle(out.device, stream))
+    _check(rc, "taco_selftest_encode_bits")
     return out
 
 

@@ -332,6 +332,9 @@ taco_status_t reduce_impl(const void *const *packed_shards, int num_shards, int6
 constexpr Scheme kMethod{TACO_VARIANT_ASH_DS, TACO_CODE_E4M3};
 
 }  // namespace
+cudaError_t launch_encode_selftest(int code, uint32_t first, int64_t count, void *codes, int grid,
+                                   cudaStream_t stream);   // taco_selftest.cu
+
 }  // namespace taco
 
 using namespace taco;
@@ -392,6 +395,29 @@ taco_status_t taco_reduce_shards_ex(const void *const *packed_shards, int num_sh
     if (st != TACO_OK)
         return st;
     return reduce_impl(packed_shards, num_shards, rows, hidden, options->block, scheme, packed_out, stream);
+}
+
+taco_status_t taco_selftest_encode_bits(int code, uint32_t first, int64_t count, void *codes_out,
+                                        taco_stream_t stream)
+{
+    if (code < TACO_CODE_E4M3 || code > TACO_CODE_INT8)
+        return TACO_ERR_BAD_OPTIONS;
+    if (count < 0 || count % 4 != 0 || first % 4 != 0 || count > (int64_t{1} << 32))
+        return TACO_ERR_BAD_SHAPE;
+    if (count == 0)
+        return TACO_OK;
+    if (!codes_out)
+        return TACO_ERR_NULL_POINTER;
+    if (!aligned16(codes_out))
+        return TACO_ERR_MISALIGNED;
+    DeviceState *dev = nullptr;
+    const taco_status_t st = device_state(&dev);
+    if (st != TACO_OK)
+        return st;
+    const int64_t want = (count / 4 + 255) / 256, cap = static_cast<int64_t>(dev->sm_count) * 8;
+    const cudaError_t e = launch_encode_selftest(code, first, count, codes_out, static_cast<int>(want < cap ? want : cap),
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TACO_OK : cuda_fail(e);
 }
 
 taco_status_t taco_selftest_wait_timeout(taco_stream_t stream)

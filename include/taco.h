@@ -195,6 +195,25 @@ TACO_API taco_status_t taco_device_status(taco_stream_t stream, uint32_t *flags_
  */
 TACO_API taco_status_t taco_selftest_wait_timeout(taco_stream_t stream);
 
+/*
+ * Self-test of the code conversion (no counterpart in the paper): writes
+ * codes_out[i] = the code (taco_code_t `code`) of the float32 whose bit
+ * pattern is first + i (modulo 2^32), for i < count, computed with the same
+ * device function the kernels use to quantize, so that it can be compared with
+ * an independent encoder over every float32.  E4M3 and E5M2 use the hardware's
+ * saturating round-to-nearest-even conversions (NaN inputs give NaN codes);
+ * INT8 rounds half to even and is defined for |u| < 127.5 (the kernels feed
+ * it |u| <= 127 up to FP32 rounding).
+ *
+ *   code       TACO_CODE_E4M3, _E5M2 or _INT8 (TACO_ERR_BAD_OPTIONS otherwise)
+ *   first      first bit pattern, a multiple of 4
+ *   count      number of codes, a multiple of 4, at most 2^32
+ *              (TACO_ERR_BAD_SHAPE otherwise; 0 launches nothing)
+ *   codes_out  device, out: count bytes, 16-byte aligned
+ */
+TACO_API taco_status_t taco_selftest_encode_bits(int code, uint32_t first, int64_t count, void *codes_out,
+                                                 taco_stream_t stream);
+
 /* Static, human-readable name of a status. */
 TACO_API const char *taco_status_string(taco_status_t status);
 

@@ -84,6 +84,7 @@ def _load():
         "taco_oracle_decompress_bf16_ex": (i32, [c_u8p, i64, i32, i32, i32, c_u16p]),
         "taco_oracle_reduce_shards_ex": (i32, [ctypes.POINTER(c_u8p), i32, i64, i32, i32, i32, c_u8p]),
         "taco_oracle_code_encode_array": (None, [i32, c_f32p, i64, c_u8p]),
+        "taco_oracle_code_encode_bits": (None, [i32, ctypes.c_uint32, i64, c_u8p]),
         "taco_oracle_code_value_array": (None, [i32, c_u8p, i64, c_f64p]),
         "taco_oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
         "taco_oracle_e4m3_value": (ctypes.c_double, [ctypes.c_uint8]),
@@ -169,6 +170,16 @@ def code_encode(code: int, u: np.ndarray) -> np.ndarray:
     u = np.ascontiguousarray(u, dtype=np.float32).reshape(-1)
     out = np.empty(u.size, dtype=np.uint8)
     _load().taco_oracle_code_encode_array(code, _ptr(u, ctypes.c_float), u.size, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def code_encode_bits(code: int, first: int, count: int, out: np.ndarray = None) -> np.ndarray:
+    """Codes of the float32 values with bit patterns first .. first + count - 1
+    (modulo 2^32), written into `out` (uint8, count elements) if given."""
+    if out is None:
+        out = np.empty(count, dtype=np.uint8)
+    assert out.dtype == np.uint8 and out.size == count and out.flags.c_contiguous
+    _load().taco_oracle_code_encode_bits(code, first & 0xFFFFFFFF, count, _ptr(out, ctypes.c_uint8))
     return out
 
 

@@ -561,6 +561,14 @@ void taco_oracle_code_encode_array(int code, const float *u, int64_t n, uint8_t 
         out[i] = code_encode(code, u[i]);
 }
 
+/* Codes of the float32 values with bit patterns first, first + 1, ...
+ * (modulo 2^32): every input of the conversion, for comparisons. */
+void taco_oracle_code_encode_bits(int code, uint32_t first, int64_t count, uint8_t *out)
+{
+    for (int64_t i = 0; i < count; i++)
+        out[i] = code_encode(code, f32_from_bits(first + (uint32_t)i));
+}
+
 void taco_oracle_code_value_array(int code, const uint8_t *codes, int64_t n, double *out)
 {
     for (int64_t i = 0; i < n; i++)

@@ -92,3 +92,18 @@ def test_binding_refuses_cpu_tensors():
     import fp8_compression_tensor_gb300 as t
     with pytest.raises(TypeError):
         t.compress(torch.zeros(4, 128, dtype=torch.bfloat16), 128)
+
+
+def test_encode_selftest_validated_on_host(lib):
+    """taco_selftest_encode_bits checks its arguments before any device call."""
+    fn = lib.taco_selftest_encode_bits
+    assert fn(3, 0, 16, 16, None) == 9            # unknown code format
+    assert fn(-1, 0, 16, 16, None) == 9
+    assert fn(0, 0, 6, 16, None) == 2             # count not a multiple of 4
+    assert fn(0, 2, 16, 16, None) == 2            # first not a multiple of 4
+    assert fn(0, 0, (1 << 32) + 4, 16, None) == 2  # more than every pattern
+    assert fn(0, 0, -4, 16, None) == 2
+    assert fn(1, 0, 0, None, None) == 0           # nothing to do
+    assert fn(1, 0, 16, None, None) == 1          # null output
+    assert fn(2, 0, 16, 8, None) == 4             # misaligned output
+

@@ -286,3 +286,15 @@ def test_bad_scheme_rejected():
         oracle.compress(bits, 128, 4, 0)
     with pytest.raises(ValueError):
         oracle.compress(bits, 128, 0, 3)
+
+
+def test_encode_bits_equals_the_array_encoder():
+    """code_encode_bits (every input of a bit-pattern range, modulo 2^32) is
+    the same encoder as code_encode on the corresponding float32 array."""
+    for code in (0, 1, 2):
+        for first in (0, 0x3BFFF000, 0x7F7FF000, 0xBF000000, 0xFFFFF000):
+            bits = (np.arange(1 << 13, dtype=np.uint64) + first) & 0xFFFFFFFF
+            u = bits.astype(np.uint32).view(np.float32)
+            ref = oracle.code_encode(code, u)
+            assert np.array_equal(oracle.code_encode_bits(code, first, bits.size), ref), (code, hex(first))
+
