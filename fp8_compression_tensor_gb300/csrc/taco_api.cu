@@ -80,7 +80,9 @@ void init_device(DeviceState &st)
     const int blocks[5] = {32, 64, 128, 256, 512};
     for (int i = 0; i < 5 && e == cudaSuccess; i++) {
         if (tensor_core_block(blocks[i])) {
-            e = init_kernel(compress_kernel_info(blocks[i]), &st.ctas_per_sm);
+            e = init_kernel(compress_kernel_info(blocks[i], 0), &st.ctas_per_sm);
+            if (e == cudaSuccess)
+                e = init_kernel(compress_kernel_info(blocks[i], 2), &st.ctas_per_sm);
             for (int code = 0; code < 3 && e == cudaSuccess; code += 2)   // E5M2 shares the E4M3 kernel
                 e = init_kernel(decompress_kernel_info(blocks[i], code), &st.ctas_per_sm);
         } else {
@@ -224,7 +226,7 @@ taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, in
     }
     // Tensor-core kernel over tiles of 128 blocks: one CTA per tile, of which
     // one per SM runs and takes the tiles of CTAs it cancels before they start.
-    const KernelInfo ki = compress_kernel_info(block);
+    const KernelInfo ki = compress_kernel_info(block, scheme.variant);
     const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
     if (ntiles > INT32_MAX)
         return TACO_ERR_BAD_SHAPE;

@@ -44,6 +44,7 @@
 // and converts Z = alpha y / sqrt(B) directly; E5M2 and INT8 codes use
 // Q_max = 57344 and 127.
 #include <cstring>
+#include <type_traits>
 
 #include <cuda.h>
 
@@ -139,7 +140,7 @@ __device__ void write_hadamard_sw128(uint8_t *h, bool rotate)
     }
 }
 
-template <int B, int STAGES, int EPG, int NBG>
+template <int B, int STAGES, int EPG, int NBG, bool DS_ONLY>
 __global__ void __launch_bounds__(tc_threads(EPG), 1)
     taco_compress_kernel(const __grid_constant__ CUtensorMap tmap_x, uint8_t *__restrict__ packed,
                             int64_t nblocks, uint32_t *__restrict__ fault, const Scheme scheme)
@@ -211,7 +212,8 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     }
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
-    const bool rotate = scheme.variant != 2;                        // DS only: no rotation
+    // DS only (no rotation) is its own instantiation; the others rotate.
+    constexpr bool rotate = !DS_ONLY;
     const bool adaptive = scheme.variant == 0 || scheme.variant == 3;  // alpha from Eqs. (6)-(7)
     const bool dual_scale = scheme.variant != 3;                    // s from Eq. (9)
     write_hadamard_sw128<Lay::kN>(base + Lay::kOffH, rotate);
@@ -395,29 +397,68 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             const uint32_t rec_block = sbase + Lay::kOffOut + ob * Lay::kOutBytes + blk * Lay::kRec;
             const uint32_t rec = rec_block + part * 128;
 
-            // Pass 2: codes (Eq. 10) two per cvt, 32 per chunk.
-            const float2 k2 = make_float2(k, k);
+            // Pass 2: codes (Eq. 10) two per cvt, 32 per chunk.  `scaled`:
+            // every value is first multiplied by `pre` (exact).
+            auto code_pass = [&](float kk, auto scaled, float pre) {
+                const float2 k2 = make_float2(kk, kk);
+                // The rare scaled pass and the divisions of DS only stay
+                // compact (one chunk at a time).
+#pragma unroll((decltype(scaled)::value || DS_ONLY) ? 1 : Lay::kAccCols / 32)
+                for (int c = 0; c < Lay::kAccCols / 32; c++) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + 32 * c, r);
+                    tmem_ld_wait();
+                    if constexpr (decltype(scaled)::value) {
 #pragma unroll
-            for (int c = 0; c < Lay::kAccCols / 32; c++) {
-                uint32_t r[32];
-                tmem_ld32(taddr + 32 * c, r);
-                tmem_ld_wait();
-                uint32_t cw[8];
+                        for (int j = 0; j < 32; j++)
+                            r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), pre));
+                    }
+                    uint32_t cw[8];
+                    if constexpr (!DS_ONLY) {
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const float2 u0 = mul2(make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), k2);
-                    const float2 u1 =
-                        mul2(make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), k2);
-                    cw[j] = encode4(scheme.code, u0.x, u0.y, u1.x, u1.y);
+                        for (int j = 0; j < 8; j++) {
+                            const float2 u0 =
+                                mul2(make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), k2);
+                            const float2 u1 =
+                                mul2(make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), k2);
+                            cw[j] = encode4(scheme.code, u0.x, u0.y, u1.x, u1.y);
+                        }
+                    } else {
+                        // DS only: the unrotated block's values G / s with s =
+                        // max|G| / Q_max, by IEEE division as Eq. (10) writes it
+                        // (ratios of bf16 values land exactly on rounding
+                        // midpoints often, and there only the quotient itself
+                        // decides the code as the method does).
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            float u[4];
+#pragma unroll
+                            for (int h = 0; h < 4; h++)
+                                u[h] = s > 0.f ? __fdiv_rn(__uint_as_float(r[4 * j + h]), s) : 0.f;
+                            cw[j] = encode4(scheme.code, u[0], u[1], u[2], u[3]);
+                        }
+                    }
+                    if (!(ymax > 0.f)) {
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+                            cw[j] = 0u;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        sts64(rec + 32 * c + 8 * j, cw[2 * j], cw[2 * j + 1]);
                 }
-                if (!(ymax > 0.f)) {
-#pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        cw[j] = 0u;
+            };
+            code_pass(k, std::false_type{}, 1.0f);
+            if constexpr (!DS_ONLY) {
+                // A tiny rotation (0 < max|y| < 2^-100; Q_max / max|y| may
+                // have overflowed above) is coded again from values scaled by
+                // 2^64, which keeps the roundings of the unscaled formula.  DS
+                // only divides and needs no scaling.
+                const bool tiny = dual_scale && ymax > 0.f && ymax < kTinyValue;
+                if (__any_sync(kFullMask, tiny)) {     // warp-uniform, rare
+                    const float pre = tiny ? kTinyUp : 1.0f;
+                    code_pass(__fdiv_rn(qmax, __fmul_rn(ymax, pre)), std::true_type{}, pre);
                 }
-#pragma unroll
-                for (int j = 0; j < 4; j++)
-                    sts64(rec + 32 * c + 8 * j, cw[2 * j], cw[2 * j + 1]);
             }
             // The accumulator is read: hand it back to the MMA warp.
             tc_fence_before_sync();
@@ -473,10 +514,14 @@ template <int B, int STAGES, int EPG, int NBG>
 struct TcCompressConfig {
     using Lay = TcCompressLayout<B, STAGES, EPG, NBG>;
     static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
-    static void *fn() { return reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG>); }
-    static KernelInfo info()
+    static void *fn(bool ds_only)
     {
-        return KernelInfo{fn(), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), Lay::kTileBlocks, 0};
+        return ds_only ? reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG, true>)
+                       : reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG, false>);
+    }
+    static KernelInfo info(bool ds_only)
+    {
+        return KernelInfo{fn(ds_only), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), Lay::kTileBlocks, 0};
     }
 };
 
@@ -500,13 +545,14 @@ using CompressTc512 = TcCompressConfig<512, TACO_TC512_CFG / 100, TACO_TC512_CFG
 
 }  // namespace
 
-KernelInfo compress_kernel_info(int block)
+KernelInfo compress_kernel_info(int block, int variant)
 {
+    const bool ds_only = variant == 2;
     switch (block) {
-    case 64: return CompressTc64::info();
-    case 128: return CompressTc128::info();
-    case 256: return CompressTc256::info();
-    case 512: return CompressTc512::info();
+    case 64: return CompressTc64::info(ds_only);
+    case 128: return CompressTc128::info(ds_only);
+    case 256: return CompressTc256::info(ds_only);
+    case 512: return CompressTc512::info(ds_only);
     default: return KernelInfo{};
     }
 }
@@ -514,7 +560,7 @@ KernelInfo compress_kernel_info(int block)
 cudaError_t launch_compress(int block, Scheme scheme, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault,
                             int grid, cudaStream_t stream)
 {
-    const KernelInfo ki = compress_kernel_info(block);
+    const KernelInfo ki = compress_kernel_info(block, scheme.variant);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     CUtensorMap map;

@@ -390,7 +390,13 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                         w[2 * q + 1] = v.y;
                     }
                     const uint2 meta = from_global ? *reinterpret_cast<const uint2 *>(rg + B) : lds64(rs + B);
-                    f = __fdiv_rn(__fmul_rn(__uint_as_float(meta.y), rr), __uint_as_float(meta.x));
+                    const float sv = __uint_as_float(meta.y), av = __uint_as_float(meta.x);
+                    f = __fdiv_rn(__fmul_rn(sv, rr), av);
+                    // A tiny factor (below 2^-100, or flushed to zero by the
+                    // division) is stored 2^64 times larger and negated: the
+                    // epilogue then scales its products back by 2^-64.
+                    if (sv > 0.f && f < kTinyValue)
+                        f = -__fdiv_rn(__fmul_rn(__fmul_rn(sv, kTinyUp), rr), av);
                 } else {
 #pragma unroll
                     for (int q = 0; q < PC / 4; q++)
@@ -497,7 +503,17 @@ __global__ void __launch_bounds__(dthreads(EPG), 1)
                         }
                     }
                 }
-                const float f = fb[b];
+                // A negative factor is a tiny block's factor times -2^64: its
+                // products are scaled back by 2^-64 (the rare pass below).
+                float f = fb[b];
+                if (__any_sync(kFullMask, f < 0.f)) {      // warp-uniform, rare
+                    if (f < 0.f) {                         // the products, scaled back; then a factor 1
+#pragma unroll
+                        for (int h = 0; h < 32; h++)
+                            r[h] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(r[h]), -f), kTinyDown));
+                        f = 1.0f;
+                    }
+                }
                 const float2 f2 = make_float2(f, f);
                 const int row = (B == 64) ? 2 * m + b : m; // y row within the tile
                 const int el = (B == 64) ? e0 % 64 : e0;   // element within the block row

@@ -17,6 +17,22 @@ constexpr float kTau = 1.0f;
 constexpr float kEps = 1e-30f;
 constexpr float kQmax = 448.0f;
 
+// Blocks at the bottom of the binary32 range (the near-zero region where the
+// Adaptive Scale makes alpha ~ 1e15).  The kernels work on unscaled values
+// (the rotation y = H G, or a shard's factor s / alpha), which there sit near
+// or inside the subnormal range: Q_max / max|y| overflows once max|y| <
+// Q_max / FLT_MAX (2^-119.2 for E4M3, 2^-112.2 for E5M2), and a subnormal
+// factor keeps only a few significant bits.  Below kTinyValue such a value is
+// multiplied by kTinyUp = 2^64 first (exact) and the result by kTinyDown =
+// 2^-64 at the end, which gives the same roundings as the unscaled formula
+// would in a binary32 without overflow or underflow.
+constexpr float kTinyValue = 0x1p-100f;
+// The shard reduce detects such blocks by their sum: below 2^-80 every
+// factor s_p / alpha_p may lie in that range (sum_p 448 s_p / alpha_p bounds it).
+constexpr float kTinySum = 0x1p-80f;
+constexpr float kTinyUp = 0x1p64f;
+constexpr float kTinyDown = 0x1p-64f;
+
 // Fault flag bits written when a kernel gives up waiting.
 constexpr uint32_t kFaultCompress = 1u;
 constexpr uint32_t kFaultDecompress = 2u;

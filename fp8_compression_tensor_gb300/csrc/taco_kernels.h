@@ -47,7 +47,7 @@ struct Scheme {
     int code;
 };
 
-KernelInfo compress_kernel_info(int block);
+KernelInfo compress_kernel_info(int block, int variant);   // variant 2 (DS only) has its own kernel
 KernelInfo decompress_kernel_info(int block, int code);   // code 2 (INT8) has its own kernel
 KernelInfo reduce_kernel_info(int block, int code, int num_shards);
 

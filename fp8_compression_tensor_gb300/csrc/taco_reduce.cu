@@ -33,6 +33,8 @@
 // tile to the consumers only when it issues its copies, after the stage's
 // previous item was released, so the consumer groups, which take turns on the
 // stages, never see an older phase of a stage barrier as the one they wait for.
+#include <type_traits>
+
 #include "taco_device.cuh"
 #include "taco_kernels.h"
 #include "taco_sched.cuh"
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     const int64_t nblocks = args.nblocks;
     const bool adaptive = args.variant == 0 || args.variant == 3;   // alpha' from the energy of W
     const bool dual_scale = args.variant != 3;                      // s' from max|W|
+    const bool ds_only = args.variant == 2;                         // no rotation: W is the decoded sum
     // Stages of P record runs in the ring.
     const int stage_bytes = P * Lay::kRunBytes;
     int nst = kRingBytes / stage_bytes;
@@ -279,80 +282,108 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             const int64_t blk = t * T + bl;
             const uint32_t rec_s = sbase + Lay::kOffRing + s * stage_bytes + bl * kRec;
 
-            // W = sum_p q_p * (s_p / alpha_p) in shard order.
+            // W = sum_p q_p * (s_p / alpha_p) in shard order.  `scaled`: every
+            // factor is formed 2^64 times larger (s_p 2^64 / alpha_p), and the
+            // records are read again from global memory (the stage is gone).
             float w[LC];
+            auto accumulate = [&](auto scaled) {
+                constexpr bool kScaled = decltype(scaled)::value;
+                auto factor = [&](uint2 meta) {
+                    const float sv = kScaled ? __fmul_rn(__uint_as_float(meta.y), kTinyUp) : __uint_as_float(meta.y);
+                    return __fdividef(sv, __uint_as_float(meta.x));
+                };
 #pragma unroll
-            for (int k = 0; k < LC; k++)
-                w[k] = 0.f;
-            // s_p / alpha_p below is within 2 ulp (alpha_p <= 1e15 is far from
-            // the range where the fast quotient underflows).
-            if (active && !from_global) {
-                const uint32_t r0 = rec_s + LC * part;
+                for (int k = 0; k < LC; k++)
+                    w[k] = 0.f;
+                // s_p / alpha_p below is within 2 ulp (alpha_p <= 1e15 is far from
+                // the range where the fast quotient underflows).
+                if (active && !from_global && !kScaled) {
+                    const uint32_t r0 = rec_s + LC * part;
 #pragma unroll(PFIX > 0 ? PFIX : 1)
-                for (int p = 0; p < P; p++) {
-                    const uint32_t r = r0 + p * Lay::kRunBytes;
-                    uint32_t words[LW];
+                    for (int p = 0; p < P; p++) {
+                        const uint32_t r = r0 + p * Lay::kRunBytes;
+                        uint32_t words[LW];
 #pragma unroll
-                    for (int h = 0; h < LW / 2; h++) {
-                        const uint2 a = lds64(r + 8 * h);
-                        words[2 * h] = a.x;
-                        words[2 * h + 1] = a.y;
+                        for (int h = 0; h < LW / 2; h++) {
+                            const uint2 a = lds64(r + 8 * h);
+                            words[2 * h] = a.x;
+                            words[2 * h + 1] = a.y;
+                        }
+                        accumulate_shard<CODE>(w, words, factor(lds64(r - LC * part + B)));
                     }
-                    const uint2 meta = lds64(r - LC * part + B);
-                    accumulate_shard<CODE>(w, words, __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
-                }
-            } else if (active) {
-                // The tile's odd last record is not in the bulk copies.
-                for (int p = 0; p < P; p++) {
-                    const uint8_t *r = shard_ptr[p] + blk * kRec;
-                    uint32_t words[LW];
+                } else if (active) {
+                    // The tile's odd last record is not in the bulk copies (and
+                    // the rare scaled pass reads every record again from there).
+#pragma unroll 1
+                    for (int p = 0; p < P; p++) {
+                        const uint8_t *r = shard_ptr[p] + blk * kRec;
+                        uint32_t words[LW];
 #pragma unroll
-                    for (int h = 0; h < LW / 2; h++) {
-                        const uint2 a = ldg_u2(r + LC * part + 8 * h);
-                        words[2 * h] = a.x;
-                        words[2 * h + 1] = a.y;
+                        for (int h = 0; h < LW / 2; h++) {
+                            const uint2 a = ldg_u2(r + LC * part + 8 * h);
+                            words[2 * h] = a.x;
+                            words[2 * h + 1] = a.y;
+                        }
+                        accumulate_shard<CODE>(w, words, factor(ldg_u2(r + B)));
                     }
-                    const uint2 meta = ldg_u2(r + B);
-                    accumulate_shard<CODE>(w, words, __fdividef(__uint_as_float(meta.y), __uint_as_float(meta.x)));
                 }
-            }
+            };
+            accumulate(std::false_type{});
             // The stage is read: hand it back to the loader.
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty_bar(s));
 
             // Energy |W|^2 and max|W| over the block's threads.
-            float2 e2 = make_float2(0.f, 0.f);
-            float wmax = 0.f;
+            float e = 0.f, wmax = 0.f;
+            auto energy_max = [&]() {
+                float2 e2 = make_float2(0.f, 0.f);
+                wmax = 0.f;
 #pragma unroll
-            for (int k = 0; k < LC; k += 2) {
-                const float2 wi = make_float2(w[k], w[k + 1]);
-                e2 = fma2(wi, wi, e2);
-                wmax = max3(wmax, fabsf(w[k]), fabsf(w[k + 1]));
-            }
-            float e = e2.x + e2.y;
+                for (int k = 0; k < LC; k += 2) {
+                    const float2 wi = make_float2(w[k], w[k + 1]);
+                    e2 = fma2(wi, wi, e2);
+                    wmax = max3(wmax, fabsf(w[k]), fabsf(w[k + 1]));
+                }
+                e = e2.x + e2.y;
 #pragma unroll
-            for (int d = 1; d < Lay::kLpb; d <<= 1) {
-                e = e + __shfl_xor_sync(kFullMask, e, d);
-                wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, d));
+                for (int d = 1; d < Lay::kLpb; d <<= 1) {
+                    e = e + __shfl_xor_sync(kFullMask, e, d);
+                    wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, d));
+                }
+            };
+            energy_max();
+            // A sum below 2^-80 (the near-zero region, where the factors
+            // s_p / alpha_p are subnormal or zero in binary32, or an exact
+            // cancellation) is summed again with scaled factors; its results
+            // are scaled back by post = 2^-64 below.  DS only keeps the
+            // unscaled sum, which is then the decoded shards' FP32 sum itself
+            // (products q s_p, no rotation, alpha = 1).
+            const bool tiny = active && !ds_only && wmax < kTinySum;
+            if (__any_sync(kFullMask, tiny)) {     // warp-uniform, rare
+                if (tiny)
+                    accumulate(std::true_type{});
+                energy_max();                       // the other blocks get the same values again
             }
+            const float post = tiny ? kTinyDown : 1.0f;
 
-            const float m = e * (1.0f / B);
+            // post = 2^-64 where W was summed 2^64 times larger (1 elsewhere).
+            const float m = __fmul_rn(__fmul_rn(e, post), post * (1.0f / B));
             const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(m + kEps)) : 1.0f;
             constexpr float qmax = CODE == 0 ? 448.0f : CODE == 1 ? 57344.0f : 127.0f;
             float sc = 0.f, kq = 0.f;
             if (!dual_scale) {          // ASH only: codes of alpha' W, s' = 1
                 sc = 1.0f;
-                kq = alpha;
+                kq = __fmul_rn(alpha, post);
             } else if (wmax > 0.f) {
-                sc = __fdiv_rn(__fmul_rn(alpha, wmax), qmax);
+                sc = __fdiv_rn(__fmul_rn(__fmul_rn(alpha, wmax), post), qmax);
                 kq = __fdiv_rn(qmax, wmax);
             }
             uint32_t o[LW];
 #pragma unroll
             for (int j = 0; j < LW; j++)
                 o[j] = 0u;
-            if (wmax > 0.f) {
+            if (wmax > 0.f && !ds_only) {
                 const float2 k2 = make_float2(kq, kq);
 #pragma unroll
                 for (int j = 0; j < LW; j++) {
@@ -360,6 +391,13 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                     const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
                     o[j] = encode4(CODE, u0.x, u0.y, u1.x, u1.y);
                 }
+            } else if (wmax > 0.f) {
+                // DS only: W is the sum of the decoded shards itself (no
+                // rotation, alpha = 1); its codes are W / s' by IEEE division.
+#pragma unroll
+                for (int j = 0; j < LW; j++)
+                    o[j] = encode4(CODE, __fdiv_rn(w[4 * j], sc), __fdiv_rn(w[4 * j + 1], sc),
+                                   __fdiv_rn(w[4 * j + 2], sc), __fdiv_rn(w[4 * j + 3], sc));
             }
             if (active) {
                 uint8_t *rec = args.out + blk * kRec;

@@ -217,21 +217,43 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_compress_kernel(const 
         for (int i = 0; i < B; i += 2)
             ymax = max3(ymax, fabsf(v[i]), fabsf(v[i + 1]));
         const float alpha = adaptive ? __fdiv_rn(kTau, __fsqrt_rn(e * (1.0f / B) + kEps)) : 1.0f;
+        // A tiny rotation (max|y| < 2^-100) is scaled by 2^64 before its codes
+        // are formed, so that Q_max / max|y| cannot overflow.
+        const bool tiny = dual_scale && rotate && ymax > 0.f && ymax < kTinyValue;
+        const float pre = tiny ? kTinyUp : 1.0f;
         float s = 0.f, kq = 0.f;
         if (!dual_scale) {
             s = 1.0f;
             kq = __fmul_rn(alpha, rr);
         } else if (ymax > 0.f) {
             s = __fdiv_rn(__fmul_rn(__fmul_rn(alpha, ymax), rr), qmax);
-            kq = __fdiv_rn(qmax, ymax);
+            kq = __fdiv_rn(qmax, __fmul_rn(ymax, pre));
+        }
+        if (tiny) {
+#pragma unroll
+            for (int i = 0; i < B; i++)
+                v[i] = __fmul_rn(v[i], kTinyUp);
         }
         uint32_t cw[B / 4];
         const float2 k2 = make_float2(kq, kq);
+        if (rotate || !dual_scale) {
 #pragma unroll
-        for (int j = 0; j < B / 4; j++) {
-            const float2 u0 = mul2(make_float2(v[4 * j], v[4 * j + 1]), k2);
-            const float2 u1 = mul2(make_float2(v[4 * j + 2], v[4 * j + 3]), k2);
-            cw[j] = ymax > 0.f ? encode4(scheme.code, u0.x, u0.y, u1.x, u1.y) : 0u;
+            for (int j = 0; j < B / 4; j++) {
+                const float2 u0 = mul2(make_float2(v[4 * j], v[4 * j + 1]), k2);
+                const float2 u1 = mul2(make_float2(v[4 * j + 2], v[4 * j + 3]), k2);
+                cw[j] = ymax > 0.f ? encode4(scheme.code, u0.x, u0.y, u1.x, u1.y) : 0u;
+            }
+        } else {
+            // DS only: G / s by IEEE division, as Eq. (10) writes it (bf16
+            // ratios often land exactly on rounding midpoints).
+#pragma unroll
+            for (int j = 0; j < B / 4; j++) {
+                float u[4];
+#pragma unroll
+                for (int h = 0; h < 4; h++)
+                    u[h] = s > 0.f ? __fdiv_rn(v[4 * j + h], s) : 0.f;
+                cw[j] = ymax > 0.f ? encode4(scheme.code, u[0], u[1], u[2], u[3]) : 0u;
+            }
         }
         if (full) {
             // The warp's 32 records are 1280 contiguous bytes: stage, then store coalesced.
@@ -293,7 +315,13 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_decompress_kernel(cons
             rec = packed + k * kRec;
         }
         const uint2 meta = *reinterpret_cast<const uint2 *>(rec + B);
-        const float f = __fdiv_rn(__fmul_rn(__uint_as_float(meta.y), rr), __uint_as_float(meta.x));
+        const float sv = __uint_as_float(meta.y), av = __uint_as_float(meta.x);
+        float f = __fdiv_rn(__fmul_rn(sv, rr), av);
+        // A tiny factor (below 2^-100, or flushed to zero by the division) is
+        // formed 2^64 times larger and the products are scaled back after it.
+        const bool tiny = sv > 0.f && f < kTinyValue;
+        if (tiny)
+            f = __fdiv_rn(__fmul_rn(__fmul_rn(sv, kTinyUp), rr), av);
         float v[B];
 #pragma unroll
         for (int j = 0; j < B / 8; j++) {
@@ -329,7 +357,9 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_decompress_kernel(cons
             uint32_t t[4];
 #pragma unroll
             for (int j = 0; j < 4; j++) {
-                const float2 g = mul2(make_float2(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]), make_float2(f, f));
+                float2 g = mul2(make_float2(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]), make_float2(f, f));
+                if (tiny)
+                    g = make_float2(__fmul_rn(g.x, kTinyDown), __fmul_rn(g.y, kTinyDown));
                 t[j] = float2_to_bf16x2(g.x, g.y);
             }
             o[q] = make_uint4(t[0], t[1], t[2], t[3]);

@@ -81,14 +81,46 @@ def near_midpoint(u_exact: np.ndarray, rel: float = 2e-6, code: int = 0) -> np.n
     return d <= rel * np.maximum(a, 2.0 ** -9)
 
 
-def noise_zone(u_exact: np.ndarray, block: int, rel: float = 1e-4) -> np.ndarray:
-    """True where an exact pre-quantisation value is below the FP32 noise of
-    its block (rel of the block's largest |u|): an exact zero or a value that
-    cancels to almost nothing comes out of either implementation's FP32 order
-    as noise of arbitrary sign, which a format with a wide subnormal range
-    (E5M2) still resolves into distinct codes."""
-    u = np.abs(np.asarray(u_exact, dtype=np.float64)).reshape(-1, block)
-    return (u <= rel * u.max(axis=1, keepdims=True)).reshape(np.shape(u_exact))
+# FP32 resolution of a block, relative to its largest |u|: the two
+# implementations compute the pre-quantisation values in binary32 in
+# different orders (the oracle through one or two explicit rotations of up to
+# 512 terms), so they may differ by a few units of 2^-24 of the block
+# maximum.  Below NOISE_REL of that maximum an exact value lies within the
+# noise (it cancels to almost nothing), and both results are noise of
+# arbitrary sign; E5M2's fine subnormal grid (2^-16 against Q_max = 57344)
+# resolves such noise into codes many grid steps apart, E4M3 and INT8 do not.
+NOISE_REL = 2.0 ** -17
+CODE_QMAX = {0: 448.0, 1: 57344.0, 2: 127.0}
+
+
+def block_max(u_exact: np.ndarray, block: int) -> np.ndarray:
+    """Largest |u| of each element's block, broadcast to the elements."""
+    a = np.abs(np.asarray(u_exact, dtype=np.float64))
+    m = a.reshape(-1, block).max(axis=1, keepdims=True)
+    return np.broadcast_to(m, (a.size // block, block)).reshape(a.shape)
+
+
+def noise_zone(u_exact: np.ndarray, block: int) -> np.ndarray:
+    """True where |u_exact| <= NOISE_REL * (largest |u| of its block)."""
+    return np.abs(np.asarray(u_exact, dtype=np.float64)) <= NOISE_REL * block_max(u_exact, block)
+
+
+def exact_values(u_exact: np.ndarray, code: int = 0) -> np.ndarray:
+    """The code value nearest to each exact u (ties to the even code,
+    saturating at +-Q_max), from the format's value table: what a
+    correctly rounded implementation in real arithmetic would store."""
+    u = np.asarray(u_exact, dtype=np.float64)
+    if code == 2:
+        return np.clip(np.rint(u), -127.0, 127.0)
+    table = decode_table(code)
+    top = 0x7E if code == 0 else 0x7B
+    mags = table[:top + 1]                       # codes 0 .. top, increasing
+    a = np.minimum(np.abs(u), mags[-1])
+    hi = np.clip(np.searchsorted(mags, a), 1, top)
+    lo = hi - 1
+    dlo, dhi = a - mags[lo], mags[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return np.copysign(mags[pick], u)
 
 
 def reduce_exact_u(shard_packed, block: int, variant: int = 0, code: int = 0) -> np.ndarray:
@@ -103,21 +135,33 @@ def reduce_exact_u(shard_packed, block: int, variant: int = 0, code: int = 0) ->
         W = W + table[c] * (s / a)[:, None]
     if variant == 3:
         return W / np.sqrt((W * W).sum(axis=1, keepdims=True) / block + 1e-30)
-    qmax = {0: 448.0, 1: 57344.0, 2: 127.0}[code]
+    qmax = CODE_QMAX[code]
     m = np.abs(W).max(axis=1, keepdims=True)
     return np.where(m > 0, qmax * W / np.where(m > 0, m, 1.0), 0.0)
 
 
 def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = True,
-                    ambiguous: np.ndarray | None = None, code: int = 0) -> dict:
+                    u_exact: np.ndarray | None = None, code: int = 0) -> dict:
     """Compares packed records (uint8 arrays) from two implementations.
 
-    `ambiguous` (optional, shape [blocks, B]) marks elements whose exact value
-    is a rounding tie up to FP32 noise (near_midpoint) or lies in the noise
-    of its block (noise_zone); a difference there is an FP32 rounding-order
-    effect and is counted separately instead of against the 1e-4 budget, as
-    long as the two decoded values differ by one grid step or by at most
-    2e-4 of the block's largest code value."""
+    Scales agree to 1e-6 relative (s = 0 blocks exactly).  Codes: every
+    differing element counts (+0 and -0 are the same value), and each differs
+    by exactly one grid step.  The count is at most 1e-4 of the elements.
+
+    With `u_exact` (the float64 values before quantisation), two FP32
+    rounding-order effects are recognised, and both stay bounded:
+      - rounding ties: where u_exact is a midpoint up to FP32 noise
+        (near_midpoint), each implementation's FP32 value lands on either
+        side; the count may exceed the 1e-4 budget only by twice the number
+        of ties at which the reference itself disagrees with the correctly
+        rounded exact value (exact_values), and such elements still differ
+        by one step;
+      - the noise zone (noise_zone): elements whose exact value is below the
+        block's FP32 resolution (NOISE_REL of its largest |u|) hold FP32
+        noise in either implementation; they may differ by more than one
+        grid step, and are not counted against the budget, but their decoded
+        values may differ by at most 2 * NOISE_REL of the block's largest
+        |u| (what either implementation's FP32 order can produce there)."""
     cg, ag, sg = records(got, block)
     cr, ar, sr = records(ref, block)
     d = code_step_distance(cg, cr, code)
@@ -125,25 +169,42 @@ def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = 
     vg, vr = table[cg], table[cr]
     zero_sign = (cg != cr) & (d == 0)
     n = cg.size
-    tie = np.zeros_like(d, dtype=bool) if ambiguous is None else np.asarray(ambiguous).reshape(d.shape)
+    mism = d > 0
+    if u_exact is None:
+        tie = np.zeros(d.shape, dtype=bool)
+        noise = np.zeros(d.shape, dtype=bool)
+        ref_tie_flips = 0
+    else:
+        u = np.asarray(u_exact, dtype=np.float64).reshape(d.shape)
+        tie = near_midpoint(u, code=code)
+        noise = noise_zone(u, block)
+        umax = block_max(u, block)
+        ref_tie_flips = int((tie & ~noise & (vr != exact_values(u, code))).sum())
     nz = sr > 0
     alpha_rel = float(np.max(np.abs(ag / ar - 1))) if ar.size else 0.0
     s_rel = float(np.max(np.abs(sg[nz] / sr[nz] - 1))) if nz.any() else 0.0
+    budget = CODE_MISMATCH_MAX * n + 2 * ref_tie_flips
+    counted = mism & ~noise
     stats = {
         "blocks": int(cr.shape[0]),
-        "code_mismatch_frac": float(((d > 0) & ~tie).sum() / max(n, 1)),
-        "tie_mismatches": int(((d > 0) & tie).sum()),
-        "code_max_step": int(d[~tie].max()) if (~tie).any() else 0,
-        "ambiguous_bad": int(((d > 1) & tie & (np.abs(vg - vr) > 2e-4 * np.abs(vr).max(axis=1, keepdims=True))).sum()),
+        "code_mismatches": int(counted.sum()),
+        "code_mismatch_frac": float(counted.sum() / max(n, 1)),
+        "mismatch_budget": float(budget),
+        "tie_mismatches": int((mism & tie).sum()),
+        "ties": int(tie.sum()),
+        "ref_tie_flips": ref_tie_flips,
+        "noise_mismatches": int((mism & noise).sum()),
+        "code_max_step": int(d[~noise].max()) if (~noise).any() else 0,
+        "noise_max_diff": float((np.abs(vg - vr)[noise] / np.maximum(umax[noise], 1e-300)).max()) if noise.any() else 0.0,
         "signed_zero_diffs": int(zero_sign.sum()),
         "alpha_max_rel": alpha_rel,
         "s_max_rel": s_rel,
         "s_zero_mismatch": int(((sg == 0) != (sr == 0)).sum()),
     }
     if check:
-        assert stats["code_mismatch_frac"] <= CODE_MISMATCH_MAX, stats
+        assert stats["code_mismatches"] <= budget, stats
         assert stats["code_max_step"] <= 1, stats
-        assert stats["ambiguous_bad"] == 0, stats
+        assert stats["noise_max_diff"] <= 2 * NOISE_REL, stats
         assert stats["alpha_max_rel"] <= SCALE_RTOL, stats
         assert stats["s_max_rel"] <= SCALE_RTOL, stats
         assert stats["s_zero_mismatch"] == 0, stats
@@ -157,7 +218,9 @@ def compare_decoded(got_bf16: np.ndarray, ref_bf16: np.ndarray, block: int, chec
     g = bf16_to_f64(got_bf16).reshape(-1, block)
     r = bf16_to_f64(ref_bf16).reshape(-1, block)
     diff = np.abs(g - r)
-    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 1e-38))) - 7)
+    # One bf16 step at |r|: 2^(e - 7) in the normal range, 2^-133 (the
+    # subnormal spacing) below 2^-126.
+    step = np.maximum(np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 1e-45))) - 7), 2.0 ** -133)
     bmax = np.abs(r).max(axis=1, keepdims=True)
     ok = diff <= np.maximum(step, 0) + 2e-6 * bmax
     stats = {"mismatch_frac": float((diff > 0).mean()) if diff.size else 0.0,

@@ -1,17 +1,27 @@
 """GPU parity at the five workloads' full sizes, in the launch configuration the
-benchmark times (one call over the whole tensor).  The oracle recomputes a
-sample of blocks one by one (plus the first and last blocks, so both ragged
-ends of the grid are covered), and the reconstruction relative L2 error over
-the whole tensor is compared with the oracle's own (the oracle runs over the
-whole tensor on several threads)."""
+benchmark times (one call over the whole tensor), element by element over the
+whole tensor:
+
+- compress: the GPU's records against the oracle's (the oracle runs over the
+  whole tensor, block ranges on several host threads);
+- decompress: the GPU decodes the oracle's records, and every bf16 output is
+  checked against the oracle's decode of the same records;
+- the reconstruction relative L2 error of the GPU's own round trip against the
+  oracle's;
+- the 8-shard reduce: the GPU reduces the oracle's shards, against the
+  oracle's reduce of the same shards, and the GPU decodes the oracle's
+  reduced records; plus the whole pipeline on the GPU.
+
+A sample of blocks (and both ends) is also recomputed by the oracle one block
+at a time, independently of the threaded runs."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads
-from parity import (RELL2_ATOL, compare_records, oracle_compress_parallel, oracle_decompress_parallel,
-                    rel_l2_bf16)
+from parity import (RELL2_ATOL, compare_decoded, compare_records, oracle_compress_parallel,
+                    oracle_decompress_parallel, rel_l2_bf16)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -43,7 +53,12 @@ def block_rows(packed, ids, block):
 
 
 CASES = [("small_4096x1024", 128), ("gpt_activation_8192x4096", 128), ("tp_grad_8192x5120", 128),
-         ("large_16384x8192", 64), ("large_16384x8192", 128), ("large_16384x8192", 256)]
+         ("large_16384x8192", 64), ("large_16384x8192", 128), ("large_16384x8192", 256),
+         ("large_16384x8192", 32), ("large_16384x8192", 512)]
+
+
+def bits_of(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
 
 
 @pytest.mark.parametrize("name,block", CASES)
@@ -57,23 +72,34 @@ def test_full_size_compress_decompress(taco, name, block):
     torch.cuda.synchronize()
     assert taco.device_status() == 0
     got = packed.cpu().numpy()
+    y_gpu = bits_of(y)
+    del xd, packed, y
+    # Sampled blocks recomputed one by one.
     ids = sample_blocks(nblocks, 1)
     xs = x.reshape(-1, block)[ids].reshape(-1)
     compare_records(block_rows(got, ids, block), oracle.compress(xs, block), block)
-    # Whole-tensor reconstruction error against the oracle's.
+    # Every record of the tensor.
     ref = oracle_compress_parallel(x, block)
+    compare_records(got, ref, block)
+    # Decompress in isolation: the GPU decodes the oracle's records, every element checked.
     y_ref = oracle_decompress_parallel(ref, x.size, block)
-    y_gpu = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
+    y_dec = bits_of(taco.decompress(torch.from_numpy(ref).to(DEV), w.rows, w.hidden, block))
+    assert taco.device_status() == 0
+    compare_decoded(y_dec, y_ref, block)
+    ys = oracle.decompress(block_rows(ref, ids, block), ids.size * block, block)
+    assert np.array_equal(y_ref.reshape(-1, block)[ids].reshape(-1), ys)
+    # Whole-tensor reconstruction error against the oracle's.
     e_gpu, e_ref = rel_l2_bf16(y_gpu, x), rel_l2_bf16(y_ref, x)
     assert abs(e_gpu - e_ref) <= RELL2_ATOL, (e_gpu, e_ref)
-    del xd, packed, y
     torch.cuda.empty_cache()
 
 
 def test_full_size_shard_reduce(taco):
     """Eight shards of the full [8192 x 5120] workload.  (1) Reduce in isolation:
-    the GPU reduces the oracle's packed shards, and the oracle reduces the same
-    shards' sampled records.  (2) The whole pipeline on the GPU (compress each
+    the GPU reduces the oracle's packed shards; every record is compared with
+    the oracle's reduce of the same shards (and a sample with the oracle run
+    one block at a time).  (2) The GPU decodes the oracle's reduced records,
+    every element checked.  (3) The whole pipeline on the GPU (compress each
     shard, reduce, decompress) against the oracle's pipeline: relative L2 error
     of the decoded sum against the exact sum of the bf16 shards."""
     w = workloads.WORKLOADS["shard_reduce_p8_8192x5120"]
@@ -84,10 +110,11 @@ def test_full_size_shard_reduce(taco):
     out = taco.reduce_shards([torch.from_numpy(r).to(DEV) for r in ref_shards], w.rows, w.hidden, block)
     torch.cuda.synchronize()
     assert taco.device_status() == 0
+    out_np = out.cpu().numpy()
+    del out
     ids = sample_blocks(n // block, 2)
     ref = oracle.reduce_shards([block_rows(r, ids, block) for r in ref_shards], ids.size * block, block)
-    compare_records(block_rows(out.cpu().numpy(), ids, block), ref, block)
-    del out
+    compare_records(block_rows(out_np, ids, block), ref, block)
 
     gpu_shards = [taco.compress(to_dev(x, w.rows, w.hidden), block) for x in xs]
     red = taco.reduce_shards(gpu_shards, w.rows, w.hidden, block)
@@ -102,15 +129,22 @@ def test_full_size_shard_reduce(taco):
     nblk = n // block
     chunk = -(-nblk // 64)
     y_ref = np.empty(n, dtype=np.uint16)
+    red_ref = np.empty(nblk * (block + 8), dtype=np.uint8)
 
     def run(b0):
         b1 = min(nblk, b0 + chunk)
         sl = [r[b0 * (block + 8):b1 * (block + 8)] for r in ref_shards]
         rr = oracle.reduce_shards(sl, (b1 - b0) * block, block)
+        red_ref[b0 * (block + 8):b1 * (block + 8)] = rr
         y_ref[b0 * block:b1 * block] = oracle.decompress(rr, (b1 - b0) * block, block)
 
     with ThreadPoolExecutor(16) as ex:
         list(ex.map(run, range(0, nblk, chunk)))
+    # Every reduced record of the GPU against the oracle's reduce of the same shards.
+    compare_records(out_np, red_ref, block)
+    # The GPU decodes the oracle's reduced records: every element.
+    y_dec = bits_of(taco.decompress(torch.from_numpy(red_ref).to(DEV), w.rows, w.hidden, block))
+    compare_decoded(y_dec, y_ref, block)
     yg = (y_gpu.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     yr = (y_ref.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     nt = np.linalg.norm(total)

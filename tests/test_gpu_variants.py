@@ -17,8 +17,8 @@ import torch
 import oracle
 import workloads
 from helpers import bf16_to_f64, records
-from parity import (RELL2_ATOL, compare_decoded, compare_records, near_midpoint, noise_zone,
-                    oracle_compress_parallel, oracle_decompress_parallel, reduce_exact_u, rel_l2_bf16)
+from parity import (RELL2_ATOL, compare_decoded, compare_records, oracle_compress_parallel,
+                    oracle_decompress_parallel, reduce_exact_u, rel_l2_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -66,8 +66,7 @@ def test_compress_decompress(taco, B, variant, code):
     ref = oracle_compress_parallel(bits, B, variant, code)
     got = taco.compress(to_dev(bits).view(ROWS, HIDDEN), B, variant=variant, code=code).cpu().numpy()
     u = exact_u(bits, B, variant, code)
-    ties = near_midpoint(u, code=code) | noise_zone(u, B)
-    compare_records(got, ref, B, ambiguous=ties, code=code)
+    compare_records(got, ref, B, u_exact=u, code=code)
     # Decompress the oracle's records on the GPU.
     y = from_dev(taco.decompress(torch.from_numpy(ref).cuda(), ROWS, HIDDEN, B, variant=variant, code=code))
     y_ref = oracle_decompress_parallel(ref, n, B, variant, code)
@@ -90,8 +89,7 @@ def test_reduce(taco, B, variant, code):
     got = taco.reduce_shards([torch.from_numpy(s).cuda() for s in shards], rows, hidden, B,
                              variant=variant, code=code).cpu().numpy()
     u = reduce_exact_u(shards, B, variant, code)
-    ties = near_midpoint(u, code=code) | noise_zone(u, B)
-    compare_records(got, ref, B, ambiguous=ties, code=code)
+    compare_records(got, ref, B, u_exact=u, code=code)
     assert taco.device_status() == 0
 
 
@@ -109,8 +107,7 @@ def test_reduce_eight_shards(taco, B, variant, code):
     got = taco.reduce_shards([torch.from_numpy(s).cuda() for s in shards], rows, hidden, B,
                              variant=variant, code=code).cpu().numpy()
     u = reduce_exact_u(shards, B, variant, code)
-    ties = near_midpoint(u, code=code) | noise_zone(u, B)
-    compare_records(got, ref, B, ambiguous=ties, code=code)
+    compare_records(got, ref, B, u_exact=u, code=code)
     assert taco.device_status() == 0
 
 
@@ -155,8 +152,7 @@ def test_small_and_large_blocks_ragged(taco, B):
         shards = [ref, oracle.compress(workloads.generate("laplace_outliers", rows, hidden, 99), B)]
         r = taco.reduce_shards([torch.from_numpy(x).cuda() for x in shards], rows, hidden, B).cpu().numpy()
         u = reduce_exact_u(shards, B)
-        compare_records(r, oracle.reduce_shards(shards, bits.size, B), B,
-                        ambiguous=near_midpoint(u) | noise_zone(u, B))
+        compare_records(r, oracle.reduce_shards(shards, bits.size, B), B, u_exact=u)
     assert taco.device_status() == 0
 
 
