@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of TACO's fused FP8 compression hot path on GB300.
 
-One step is one pass of the whole path over one synthetic tensor (default: the
-GPT-style TP activation, bf16 [8192 x 4096], block 128):
+Workload (default): bf16 [16384 x 8192] (134M elements, Laplace(0, 1e-3) bulk
+with 0.1% +-U(0.05, 0.5) outliers), block 128 -- the largest single-GPU
+configuration.  One step is one pass of the whole path over one tensor:
 
   1. taco_compress      x (bf16)            -> packed records    (Eqs. 5-10)
   2. taco_reduce_shards P = 8 row-slices of the packed tensor, taken as the P
@@ -20,10 +21,14 @@ write-back of every kernel's output is paid inside the timed region.  Each
 kernel's own average launch duration is timed the same way: graphs of R
 back-to-back launches of that kernel alone, replayed, over the rotating sets.
 
-Metric: GB/s of bf16 data processed = (2N compressed + 2N decompressed + 2N
-logical bf16 bytes of the P reduced segments) per step / step time.  The
-roofline object reports the dominant kernel's algorithmic bytes per launch
-over its average duration against the measured HBM copy bandwidth.
+Metric (`value`): compress/decompress GB/s of bf16 input = 2 x 2N bytes (the
+bf16 tensor compressed plus the bf16 tensor decompressed) over the sum of the
+two kernels' average launch durations.  The whole step (with the reduce) is
+reported under `step`; the same workload at the other block sizes under
+`blocks`; the reduce of 8 full-size [8192 x 5120] shards under
+`reduce_full_shards`.  The roofline object reports the dominant kernel's
+algorithmic bytes per launch over its average duration against the measured
+HBM copy bandwidth.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl taco|reference]
 
@@ -70,7 +75,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["taco", "reference"], default="taco")
-    ap.add_argument("--workload", default="gpt_activation_8192x4096", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="large_16384x8192", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--block", type=int, default=128)
     ap.add_argument("--shards", type=int, default=8)
     ap.add_argument("--variant", default="ash_ds", choices=["ash_ds", "hadamard_ds", "ds_only", "ash_only"],
@@ -80,6 +85,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other block sizes and the full-size shard reduce (extra keys)")
     return ap.parse_args()
 
 
@@ -133,15 +140,16 @@ def measured_peak():
 
 
 def traffic_for(op: str, workload: str, block: int):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel's
-    source has not changed since the capture."""
+    """DRAM bytes per launch from a committed ncu capture (dict with the bytes
+    read and written and how they were taken), if the kernel's source has not
+    changed since the capture; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
         e = t[op][f"{workload}/b{block}"]
         if e["source_hash"] != source_hash(KERNEL_SOURCES[op]):
             return None
-        return float(e["dram_bytes_per_launch"])
+        return e
     except Exception:
         return None
 
@@ -218,12 +226,6 @@ class ClockSampler:
 # Oracle timing (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_build_info() -> str:
-    """Compiler and flags the oracle library is built with."""
-    import oracle
-    return "gcc " + " ".join(f for f in oracle.CFLAGS if f not in ("-fPIC", "-shared"))
-
-
 def cpu_model() -> str:
     """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
     try:
@@ -243,9 +245,10 @@ def cpu_model() -> str:
     return platform.machine()
 
 
-def oracle_step_time(x_bits: np.ndarray, block: int, shards: int, threads: int) -> float:
-    """Wall time of one oracle step (compress, reduce of the P row-slices,
-    decompress) over x_bits, split into block ranges across `threads`."""
+def oracle_op_times(x_bits: np.ndarray, block: int, shards: int, threads: int) -> dict:
+    """The oracle's compress, reduce of the P row-slices and decompress over
+    x_bits, each split into block ranges across `threads`: their wall times
+    (seconds) and outputs (packed records, reduced segment, decoded bf16)."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     x = np.ascontiguousarray(x_bits).reshape(-1)
@@ -274,12 +277,26 @@ def oracle_step_time(x_bits: np.ndarray, block: int, shards: int, threads: int) 
         b0, b1 = r
         y[b0 * block:b1 * block] = oracle.decompress(packed[b0 * rec:b1 * rec], (b1 - b0) * block, block)
 
-    t0 = time.perf_counter()
+    t = {}
     with ThreadPoolExecutor(threads) as ex:
-        list(ex.map(comp, ranges(nblk)))
-        list(ex.map(reduce_, ranges(seg_blk)))
-        list(ex.map(decomp, ranges(nblk)))
-    return time.perf_counter() - t0
+        for name, fn, total in (("compress", comp, nblk), ("reduce", reduce_, seg_blk),
+                                ("decompress", decomp, nblk)):
+            t0 = time.perf_counter()
+            list(ex.map(fn, ranges(total)))
+            t[name] = time.perf_counter() - t0
+    return {"seconds": t, "packed": packed, "reduced": red, "y": y}
+
+
+def oracle_metric(n: int, t: dict) -> float:
+    """The metric for one oracle pass over n elements: GB/s of bf16 input of
+    compress and decompress (2 x 2n bytes over their summed time)."""
+    return 4.0 * n / (t["compress"] + t["decompress"]) / 1e9
+
+
+def oracle_build_info() -> str:
+    """Compiler and flags the oracle library is built with."""
+    import oracle
+    return "gcc " + " ".join(f for f in oracle.CFLAGS if f not in ("-fPIC", "-shared"))
 
 
 def max_over_ranks(values, device=None):
@@ -308,17 +325,22 @@ def host_threads() -> int:
 
 
 def sample_rows_for(w, block, shards, threads, budget_s):
-    """Rows of the workload whose oracle step takes about budget_s seconds
-    (a multiple of `shards` rows, at least `shards`)."""
+    """Rows of the workload whose oracle pass (compress, reduce, decompress)
+    takes about budget_s seconds (a multiple of `shards` rows, at least
+    `shards`)."""
     probe_rows = max(shards, min(w.rows, 64 * shards))
     x = w.tensor(row_count=probe_rows)
-    t = oracle_step_time(x, block, shards, threads)
+    t = sum(oracle_op_times(x, block, shards, threads)["seconds"].values())
     rows = int(probe_rows * budget_s / max(t, 1e-6))
     rows = max(shards, min(w.rows, rows)) // shards * shards
     return rows
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on the host cores, on a row sample of
+    the same workload; each step is one oracle pass (compress, reduce of the
+    P row-slices, decompress), and `value` is the same metric as the GPU
+    arm's (compress/decompress GB/s of bf16 input)."""
     if rank != 0:
         return
     w = workloads.WORKLOADS[args.workload]
@@ -329,19 +351,22 @@ def run_reference(args, rank, world):
     rows = sample_rows_for(w, block, shards, threads, per_step_budget)
     x = w.tensor(row_count=rows)
     for _ in range(args.warmup):
-        oracle_step_time(x, block, shards, threads)
-    times = [oracle_step_time(x, block, shards, threads) for _ in range(args.steps)]
+        oracle_op_times(x, block, shards, threads)
+    runs = [oracle_op_times(x, block, shards, threads)["seconds"] for _ in range(args.steps)]
     n = x.size
-    t = sum(times) / len(times)
-    value = 6.0 * n / t / 1e9
+    t = {k: sum(r[k] for r in runs) / len(runs) for k in runs[0]}
+    value = oracle_metric(n, t)
+    step_s = sum(t.values())
     sample = (f"rows [0, {rows}) of the {w.rows}x{w.hidden} tensor ({n} elements) per step: "
-              f"compress, reduce of {shards} row-slices, decompress; block ranges split over {threads} threads")
+              f"compress, reduce of {shards} row-slices, decompress; block ranges split over {threads} threads; "
+              f"value = 2 x 2n bytes over the mean compress + decompress time")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "block": block,
                    "reduce_shards": shards, "sample_rows": rows},
+        "ops_ms": {k: v * 1e3 for k, v in t.items()},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
                          "cpu_model": cpu_model(), "compiler": oracle_build_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -489,65 +514,60 @@ def run_taco(args, rank, world):
     flags = taco.device_status(stream=stream)
     ms_step = max_over_ranks([ev0.elapsed_time(ev1) / K], device=dev)[0]
 
-    # Each kernel alone: back-to-back launches over the rotating sets.
-    # Events split the replays into G groups: the mean over all launches, and
-    # the median and minimum of the groups' per-launch means.
-    reps = max(4, min(250, (20 * K) // (R * 10)))
-    G = min(10, reps)
-    reps = reps // G * G
-    solo_ms, solo_med, solo_min = {}, {}, {}
-    with torch.cuda.stream(stream):
-        for name, g in solo_graphs.items():
-            for _ in range(2):
-                g.replay()
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(G + 1)]
-            evs[0].record(stream)
-            for j in range(G):
-                for _ in range(reps // G):
-                    g.replay()
-                evs[j + 1].record(stream)
-            stream.synchronize()
-            per = [evs[j].elapsed_time(evs[j + 1]) / (reps // G * R) for j in range(G)]
-            solo_ms[name] = evs[0].elapsed_time(evs[G]) / (reps * R)
-            solo_med[name] = statistics.median(per)
-            solo_min[name] = min(per)
     names = ("compress", "reduce", "decompress")
-    tot = max_over_ranks([solo_ms[k] for k in names] + [solo_med[k] for k in names] + [solo_min[k] for k in names],
-                         device=dev)
-    solo_ms, solo_med, solo_min = dict(zip(names, tot[0:3])), dict(zip(names, tot[3:6])), dict(zip(names, tot[6:9]))
+    solo = time_solo(solo_graphs, stream, R, K, dev)
+    solo_ms = {k: solo[k]["ms"] for k in names}
+    t_wall2 = time.time()            # the clock record covers the steps and the per-kernel timings
 
-    # Workloads of P seeded shards (the owner's step of the two-shot AllReduce
-    # on full-size shards): the reduce of the P packed tensors, timed alone.
+    peak, peak_src = measured_peak()
+    alg = {"compress": 2 * n + nbytes, "reduce": P * seg_bytes + seg_bytes, "decompress": nbytes + 2 * n}
+
+    def op_line(op, t, alg_bytes, n_el):
+        sec = t["ms"] * 1e-3
+        return {"ms": t["ms"], "bf16_gbs": 2 * n_el / sec / 1e9, "hbm_gbs": alg_bytes / sec / 1e9,
+                "frac_of_measured_hbm": alg_bytes / sec / 1e9 / peak,
+                "frac_of_nominal_8tbs": alg_bytes / sec / 1e9 / 8000.0, "algorithmic_bytes": alg_bytes,
+                "launches_timed": t["launches"], "ms_median_of_groups": t["median"], "ms_min_of_groups": t["min"],
+                "groups": t["groups"]}
+
+    ops = {op: op_line(op, solo[op], alg[op], n) for op in names}
+    # The reduce's logical bf16 input is P segments of N / P elements: N.
+    value = whole_job_gbs(world, 4.0 * n, solo_ms["compress"] + solo_ms["decompress"])
+
+    # Extra keys: the same workload at its other block sizes, and the reduce
+    # of 8 full-size shards (the owner's local step on the P-seed workload).
+    blocks = None
     full_reduce = None
-    if len(w.seeds) > 1:
-        Pf = len(w.seeds)
-        xsf = [torch.from_numpy(w.tensor(seed=sd).view(np.int16)).view(torch.bfloat16).to(dev).view(rows, hidden)
-               for sd in w.seeds]
-        full = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(Pf)]
-        full_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        with torch.cuda.stream(stream):
-            for p_ in range(Pf):
-                taco.compress(xsf[p_], block, out=full[p_], stream=stream, **scheme)
-            del xsf
-            g_full = capture(lambda: taco.reduce_shards(full, rows, hidden, block, out=full_out, stream=stream,
-                                                        **scheme))
-            for _ in range(3):
-                g_full.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps_f = 50
-            a.record(stream)
-            for _ in range(reps_f):
-                g_full.replay()
-            b.record(stream)
-            stream.synchronize()
-        ms_f = max_over_ranks([a.elapsed_time(b) / reps_f], device=dev)[0]
-        alg_f = (Pf + 1) * nbytes
-        full_reduce = {"ms": ms_f, "shards": Pf, "algorithmic_bytes": alg_f, "hbm_gbs": alg_f / ms_f / 1e6,
-                       "logical_bf16_gbs": Pf * 2 * n / ms_f / 1e6,
-                       "what": f"reduce of {Pf} full-size packed shards (seeds {list(w.seeds)}), "
-                               f"back-to-back graph replays"}
+    if not args.no_extras:
+        blocks = {}
+        for b in w.blocks:
+            if b == block:
+                continue
+            nb = taco.compressed_bytes(rows, hidden, b)
+            sb = taco.compressed_bytes(seg_rows, hidden, b)
+            pk_b = [torch.empty(nb, dtype=torch.uint8, device=dev) for _ in range(R)]
+            rd_b = [torch.empty(sb, dtype=torch.uint8, device=dev) for _ in range(R)]
+            sg_b = [[pk_b[r][p * sb:(p + 1) * sb] for p in range(P)] for r in range(R)]
+            fns = {"compress": lambda r, b=b, pk_b=pk_b: taco.compress(xs[r], b, out=pk_b[r], stream=stream,
+                                                                        **scheme),
+                   "reduce": lambda r, b=b, sg_b=sg_b, rd_b=rd_b: taco.reduce_shards(
+                       sg_b[r], seg_rows, hidden, b, out=rd_b[r], stream=stream, **scheme),
+                   "decompress": lambda r, b=b, pk_b=pk_b: taco.decompress(pk_b[r], rows, hidden, b, out=ys[r],
+                                                                          stream=stream, **scheme)}
+            with torch.cuda.stream(stream):
+                for r in range(R):
+                    fns["compress"](r)
+                graphs = {name: capture(lambda fn=fns[name]: [fn(r) for r in range(R)]) for name in names}
+            tb = time_solo(graphs, stream, R, K, dev)
+            alg_b = {"compress": 2 * n + nb, "reduce": (P + 1) * sb, "decompress": nb + 2 * n}
+            entry = {op: op_line(op, tb[op], alg_b[op], n) for op in names}
+            entry["value"] = whole_job_gbs(world, 4.0 * n, tb["compress"]["ms"] + tb["decompress"]["ms"])
+            blocks[str(b)] = entry
+            del pk_b, rd_b, sg_b, graphs
+            torch.cuda.empty_cache()
+        full_reduce = time_full_shard_reduce(taco, workloads.WORKLOADS["shard_reduce_p8_8192x5120"], block, scheme,
+                                             stream, dev, capture, peak)
     x, packed, reduced, y = xs[0], packs[0], reds[0], ys[0]
-    segments = segs[0]
 
     # Reconstruction error of the round trip (paper Eq. 21), fp64 over the tensor.
     with torch.cuda.stream(stream):
@@ -556,6 +576,7 @@ def run_taco(args, rank, world):
     stream.synchronize()
     xd, yd = x.double(), y.double()
     rel_l2 = float(torch.linalg.vector_norm(yd - xd) / torch.linalg.vector_norm(xd))
+    del xd, yd
 
     # End to end through the public API with host buffers: pinned H2D of the
     # step's input, the three calls, D2H of the decompressed tensor and of
@@ -599,75 +620,73 @@ def run_taco(args, rank, world):
             e2e_step(k)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k_e2e = max(1, min(K, 400))
+        k_e2e = max(1, min(K, 100))
         e0.record(s_in)
         for k in range(k_e2e):
             e2e_step(k)
         e1.record(s_out)
         barrier()
         ms = max_over_ranks([e0.elapsed_time(e1) / k_e2e], device=dev)[0]
-        e2e = {"value": whole_job_gbs(world, 6.0 * n, ms), "unit": UNIT, "ms_per_step": ms,
+        e2e = {"value": whole_job_gbs(world, 4.0 * n, ms), "unit": UNIT, "ms_per_step": ms,
                "steps": k_e2e, "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + seg_bytes,
+               "what": "compress + reduce + decompress through the public API with the input uploaded from and "
+                       "the decompressed tensor and reduced segment downloaded to pinned host memory every step; "
+                       "value = 2 x 2N bf16 bytes per step over the step time",
                "overlap": "uploads, kernels and downloads on three streams, two buffer sets"}
 
     sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1) if not args.no_clocks else None
+    clocks = sampler.summary(t_wall0, t_wall2) if not args.no_clocks else None
+    flags |= taco.device_status(stream=stream)
+
+    cpu = None
+    parity = None
+    if not args.no_cpu_baseline:
+        threads = host_threads()
+        # About 20 s of CPU work (threads x wall seconds): a row sample of the
+        # workload, its oracle pass repeated while the whole tensor is too
+        # small to fill the budget.
+        budget = max(1.0, 20.0 / threads)
+        srows = sample_rows_for(w, block, P, threads, budget)
+        xsmp = x_host_bits[:srows]
+        runs = [oracle_op_times(xsmp, block, P, threads)]
+        while sum(sum(r["seconds"].values()) for r in runs) < budget:
+            runs.append(oracle_op_times(xsmp, block, P, threads))
+        t_cpu = {k: sum(r["seconds"][k] for r in runs) / len(runs) for k in runs[0]["seconds"]}
+        # The same oracle on one core, on a sample of about 2 s.
+        rows1 = sample_rows_for(w, block, P, 1, 2.0)
+        t1 = oracle_op_times(x_host_bits[:rows1], block, P, 1)["seconds"]
+        cpu = {"value": oracle_metric(xsmp.size, t_cpu), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"rows [0, {srows}) of the {rows}x{hidden} tensor: {len(runs)} oracle pass(es) "
+                         f"(compress, reduce of {P} row-slices, decompress), block ranges split over "
+                         f"{threads} threads; value = 2 x 2n bytes over the mean compress + decompress time",
+               "seconds": sum(sum(r["seconds"].values()) for r in runs),
+               "ops_ms": {k: v * 1e3 for k, v in t_cpu.items()},
+               "single_core": {"value": oracle_metric(rows1 * hidden, t1), "unit": UNIT, "cores": 1,
+                               "sample": f"rows [0, {rows1}): one oracle pass on one thread"},
+               "cpu_model": cpu_model(), "compiler": oracle_build_info()}
+        # Parity of the timed kernels against the oracle's outputs on the same
+        # sample rows (outside every timed region).
+        parity = parity_against_oracle(taco, runs[-1], xsmp, block, P, scheme, stream, dev)
 
     if rank != 0:
         return
 
-    peak, peak_src = measured_peak()
-    alg = {
-        "compress": 2 * n + nbytes,
-        "reduce": P * seg_bytes + seg_bytes,
-        "decompress": nbytes + 2 * n,
-    }
-    avg_ms = solo_ms
-    ops = {}
-    for op in ("compress", "reduce", "decompress"):
-        t = avg_ms[op] * 1e-3
-        ops[op] = {"ms": avg_ms[op], "bf16_gbs": 2 * n / t / 1e9,
-                   "hbm_gbs": alg[op] / t / 1e9, "frac_of_measured_hbm": alg[op] / t / 1e9 / peak,
-                   "frac_of_nominal_8tbs": alg[op] / t / 1e9 / 8000.0,
-                   "algorithmic_bytes": alg[op], "launches_timed": reps * R,
-                   "ms_median_of_groups": solo_med[op], "ms_min_of_groups": solo_min[op], "groups": G}
-    dom = max(avg_ms, key=avg_ms.get)
-    achieved = alg[dom] / (avg_ms[dom] * 1e-3) / 1e9
+    dom = max(("compress", "decompress", "reduce"), key=lambda k: solo_ms[k])
+    achieved = alg[dom] / (solo_ms[dom] * 1e-3) / 1e9
+    tr = traffic_for(dom, w.name, block)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_src,
-                "traffic": traffic_for(dom, w.name, block),
+                "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "traffic_read": tr["dram_read_per_launch"] if tr else None,
+                "traffic_write": tr["dram_write_per_launch"] if tr else None,
+                "traffic_how": tr["how"] if tr else "no capture of the current kernel code",
                 "algorithmic_bytes_per_launch": alg[dom],
-                "duration": (f"mean of {reps * R} back-to-back launches of the kernel alone (graph replays over "
-                             f"the {R} rotating sets), CUDA events on its stream")}
-
-    cpu = None
-    if not args.no_cpu_baseline:
-        threads = host_threads()
-        # About 20 s of CPU work (threads x wall seconds): a row sample of the
-        # workload, its oracle step repeated while the whole tensor is too
-        # small to fill the budget.
-        budget = max(1.0, 20.0 / threads)
-        srows = sample_rows_for(w, block, P, threads, budget)
-        xs = x_host_bits[:srows]
-        times = [oracle_step_time(xs, block, P, threads)]
-        while sum(times) < budget:
-            times.append(oracle_step_time(xs, block, P, threads))
-        t_cpu = sum(times) / len(times)
-        # The same oracle on one core, on a sample of about 2 s.
-        rows1 = sample_rows_for(w, block, P, 1, 2.0)
-        t1 = oracle_step_time(x_host_bits[:rows1], block, P, 1)
-        cpu = {"value": 6.0 * xs.size / t_cpu / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"rows [0, {srows}) of the {rows}x{hidden} tensor: {len(times)} oracle step(s) "
-                         f"(compress, reduce of {P} row-slices, decompress), block ranges split over "
-                         f"{threads} threads, mean time per step",
-               "seconds": sum(times),
-               "single_core": {"value": 6.0 * rows1 * hidden / t1 / 1e9, "unit": UNIT, "cores": 1,
-                               "sample": f"rows [0, {rows1}): one oracle step on one thread"},
-               "cpu_model": cpu_model(), "compiler": oracle_build_info()}
+                "duration": (f"mean of {solo[dom]['launches']} back-to-back launches of the kernel alone (graph "
+                             f"replays over the {R} rotating sets), CUDA events on its stream")}
 
     line = {
         "metric": METRIC,
-        "value": whole_job_gbs(world, 6.0 * n, ms_step),
+        "value": value,
         "unit": UNIT,
         "n_gpus": world,
         "steps": K,
@@ -680,8 +699,9 @@ def run_taco(args, rank, world):
         "data": "synthetic",
         "config": {"workload": w.name, "rows": rows, "hidden": hidden, "block": block, "reduce_shards": P,
                    "variant": args.variant, "code": args.code,
+                   "value": "2 x 2N bytes of bf16 input (compressed and decompressed) over the summed mean "
+                            "launch times of compress and decompress, each timed alone back to back",
                    "step": "compress + reduce_shards(P row-slices of the packed tensor) + decompress",
-                   "bytes_per_step": "6N: 2N compressed + 2N logical bf16 of the reduced segments + 2N decompressed",
                    "l2": (f"no flush; inputs larger than L2: {R} rotating buffer sets of {set_bytes / 1e6:.1f} MB "
                           f"(L2 {l2 / 1e6:.0f} MB); step k compresses set k, reduces set k-2, decompresses "
                           f"set k-3; graph replays (one graph per R steps, a branch per kernel kind with edges "
@@ -689,10 +709,15 @@ def run_taco(args, rank, world):
                           f"boundaries), one CUDA-event pair around the K steps"),
                    "buffer_sets": R,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "step": {"ms": ms_step, "gbs_6n": whole_job_gbs(world, 6.0 * n, ms_step),
+                 "what": "the K timed steps: 6N bytes per step (2N compressed + 2N logical bf16 of the reduced "
+                         "segments + 2N decompressed) over the step time"},
         "ops": ops,
-        "ops_sum_ms": sum(avg_ms.values()),
-        "quality": {"rel_l2_round_trip": rel_l2},
+        "ops_sum_ms": sum(solo_ms.values()),
+        "blocks": blocks,
         "reduce_full_shards": full_reduce,
+        "quality": {"rel_l2_round_trip": rel_l2},
+        "parity": parity,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -703,6 +728,112 @@ def run_taco(args, rank, world):
         "gpu": props.name,
     }
     print(json.dumps(line), flush=True)
+
+
+def time_solo(graphs: dict, stream, R: int, K: int, dev) -> dict:
+    """Each kernel alone: its graph of R back-to-back launches over the
+    rotating sets, replayed; events split the replays into G groups.  Per
+    kernel: the mean over all launches (ms), the median and minimum of the
+    groups' per-launch means, MAX over ranks."""
+    import torch
+    reps = max(4, min(250, (20 * K) // (R * 10)))
+    G = min(10, reps)
+    reps = reps // G * G
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, g in graphs.items():
+            for _ in range(2):
+                g.replay()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(G + 1)]
+            evs[0].record(stream)
+            for j in range(G):
+                for _ in range(reps // G):
+                    g.replay()
+                evs[j + 1].record(stream)
+            stream.synchronize()
+            per = [evs[j].elapsed_time(evs[j + 1]) / (reps // G * R) for j in range(G)]
+            t = max_over_ranks([evs[0].elapsed_time(evs[G]) / (reps * R), statistics.median(per), min(per)],
+                               device=dev)
+            out[name] = {"ms": t[0], "median": t[1], "min": t[2], "launches": reps * R, "groups": G}
+    return out
+
+
+def time_full_shard_reduce(taco, wf, block, scheme, stream, dev, capture, peak):
+    """The reduce of P full-size packed shards (the P-seed workload: each shard
+    its own seeded tensor, compressed on the GPU), back-to-back graph
+    replays."""
+    import torch
+    Pf = len(wf.seeds)
+    rows, hidden = wf.rows, wf.hidden
+    n = rows * hidden
+    nbytes = taco.compressed_bytes(rows, hidden, block)
+    full = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(Pf)]
+    full_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for p_, sd in enumerate(wf.seeds):
+            xf = torch.from_numpy(wf.tensor(seed=sd).view(np.int16)).view(torch.bfloat16).to(dev).view(rows, hidden)
+            taco.compress(xf, block, out=full[p_], stream=stream, **scheme)
+            stream.synchronize()
+            del xf
+        g_full = capture(lambda: taco.reduce_shards(full, rows, hidden, block, out=full_out, stream=stream,
+                                                    **scheme))
+        for _ in range(3):
+            g_full.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps_f = 50
+        a.record(stream)
+        for _ in range(reps_f):
+            g_full.replay()
+        b.record(stream)
+        stream.synchronize()
+    ms_f = max_over_ranks([a.elapsed_time(b) / reps_f], device=dev)[0]
+    alg_f = (Pf + 1) * nbytes
+    return {"workload": wf.name, "ms": ms_f, "shards": Pf, "block": block, "algorithmic_bytes": alg_f,
+            "hbm_gbs": alg_f / ms_f / 1e6, "frac_of_measured_hbm": alg_f / ms_f / 1e6 / peak,
+            "frac_of_nominal_8tbs": alg_f / ms_f / 1e6 / 8000.0, "logical_bf16_gbs": Pf * 2 * n / ms_f / 1e6,
+            "what": f"reduce of {Pf} full-size packed [{rows} x {hidden}] shards (seeds {list(wf.seeds)}), "
+                    f"back-to-back graph replays, the same input every replay"}
+
+
+def parity_against_oracle(taco, run, x_bits, block, P, scheme, stream, dev) -> dict:
+    """Parity statistics of the GPU kernels against the oracle's outputs of
+    one timed oracle pass (`run`, from oracle_op_times) on the same sample
+    rows: the GPU's records against the oracle's, the GPU's decode of the
+    oracle's records, and the GPU's reduce of the oracle's P row-slices (the
+    stats of tests/parity.py, reported, not asserted)."""
+    import torch
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import bf16_to_f64, exact_compress_quantities
+    from parity import compare_decoded, compare_records, reduce_exact_u
+    if scheme["variant"] != "ash_ds" or scheme["code"] != "e4m3":
+        return None
+    rows, hidden = x_bits.shape
+    nblk = x_bits.size // block
+    rec = block + 8
+    seg_rows = rows // P
+    seg_bytes = seg_rows * hidden // block * rec
+    with torch.cuda.stream(stream):
+        xd = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).to(dev)
+        got = taco.compress(xd, block, stream=stream).cpu().numpy()
+        ref_dev = torch.from_numpy(run["packed"]).to(dev)
+        y = taco.decompress(ref_dev, rows, hidden, block, stream=stream)
+        segs = [ref_dev[p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)]
+        red = taco.reduce_shards(segs, seg_rows, hidden, block, stream=stream).cpu().numpy()
+        y_np = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
+    _, _, u, _ = exact_compress_quantities(bf16_to_f64(x_bits.reshape(-1)), block)
+    c = compare_records(got, run["packed"], block, check=False, u_exact=u)
+    segs_np = [run["packed"][p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)]
+    r = compare_records(red, run["reduced"], block, check=False, u_exact=reduce_exact_u(segs_np, block))
+    d = compare_decoded(y_np, run["y"], block, check=False)
+    keep = ("code_mismatch_frac", "code_mismatches", "tie_mismatches", "code_max_step", "alpha_max_rel",
+            "s_max_rel", "s_zero_mismatch")
+    return {"sample_blocks": nblk,
+            "compress": {k: c[k] for k in keep},
+            "reduce": {k: r[k] for k in keep},
+            "decompress": {"bf16_mismatch_frac": d["mismatch_frac"], "beyond_one_step": d["bad"]},
+            "bar": "scales 1e-6 relative; codes identical except <= 1e-4 of elements (+ rounding ties the "
+                   "oracle itself rounds away from the exact value), one step apart; decoded bf16 within one "
+                   "step where FP32 noise of the block scale reaches a midpoint"}
 
 
 def main():

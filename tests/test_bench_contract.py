@@ -35,6 +35,11 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert cb["cpu_model"] and cb["compiler"].startswith("gcc -O2")
+    # The metric: 2 x 2n bytes of bf16 input over the compress + decompress time.
+    n = d["config"]["sample_rows"] * d["config"]["hidden"]
+    ops = d["ops_ms"]
+    assert abs(d["value"] - 4.0 * n / ((ops["compress"] + ops["decompress"]) * 1e-3) / 1e9) <= 1e-9 * d["value"]
+    assert abs(d["ms_per_step"] - sum(ops.values())) <= 1e-9 * d["ms_per_step"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0

@@ -3,7 +3,8 @@
 * No source of the package (Python, CUDA, headers) imports or names the
   oracle module; importing the package loads no oracle module.
 * bench.py uses the oracle only in its timing of the oracle itself (the CPU
-  baseline and the reference arm), never in the GPU arm.
+  baseline and the reference arm) and in the parity statistics taken from
+  that timed oracle pass, never in the GPU arm's timed work.
 * With the CUDA library missing, loading it and every call raise.
 """
 import ast
@@ -49,8 +50,10 @@ def test_bench_uses_the_oracle_only_to_time_it():
     for node in top:
         names = [a.name for a in node.names] if isinstance(node, ast.Import) else [node.module or ""]
         assert not any(n == "oracle" or n.startswith("oracle.") for n in names), "module-level oracle import"
-    assert sorted(owners) == ["oracle_build_info", "oracle_step_time"], owners
-    timing = {"oracle_step_time", "sample_rows_for", "oracle_build_info"}
+    assert sorted(owners) == ["oracle_build_info", "oracle_op_times"], owners
+    # parity_against_oracle reads the tests' parity helpers (which load the
+    # oracle): it counts as oracle use too.
+    timing = {"oracle_op_times", "sample_rows_for", "oracle_build_info", "parity_against_oracle"}
     callers = {fn.name for fn in ast.walk(tree) if isinstance(fn, ast.FunctionDef)
                for node in ast.walk(fn) if isinstance(node, ast.Call)
                and getattr(node.func, "id", None) in timing}
