@@ -804,7 +804,7 @@ def parity_against_oracle(taco, run, x_bits, block, P, scheme, stream, dev) -> d
     import torch
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from helpers import bf16_to_f64, exact_compress_quantities
-    from parity import compare_decoded, compare_records, reduce_exact_u
+    from parity import compare_decoded, compare_records, exact_compress_scales, exact_reduce_scales, reduce_exact_u
     if scheme["variant"] != "ash_ds" or scheme["code"] != "e4m3":
         return None
     rows, hidden = x_bits.shape
@@ -821,19 +821,23 @@ def parity_against_oracle(taco, run, x_bits, block, P, scheme, stream, dev) -> d
         red = taco.reduce_shards(segs, seg_rows, hidden, block, stream=stream).cpu().numpy()
         y_np = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
     _, _, u, _ = exact_compress_quantities(bf16_to_f64(x_bits.reshape(-1)), block)
-    c = compare_records(got, run["packed"], block, check=False, u_exact=u)
+    c = compare_records(got, run["packed"], block, check=False, u_exact=u,
+                        scales_exact=exact_compress_scales(x_bits.reshape(-1), block))
     segs_np = [run["packed"][p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)]
-    r = compare_records(red, run["reduced"], block, check=False, u_exact=reduce_exact_u(segs_np, block))
+    r = compare_records(red, run["reduced"], block, check=False, u_exact=reduce_exact_u(segs_np, block),
+                        scales_exact=exact_reduce_scales(segs_np, block))
     d = compare_decoded(y_np, run["y"], block, check=False)
-    keep = ("code_mismatch_frac", "code_mismatches", "tie_mismatches", "code_max_step", "alpha_max_rel",
-            "s_max_rel", "s_zero_mismatch")
+    keep = ("code_mismatch_frac", "code_mismatches", "mismatch_budget", "tie_mismatches", "code_max_step",
+            "alpha_max_rel", "s_max_rel", "alpha_max_rel_vs_ref", "s_max_rel_vs_ref", "scales_closer_to_exact",
+            "s_zero_mismatch")
     return {"sample_blocks": nblk,
             "compress": {k: c[k] for k in keep},
             "reduce": {k: r[k] for k in keep},
             "decompress": {"bf16_mismatch_frac": d["mismatch_frac"], "beyond_one_step": d["bad"]},
-            "bar": "scales 1e-6 relative; codes identical except <= 1e-4 of elements (+ rounding ties the "
-                   "oracle itself rounds away from the exact value), one step apart; decoded bf16 within one "
-                   "step where FP32 noise of the block scale reaches a midpoint"}
+            "bar": "scales 1e-6 relative (or within 1e-6 of the real-arithmetic value and closer to it than the "
+                   "oracle's); codes identical except <= 1e-4 of elements (+ twice the rounding ties the oracle "
+                   "itself rounds away from the exact value), one step apart; decoded bf16 within one step where "
+                   "FP32 noise of the block scale reaches a midpoint"}
 
 
 def main():

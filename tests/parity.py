@@ -68,6 +68,24 @@ def oracle_decompress_parallel(packed: np.ndarray, n: int, block: int, variant: 
     return out
 
 
+def oracle_reduce_parallel(shards, n: int, block: int, variant: int = 0, code: int = 0) -> np.ndarray:
+    """The oracle's reduce of P packed shards over disjoint block ranges on
+    several threads (blocks are independent, so this is the same function)."""
+    nblk = n // block
+    rec = block + 8
+    out = np.empty(nblk * rec, dtype=np.uint8)
+    chunk = max(1, -(-nblk // (4 * _threads())))
+
+    def run(b0):
+        b1 = min(nblk, b0 + chunk)
+        out[b0 * rec:b1 * rec] = oracle.reduce_shards([s[b0 * rec:b1 * rec] for s in shards], (b1 - b0) * block,
+                                                      block, variant, code)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(run, range(0, nblk, chunk)))
+    return out
+
+
 def near_midpoint(u_exact: np.ndarray, rel: float = 2e-6, code: int = 0) -> np.ndarray:
     """True where an exact (float64) pre-quantisation value lies within `rel`
     (relative) of a rounding midpoint between two code values, i.e. where the
@@ -140,8 +158,44 @@ def reduce_exact_u(shard_packed, block: int, variant: int = 0, code: int = 0) ->
     return np.where(m > 0, qmax * W / np.where(m > 0, m, 1.0), 0.0)
 
 
+def exact_compress_scales(x_bf16: np.ndarray, block: int, variant: int = 0, code: int = 0):
+    """alpha and s of every block in real arithmetic (float64) from the bf16
+    input: Eqs. (6)-(7) and (9), alpha cancelling out of the codes."""
+    from helpers import hadamard
+    G = bf16_to_f64(x_bf16).reshape(-1, block)
+    qmax = CODE_QMAX[code]
+    ones = np.ones(G.shape[0])
+    alpha = 1.0 / np.sqrt((G * G).mean(axis=1) + float(np.float32(1e-30)))
+    if variant == 2:
+        return ones, np.abs(G).max(axis=1) / qmax
+    ymax = np.abs(G @ hadamard(block).T).max(axis=1)
+    if variant == 3:
+        return alpha, ones
+    a = alpha if variant == 0 else ones
+    return a, a * ymax / (np.sqrt(block) * qmax)
+
+
+def exact_reduce_scales(shard_packed, block: int, variant: int = 0, code: int = 0):
+    """alpha' and s' of every block of the shard reduction in real arithmetic
+    (float64) from the shards' records: with W = sum_p q_p s_p / alpha_p the
+    exact sum of the decoded shards is (1/sqrt B) H W (W itself for DS only),
+    so mean(S^2) = |W|^2 / B and max|Z| = alpha' max|W|."""
+    table = decode_table(code)
+    W = 0.0
+    for p in shard_packed:
+        c, a, s = records(p, block)
+        W = W + table[c] * (s / a)[:, None]
+    qmax = CODE_QMAX[code]
+    ones = np.ones(W.shape[0])
+    alpha = 1.0 / np.sqrt((W * W).sum(axis=1) / block + float(np.float32(1e-30)))
+    if variant == 3:
+        return alpha, ones
+    a = alpha if variant == 0 else ones
+    return a, a * np.abs(W).max(axis=1) / qmax
+
+
 def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = True,
-                    u_exact: np.ndarray | None = None, code: int = 0) -> dict:
+                    u_exact: np.ndarray | None = None, code: int = 0, scales_exact=None) -> dict:
     """Compares packed records (uint8 arrays) from two implementations.
 
     Scales agree to 1e-6 relative (s = 0 blocks exactly).  Codes: every
@@ -161,7 +215,15 @@ def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = 
         noise in either implementation; they may differ by more than one
         grid step, and are not counted against the budget, but their decoded
         values may differ by at most 2 * NOISE_REL of the block's largest
-        |u| (what either implementation's FP32 order can produce there)."""
+        |u| (what either implementation's FP32 order can produce there).
+
+    With `scales_exact` (alpha and s of every block in real arithmetic), a
+    block whose scales differ from the reference's by more than 1e-6 still
+    passes if they are within 1e-6 of the exact values and closer to them
+    than the reference's: the reference's binary32 evaluation of Eqs. (6)-(9)
+    (one or two explicit rotations, P decoded shards summed) can itself lie
+    more than 1e-6 from the real value where shards cancel.  Such blocks are
+    counted (`scales_closer_to_exact`)."""
     cg, ag, sg = records(got, block)
     cr, ar, sr = records(ref, block)
     d = code_step_distance(cg, cr, code)
@@ -181,8 +243,24 @@ def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = 
         umax = block_max(u, block)
         ref_tie_flips = int((tie & ~noise & (vr != exact_values(u, code))).sum())
     nz = sr > 0
-    alpha_rel = float(np.max(np.abs(ag / ar - 1))) if ar.size else 0.0
-    s_rel = float(np.max(np.abs(sg[nz] / sr[nz] - 1))) if nz.any() else 0.0
+    a_dev = np.abs(ag / ar - 1) if ar.size else np.zeros(0)
+    s_dev = np.where(nz, np.abs(sg / np.where(nz, sr, 1.0) - 1), 0.0)
+    a_raw = float(np.max(a_dev)) if a_dev.size else 0.0
+    s_raw = float(np.max(s_dev)) if s_dev.size else 0.0
+    closer = 0
+    if scales_exact is not None:
+        ae, se = (np.asarray(v, dtype=np.float64) for v in scales_exact)
+        snz = se > 0
+        ag_e, ar_e = np.abs(ag / ae - 1), np.abs(ar / ae - 1)
+        sg_e = np.where(snz, np.abs(sg / np.where(snz, se, 1.0) - 1), 0.0)
+        sr_e = np.where(snz, np.abs(sr / np.where(snz, se, 1.0) - 1), 0.0)
+        a_alt = (ag_e <= SCALE_RTOL) & (ar_e > ag_e)
+        s_alt = (sg_e <= SCALE_RTOL) & (sr_e > sg_e)
+        closer = int((((a_dev > SCALE_RTOL) & a_alt) | ((s_dev > SCALE_RTOL) & s_alt)).sum())
+        a_dev = np.where(a_alt, np.minimum(a_dev, ag_e), a_dev)
+        s_dev = np.where(s_alt, np.minimum(s_dev, sg_e), s_dev)
+    alpha_rel = float(np.max(a_dev)) if a_dev.size else 0.0
+    s_rel = float(np.max(s_dev)) if s_dev.size else 0.0
     budget = CODE_MISMATCH_MAX * n + 2 * ref_tie_flips
     counted = mism & ~noise
     stats = {
@@ -199,6 +277,9 @@ def compare_records(got: np.ndarray, ref: np.ndarray, block: int, check: bool = 
         "signed_zero_diffs": int(zero_sign.sum()),
         "alpha_max_rel": alpha_rel,
         "s_max_rel": s_rel,
+        "alpha_max_rel_vs_ref": a_raw,
+        "s_max_rel_vs_ref": s_raw,
+        "scales_closer_to_exact": closer,
         "s_zero_mismatch": int(((sg == 0) != (sr == 0)).sum()),
     }
     if check:

@@ -21,7 +21,8 @@ import torch
 import oracle
 import workloads
 from parity import (RELL2_ATOL, compare_decoded, compare_records, oracle_compress_parallel,
-                    oracle_decompress_parallel, rel_l2_bf16)
+                    oracle_decompress_parallel, oracle_reduce_parallel, reduce_exact_u, rel_l2_bf16,
+                    exact_compress_scales, exact_reduce_scales)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -80,7 +81,7 @@ def test_full_size_compress_decompress(taco, name, block):
     compare_records(block_rows(got, ids, block), oracle.compress(xs, block), block)
     # Every record of the tensor.
     ref = oracle_compress_parallel(x, block)
-    compare_records(got, ref, block)
+    compare_records(got, ref, block, scales_exact=exact_compress_scales(x, block))
     # Decompress in isolation: the GPU decodes the oracle's records, every element checked.
     y_ref = oracle_decompress_parallel(ref, x.size, block)
     y_dec = bits_of(taco.decompress(torch.from_numpy(ref).to(DEV), w.rows, w.hidden, block))
@@ -91,6 +92,31 @@ def test_full_size_compress_decompress(taco, name, block):
     # Whole-tensor reconstruction error against the oracle's.
     e_gpu, e_ref = rel_l2_bf16(y_gpu, x), rel_l2_bf16(y_ref, x)
     assert abs(e_gpu - e_ref) <= RELL2_ATOL, (e_gpu, e_ref)
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("block", [64, 128, 256])
+def test_full_size_row_slice_reduce(taco, block):
+    """The benchmark's reduce: the 8 row-slices of the packed [16384 x 8192]
+    tensor (here the oracle's records) reduced on the GPU in one call; every
+    reduced record against the oracle's reduce of the same slices.  Laplace
+    data with outliers: the slices' decoded values cancel in many blocks, which
+    tests the precision of the scales."""
+    w = workloads.WORKLOADS["large_16384x8192"]
+    P = 8
+    x = w.tensor().reshape(-1)
+    ref = oracle_compress_parallel(x, block)
+    seg_rows = w.rows // P
+    seg_bytes = taco.compressed_bytes(seg_rows, w.hidden, block)
+    segs = [ref[p * seg_bytes:(p + 1) * seg_bytes] for p in range(P)]
+    out = taco.reduce_shards([torch.from_numpy(s).to(DEV) for s in segs], seg_rows, w.hidden, block)
+    got = out.cpu().numpy()
+    assert taco.device_status() == 0
+    red = oracle_reduce_parallel(segs, seg_rows * w.hidden, block)
+    st = compare_records(got, red, block, u_exact=reduce_exact_u(segs, block),
+                         scales_exact=exact_reduce_scales(segs, block))
+    assert st["blocks"] == seg_rows * w.hidden // block
+    del out
     torch.cuda.empty_cache()
 
 
@@ -141,7 +167,7 @@ def test_full_size_shard_reduce(taco):
     with ThreadPoolExecutor(16) as ex:
         list(ex.map(run, range(0, nblk, chunk)))
     # Every reduced record of the GPU against the oracle's reduce of the same shards.
-    compare_records(out_np, red_ref, block)
+    compare_records(out_np, red_ref, block, scales_exact=exact_reduce_scales(ref_shards, block))
     # The GPU decodes the oracle's reduced records: every element.
     y_dec = bits_of(taco.decompress(torch.from_numpy(red_ref).to(DEV), w.rows, w.hidden, block))
     compare_decoded(y_dec, y_ref, block)

@@ -21,7 +21,7 @@ import oracle
 import workloads
 from helpers import bf16_to_f64, exact_compress_quantities, records
 from near_zero import CODE_QMAX, near_zero_blocks
-from parity import compare_decoded, compare_records, reduce_exact_u
+from parity import compare_decoded, compare_records, exact_reduce_scales, reduce_exact_u
 
 pytestmark = pytest.mark.gpu
 
@@ -105,7 +105,8 @@ def test_near_zero_reduce(taco, B, code):
         got = taco.reduce_shards([torch.from_numpy(s).to(DEV) for s in shards], nb, B, B, code=code).cpu().numpy()
         cg, _, sg = records(got, B)
         assert no_nan_codes(cg, code)
-        compare_records(got, ref, B, code=code, u_exact=reduce_exact_u(shards, B, 0, code))
+        compare_records(got, ref, B, code=code, u_exact=reduce_exact_u(shards, B, 0, code),
+                        scales_exact=exact_reduce_scales(shards, B, 0, code))
     # A shard and its negation cancel to the all-zero record.
     assert np.all(cg == 0) and np.all(sg == 0)
     assert taco.device_status() == 0

@@ -9,7 +9,7 @@ import torch
 import oracle
 import workloads
 from helpers import hadamard, records
-from parity import (RELL2_ATOL, compare_decoded, compare_records, oracle_compress_parallel,
+from parity import (RELL2_ATOL, compare_decoded, compare_records, exact_reduce_scales, oracle_compress_parallel,
                     oracle_decompress_parallel, reduce_exact_u, rel_l2_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -88,7 +88,8 @@ def test_reduce_parity(taco, block, P):
     ref = oracle.reduce_shards(packed, xs[0].size, block)
     got = taco.reduce_shards([u8_dev(p) for p in packed], rows, hidden, block)
     torch.cuda.synchronize()
-    compare_records(got.cpu().numpy(), ref, block, u_exact=reduce_exact_u(packed, block))
+    compare_records(got.cpu().numpy(), ref, block, u_exact=reduce_exact_u(packed, block),
+                    scales_exact=exact_reduce_scales(packed, block))
 
 
 def test_reduce_repeated_and_negated_shards(taco):

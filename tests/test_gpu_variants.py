@@ -17,7 +17,7 @@ import torch
 import oracle
 import workloads
 from helpers import bf16_to_f64, records
-from parity import (RELL2_ATOL, compare_decoded, compare_records, oracle_compress_parallel,
+from parity import (RELL2_ATOL, compare_decoded, compare_records, exact_reduce_scales, oracle_compress_parallel,
                     oracle_decompress_parallel, reduce_exact_u, rel_l2_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -89,7 +89,7 @@ def test_reduce(taco, B, variant, code):
     got = taco.reduce_shards([torch.from_numpy(s).cuda() for s in shards], rows, hidden, B,
                              variant=variant, code=code).cpu().numpy()
     u = reduce_exact_u(shards, B, variant, code)
-    compare_records(got, ref, B, u_exact=u, code=code)
+    compare_records(got, ref, B, u_exact=u, code=code, scales_exact=exact_reduce_scales(shards, B, variant, code))
     assert taco.device_status() == 0
 
 
@@ -107,7 +107,7 @@ def test_reduce_eight_shards(taco, B, variant, code):
     got = taco.reduce_shards([torch.from_numpy(s).cuda() for s in shards], rows, hidden, B,
                              variant=variant, code=code).cpu().numpy()
     u = reduce_exact_u(shards, B, variant, code)
-    compare_records(got, ref, B, u_exact=u, code=code)
+    compare_records(got, ref, B, u_exact=u, code=code, scales_exact=exact_reduce_scales(shards, B, variant, code))
     assert taco.device_status() == 0
 
 

@@ -161,3 +161,43 @@ def test_noise_zone_differences_are_bounded_by_value():
     c[1, 7] = big
     with pytest.raises(AssertionError):
         compare_records(got, ref, B, u_exact=u, code=code)
+
+
+def test_exact_scales_agree_with_the_oracle():
+    """The real-arithmetic scales used by the rule against the oracle's binary32
+    ones: compress (every variant) and a 3-shard reduce."""
+    from parity import exact_compress_scales, exact_reduce_scales
+    from helpers import records
+    bits = workloads.generate("student_t_channels", 32, 1024, 5).reshape(-1)
+    for variant in range(4):
+        for code in (0, 1, 2):
+            ref = oracle.compress(bits, B, variant, code)
+            _, a, s = records(ref, B)
+            ae, se = exact_compress_scales(bits, B, variant, code)
+            assert np.max(np.abs(a / ae - 1)) < 1e-6 and np.max(np.abs(s / se - 1)) < 1e-6, (variant, code)
+    shards = [oracle.compress(workloads.generate("student_t_channels", 32, 1024, p).reshape(-1), B) for p in range(3)]
+    _, a, s = records(oracle.reduce_shards(shards, 32 * 1024, B), B)
+    ae, se = exact_reduce_scales(shards, B)
+    assert np.max(np.abs(a / ae - 1)) < 2e-6 and np.max(np.abs(s / se - 1)) < 2e-6
+
+
+def test_scale_closer_to_exact_passes_and_otherwise_fails(case):
+    from parity import exact_compress_scales
+    bits, ref = case
+    ae, se = exact_compress_scales(bits, B)
+    got = ref.copy()
+    rec = got.reshape(-1, B + 8)
+    ref_rec = ref.reshape(-1, B + 8)
+    # Block 3: the reference's alpha moved 3e-6 off the exact value; the
+    # tested alpha is the exact value rounded to binary32.
+    bad_ref = ref.copy().reshape(-1, B + 8)
+    bad_ref[3, B:B + 4] = np.float32(ae[3] * (1 + 3e-6)).reshape(1).view(np.uint8)
+    rec[3, B:B + 4] = np.float32(ae[3]).reshape(1).view(np.uint8)
+    st = compare_records(got, bad_ref.reshape(-1), B, scales_exact=(ae, se))
+    assert st["scales_closer_to_exact"] == 1 and st["alpha_max_rel_vs_ref"] > 2e-6
+    with pytest.raises(AssertionError):
+        compare_records(got, bad_ref.reshape(-1), B)            # without the exact values
+    # Tested alpha 3e-6 off both: fails.
+    rec[3, B:B + 4] = np.float32(ae[3] * (1 - 3e-6)).reshape(1).view(np.uint8)
+    with pytest.raises(AssertionError):
+        compare_records(got, bad_ref.reshape(-1), B, scales_exact=(ae, se))
