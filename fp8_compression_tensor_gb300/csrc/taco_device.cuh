@@ -307,7 +307,8 @@ __device__ __forceinline__ void int8x4_to_float(uint32_t x, float2 &q0, float2 &
 
 // Codes of four values, first value in the low byte.  INT8 rounds to the
 // nearest integer, ties to even; the callers keep |u| <= 127 (u = Q_max y /
-// max|y| rounds to at most 127, and a direct cast has |u| <= sqrt(B) <= 16).
+// max|y| rounds to at most 127, and a direct cast has |u| <= sqrt(B) <= sqrt(512),
+// about 22.6).
 __device__ __forceinline__ uint32_t encode4(int code, float a, float b, float c, float d)
 {
     if (code == 0)
