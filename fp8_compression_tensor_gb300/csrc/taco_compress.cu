@@ -397,12 +397,13 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             const uint32_t rec_block = sbase + Lay::kOffOut + ob * Lay::kOutBytes + blk * Lay::kRec;
             const uint32_t rec = rec_block + part * 128;
 
+            const float srcp = DS_ONLY ? __frcp_rn(s) : 0.f;   // DS only: 1/s, correctly rounded
             // Pass 2: codes (Eq. 10) two per cvt, 32 per chunk.  `scaled`:
             // every value is first multiplied by `pre` (exact).
             auto code_pass = [&](float kk, auto scaled, float pre) {
                 const float2 k2 = make_float2(kk, kk);
-                // The rare scaled pass and the divisions of DS only stay
-                // compact (one chunk at a time).
+                // The rare scaled pass and DS only stay compact (one chunk at
+                // a time).
 #pragma unroll((decltype(scaled)::value || DS_ONLY) ? 1 : Lay::kAccCols / 32)
                 for (int c = 0; c < Lay::kAccCols / 32; c++) {
                     uint32_t r[32];
@@ -423,12 +424,22 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                                 mul2(make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), k2);
                             cw[j] = encode4(scheme.code, u0.x, u0.y, u1.x, u1.y);
                         }
-                    } else {
+                    } else if (s >= kDivFastMin) {
                         // DS only: the unrotated block's values G / s with s =
-                        // max|G| / Q_max, by IEEE division as Eq. (10) writes it
+                        // max|G| / Q_max, correctly rounded as Eq. (10) writes it
                         // (ratios of bf16 values land exactly on rounding
                         // midpoints often, and there only the quotient itself
                         // decides the code as the method does).
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            const float2 u0 = div2_by(
+                                make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), s, srcp);
+                            const float2 u1 = div2_by(
+                                make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), s, srcp);
+                            cw[j] = encode4(scheme.code, u0.x, u0.y, u1.x, u1.y);
+                        }
+                    } else {
+                        // DS only with a tiny (or zero) s: IEEE division.
 #pragma unroll
                         for (int j = 0; j < 8; j++) {
                             float u[4];

@@ -32,6 +32,8 @@ constexpr float kTinyValue = 0x1p-100f;
 constexpr float kTinySum = 0x1p-80f;
 constexpr float kTinyUp = 0x1p64f;
 constexpr float kTinyDown = 0x1p-64f;
+// Smallest divisor for which div2_by (reciprocal and one correction) is used.
+constexpr float kDivFastMin = 0x1p-100f;
 
 // Fault flag bits written when a kernel gives up waiting.
 constexpr uint32_t kFaultCompress = 1u;
@@ -240,6 +242,21 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b)
 
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// y / s rounded to nearest for the two values of y, given rcp = 1/s
+// correctly rounded (__frcp_rn): the quotient q = y * rcp is corrected once,
+// q + (y - q s) * rcp, the residual y - q s being exact in a fused
+// multiply-add.  This gives the correctly rounded quotient (the classic
+// correction step for a correctly rounded reciprocal; the test suite checks it
+// against exact rational division on random and on exact quotients).  Valid for
+// a normal s with 2^-100 <= s < 2^100; callers divide exactly otherwise.
+__device__ __forceinline__ float2 div2_by(float2 y, float s, float rcp)
+{
+    const float2 r2 = make_float2(rcp, rcp), s2 = make_float2(s, s);
+    const float2 q = __fmul2_rn(y, r2);
+    const float2 e = __ffma2_rn(make_float2(-q.x, -q.y), s2, y);
+    return __ffma2_rn(e, r2, q);
+}
 
 __device__ __forceinline__ float max3(float a, float b, float c)
 {

@@ -391,9 +391,18 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                     const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
                     o[j] = encode4(CODE, u0.x, u0.y, u1.x, u1.y);
                 }
-            } else if (wmax > 0.f) {
+            } else if (ds_only && sc >= kDivFastMin) {
                 // DS only: W is the sum of the decoded shards itself (no
-                // rotation, alpha = 1); its codes are W / s' by IEEE division.
+                // rotation, alpha = 1); its codes are W / s' correctly rounded.
+                const float srcp = __frcp_rn(sc);
+#pragma unroll
+                for (int j = 0; j < LW; j++) {
+                    const float2 u0 = div2_by(make_float2(w[4 * j], w[4 * j + 1]), sc, srcp);
+                    const float2 u1 = div2_by(make_float2(w[4 * j + 2], w[4 * j + 3]), sc, srcp);
+                    o[j] = encode4(CODE, u0.x, u0.y, u1.x, u1.y);
+                }
+            } else if (ds_only && wmax > 0.f) {
+                // DS only with a tiny s': IEEE division.
 #pragma unroll
                 for (int j = 0; j < LW; j++)
                     o[j] = encode4(CODE, __fdiv_rn(w[4 * j], sc), __fdiv_rn(w[4 * j + 1], sc),

@@ -243,9 +243,18 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_compress_kernel(const 
                 const float2 u1 = mul2(make_float2(v[4 * j + 2], v[4 * j + 3]), k2);
                 cw[j] = ymax > 0.f ? encode4(scheme.code, u0.x, u0.y, u1.x, u1.y) : 0u;
             }
-        } else {
-            // DS only: G / s by IEEE division, as Eq. (10) writes it (bf16
+        } else if (s >= kDivFastMin) {
+            // DS only: G / s correctly rounded, as Eq. (10) writes it (bf16
             // ratios often land exactly on rounding midpoints).
+            const float srcp = __frcp_rn(s);
+#pragma unroll
+            for (int j = 0; j < B / 4; j++) {
+                const float2 u0 = div2_by(make_float2(v[4 * j], v[4 * j + 1]), s, srcp);
+                const float2 u1 = div2_by(make_float2(v[4 * j + 2], v[4 * j + 3]), s, srcp);
+                cw[j] = encode4(scheme.code, u0.x, u0.y, u1.x, u1.y);
+            }
+        } else {
+            // DS only with a tiny (or zero) s: IEEE division.
 #pragma unroll
             for (int j = 0; j < B / 4; j++) {
                 float u[4];
