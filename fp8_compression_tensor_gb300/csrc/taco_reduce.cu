@@ -74,28 +74,36 @@ constexpr int kRSchedAhead = TACO_REDUCE_SCHED_AHEAD;   // cancel requests in fl
 // (and the end marks of kGroups items) is reused only after its readers are done.
 static_assert(kTileRing >= kMaxStages + kGroups, "published-tile slot reused too early");
 
-template <int B>
+// MUL: passes of the consumer group over a tile.  A kernel for few shards
+// (2 or 4) takes tiles of MUL = 8 / P times as many blocks, so that a stage
+// still holds about 35 KB of records in long runs (the copies of 2 shards at
+// the 8-shard tile size moved 42% of the bandwidth).
+template <int B, int MUL = 1>
 struct ReduceLayout {
     // Codes per thread: kLaneCodes, or 16 where a block would span more than a
     // warp (its energy and maximum are reduced with shuffles inside one warp).
     static constexpr int kLC = B / kLaneCodes > 32 ? 16 : kLaneCodes;
     static constexpr int kLW = kLC / 4;                      // 32-bit words of a thread's codes
-    // Blocks per tile: one per kLpb consumer threads, halved until two stages of
-    // kMaxShards record runs fit the ring (the threads beyond it stay idle).
-    static constexpr int tile_blocks()
+    // Shards a kernel of this layout takes at most.
+    static constexpr int kMaxP = MUL > 1 ? 8 / MUL : kMaxShards;
+    // Blocks per consumer pass: one per kLpb consumer threads, halved until two
+    // stages of kMaxP record runs of a tile fit the ring (the threads beyond it
+    // stay idle).
+    static constexpr int pass_blocks()
     {
         int t = kConsumers * kLC / B;
-        while (t > 2 && 2 * kMaxShards * t * (B + 8) > kRingBytes)
+        while (t > 2 && 2 * kMaxP * MUL * t * (B + 8) > kRingBytes)
             t /= 2;
         return t;
     }
-    static constexpr int kT = tile_blocks();
+    static constexpr int kSub = pass_blocks();
+    static constexpr int kT = MUL * kSub;                    // blocks per tile
     static constexpr int kLpb = B / kLC;                     // threads per block
     static_assert(kLpb <= 32 && 32 % kLpb == 0, "a block's threads lie in one warp");
     static constexpr int kRec = B + 8;
     static constexpr int kRunBytes = kT * kRec;             // one shard's records of a tile
     static_assert(kT % 2 == 0 && kRunBytes % 16 == 0, "bulk copies need 16-byte multiples");
-    static_assert(kRingBytes >= 2 * kMaxShards * kRunBytes, "at least two stages at P = 16");
+    static_assert(kRingBytes >= 2 * kMaxP * kRunBytes, "at least two stages at the largest shard count");
     // Offsets from the 128-byte aligned base.
     static constexpr int kOffRing = 0;
     static constexpr int kOffSched = kOffRing + kRingBytes;           // 16-byte aligned
@@ -154,7 +162,8 @@ __device__ __forceinline__ uint2 ldg_u2(const uint8_t *p)
 template <int B, int CODE, int PFIX>
 __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const ReduceArgs args, uint32_t *fault)
 {
-    using Lay = ReduceLayout<B>;
+    constexpr int MUL = PFIX == 2 ? 4 : PFIX == 4 ? 2 : 1;
+    using Lay = ReduceLayout<B, MUL>;
     constexpr int T = Lay::kT;
     constexpr int kRec = Lay::kRec;
     constexpr int LC = Lay::kLC, LW = Lay::kLW;
@@ -277,10 +286,13 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             if (!mbar_wait_bounded(full_bar(s), (i / nst) & 1, fault, kFaultReduce))
                 break;
             const int nvalid = tile_valid(t);
-            const bool active = bl < nvalid;
-            const bool from_global = (nvalid & 1) && bl == nvalid - 1;   // not in the bulk copies
-            const int64_t blk = t * T + bl;
-            const uint32_t rec_s = sbase + Lay::kOffRing + s * stage_bytes + bl * kRec;
+#pragma unroll 1
+            for (int sub = 0; sub < MUL; sub++) {
+            const int blt = sub * Lay::kSub + bl;                          // block within the tile
+            const bool active = bl < Lay::kSub && blt < nvalid;
+            const bool from_global = (nvalid & 1) && blt == nvalid - 1;   // not in the bulk copies
+            const int64_t blk = t * T + blt;
+            const uint32_t rec_s = sbase + Lay::kOffRing + s * stage_bytes + blt * kRec;
 
             // W = sum_p q_p * (s_p / alpha_p) in shard order.  `scaled`: every
             // factor is formed 2^64 times larger (s_p 2^64 / alpha_p), and the
@@ -329,10 +341,12 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                 }
             };
             accumulate(std::false_type{});
-            // The stage is read: hand it back to the loader.
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty_bar(s));
+            if (sub == MUL - 1) {
+                // The stage is read: hand it back to the loader.
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty_bar(s));
+            }
 
             // Energy |W|^2 and max|W| over the block's threads.
             float e = 0.f, wmax = 0.f;
@@ -417,6 +431,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
                 if (part == 0)
                     *reinterpret_cast<uint2 *>(rec + B) = make_uint2(__float_as_uint(alpha), __float_as_uint(sc));
             }
+            }   // sub
         }
     }
 }
@@ -424,8 +439,9 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
 template <int B, int CODE, int PFIX = 0>
 KernelInfo info()
 {
-    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B, CODE, PFIX>), ReduceLayout<B>::kSmem,
-                      kRThreads, ReduceLayout<B>::kT, kRThreads / 32};
+    using Lay = ReduceLayout<B, PFIX == 2 ? 4 : PFIX == 4 ? 2 : 1>;
+    return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B, CODE, PFIX>), Lay::kSmem, kRThreads,
+                      Lay::kT, kRThreads / 32};
 }
 
 template <int CODE, int PFIX = 0>
@@ -445,8 +461,13 @@ KernelInfo info_for_block(int block)
 
 KernelInfo reduce_kernel_info(int block, int code, int num_shards)
 {
-    // The method's shard count (8) has kernels with the shard loop unrolled,
-    // for every code format and block size.
+    // Tensor-parallel degrees 2 and 4 (the owner reduces 2 or 4 segments)
+    // have kernels with the shard loop unrolled and longer tiles, for the
+    // method's E4M3 codes.
+    if (TACO_REDUCE_FIXED_P8 && code == 0 && (num_shards == 2 || num_shards == 4))
+        return num_shards == 2 ? info_for_block<0, 2>(block) : info_for_block<0, 4>(block);
+    // The 8-shard case has kernels with the shard loop unrolled, for every
+    // code format and block size.
     if (TACO_REDUCE_FIXED_P8 && num_shards == 8) {
         switch (code) {
         case 0: return info_for_block<0, 8>(block);

@@ -95,15 +95,15 @@ def test_full_size_compress_decompress(taco, name, block):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("block", [64, 128, 256])
-def test_full_size_row_slice_reduce(taco, block):
-    """The benchmark's reduce: the 8 row-slices of the packed [16384 x 8192]
+@pytest.mark.parametrize("block,P", [(64, 8), (128, 8), (256, 8), (128, 2), (128, 4)])
+def test_full_size_row_slice_reduce(taco, block, P):
+    """The benchmark's reduce: the P row-slices of the packed [16384 x 8192]
     tensor (here the oracle's records) reduced on the GPU in one call; every
-    reduced record against the oracle's reduce of the same slices.  Laplace
+    reduced record against the oracle's reduce of the same slices (P = 8, and
+    the 2- and 4-shard kernels).  Laplace
     data with outliers: the slices' decoded values cancel in many blocks, which
     tests the precision of the scales."""
     w = workloads.WORKLOADS["large_16384x8192"]
-    P = 8
     x = w.tensor().reshape(-1)
     ref = oracle_compress_parallel(x, block)
     seg_rows = w.rows // P

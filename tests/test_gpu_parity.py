@@ -75,7 +75,7 @@ def test_compress_decompress_parity(taco, rows, hidden, block, dist):
 
 
 @pytest.mark.parametrize("block", [64, 128, 256])
-@pytest.mark.parametrize("P", [1, 2, 5, 8, 16])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16])
 def test_reduce_parity(taco, block, P):
     """GPU reduce of the oracle's packed shards against the oracle's reduce.
     With two shards, exact rounding ties are common (u' = Q_max (q1 f1 + q2 f2) /
