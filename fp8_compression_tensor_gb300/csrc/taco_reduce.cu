@@ -78,11 +78,16 @@ static_assert(kTileRing >= kMaxStages + kGroups, "published-tile slot reused too
 // (2 or 4) takes tiles of MUL = 8 / P times as many blocks, so that a stage
 // still holds about 35 KB of records in long runs (the copies of 2 shards at
 // the 8-shard tile size moved 42% of the bandwidth).
-template <int B, int MUL = 1>
+// LCODES: codes per thread per shard (0: kLaneCodes).  The 16-shard kernel
+// takes 8, which halves its tiles so that five stages of 16 record runs fit
+// the ring instead of two.
+template <int B, int MUL = 1, int LCODES = 0>
 struct ReduceLayout {
-    // Codes per thread: kLaneCodes, or 16 where a block would span more than a
-    // warp (its energy and maximum are reduced with shuffles inside one warp).
-    static constexpr int kLC = B / kLaneCodes > 32 ? 16 : kLaneCodes;
+    // Codes per thread: LCODES or kLaneCodes, or 16 where a block would span
+    // more than a warp (its energy and maximum are reduced with shuffles inside
+    // one warp).
+    static constexpr int kLC0 = LCODES > 0 ? LCODES : kLaneCodes;
+    static constexpr int kLC = B / kLC0 > 32 ? 16 : kLC0;
     static constexpr int kLW = kLC / 4;                      // 32-bit words of a thread's codes
     // Shards a kernel of this layout takes at most.
     static constexpr int kMaxP = MUL > 1 ? 8 / MUL : kMaxShards;
@@ -163,7 +168,7 @@ template <int B, int CODE, int PFIX>
 __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const ReduceArgs args, uint32_t *fault)
 {
     constexpr int MUL = PFIX == 2 ? 4 : PFIX == 4 ? 2 : 1;
-    using Lay = ReduceLayout<B, MUL>;
+    using Lay = ReduceLayout<B, MUL, PFIX == 16 ? 8 : 0>;
     constexpr int T = Lay::kT;
     constexpr int kRec = Lay::kRec;
     constexpr int LC = Lay::kLC, LW = Lay::kLW;
@@ -439,7 +444,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
 template <int B, int CODE, int PFIX = 0>
 KernelInfo info()
 {
-    using Lay = ReduceLayout<B, PFIX == 2 ? 4 : PFIX == 4 ? 2 : 1>;
+    using Lay = ReduceLayout<B, PFIX == 2 ? 4 : PFIX == 4 ? 2 : 1, PFIX == 16 ? 8 : 0>;
     return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B, CODE, PFIX>), Lay::kSmem, kRThreads,
                       Lay::kT, kRThreads / 32};
 }
@@ -461,11 +466,14 @@ KernelInfo info_for_block(int block)
 
 KernelInfo reduce_kernel_info(int block, int code, int num_shards)
 {
-    // Tensor-parallel degrees 2 and 4 (the owner reduces 2 or 4 segments)
-    // have kernels with the shard loop unrolled and longer tiles, for the
-    // method's E4M3 codes.
+    // Tensor-parallel degrees 2, 4 and 16 (the owner reduces that many
+    // segments) have kernels with the shard loop unrolled, 2 and 4 with longer
+    // tiles, for the method's E4M3 codes.
     if (TACO_REDUCE_FIXED_P8 && code == 0 && (num_shards == 2 || num_shards == 4))
         return num_shards == 2 ? info_for_block<0, 2>(block) : info_for_block<0, 4>(block);
+    // 16 shards: the same with tiles half as long (two stages would fit otherwise).
+    if (TACO_REDUCE_FIXED_P8 && code == 0 && num_shards == 16)
+        return info_for_block<0, 16>(block);
     // The 8-shard case has kernels with the shard loop unrolled, for every
     // code format and block size.
     if (TACO_REDUCE_FIXED_P8 && num_shards == 8) {
