@@ -26,7 +26,8 @@ bf16 tensor compressed plus the bf16 tensor decompressed) over the sum of the
 two kernels' average launch durations.  The whole step (with the reduce) is
 reported under `step`; the same workload at the other block sizes under
 `blocks`; the reduce of 8 full-size [8192 x 5120] shards under
-`reduce_full_shards`.  The roofline object reports the dominant kernel's
+`reduce_full_shards`; the reduce of the tensor split into 2, 4 and 16 shards
+under `reduce_shard_counts`.  The roofline object reports the dominant kernel's
 algorithmic bytes per launch over its average duration against the measured
 HBM copy bandwidth.
 
@@ -538,6 +539,7 @@ def run_taco(args, rank, world):
     # of 8 full-size shards (the owner's local step on the P-seed workload).
     blocks = None
     full_reduce = None
+    shard_counts = None
     if not args.no_extras:
         blocks = {}
         for b in w.blocks:
@@ -567,6 +569,25 @@ def run_taco(args, rank, world):
             torch.cuda.empty_cache()
         full_reduce = time_full_shard_reduce(taco, workloads.WORKLOADS["shard_reduce_p8_8192x5120"], block, scheme,
                                              stream, dev, capture, peak)
+        # The reduce of the same packed tensor split into other shard counts
+        # (an owner's step at tensor-parallel degree 2, 4 and 16).
+        shard_counts = {}
+        for P2 in (2, 4, 16):
+            if P2 == P or rows % P2:
+                continue
+            sr2 = rows // P2
+            sb2 = taco.compressed_bytes(sr2, hidden, block)
+            outs2 = [torch.empty(sb2, dtype=torch.uint8, device=dev) for _ in range(R)]
+            segs2 = [[packs[r][p * sb2:(p + 1) * sb2] for p in range(P2)] for r in range(R)]
+            with torch.cuda.stream(stream):
+                for r in range(R):
+                    op_compress(r)
+                g2 = {"reduce": capture(lambda: [taco.reduce_shards(segs2[r], sr2, hidden, block, out=outs2[r],
+                                                                    stream=stream, **scheme) for r in range(R)])}
+            t2 = time_solo(g2, stream, R, K, dev)["reduce"]
+            shard_counts[str(P2)] = op_line("reduce", t2, (P2 + 1) * sb2, n)
+            del outs2, segs2, g2
+        torch.cuda.empty_cache()
     x, packed, reduced, y = xs[0], packs[0], reds[0], ys[0]
 
     # Reconstruction error of the round trip (paper Eq. 21), fp64 over the tensor.
@@ -716,6 +737,7 @@ def run_taco(args, rank, world):
         "ops_sum_ms": sum(solo_ms.values()),
         "blocks": blocks,
         "reduce_full_shards": full_reduce,
+        "reduce_shard_counts": shard_counts,
         "quality": {"rel_l2_round_trip": rel_l2},
         "parity": parity,
         "roofline": roofline,
