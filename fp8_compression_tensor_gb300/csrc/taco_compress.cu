@@ -38,11 +38,15 @@
 // Scales: m = sum y^2 / B^2 (Eq. 6), alpha = tau / sqrt(m + eps) (Eq. 7),
 // s = alpha * max|y| * (1/sqrt B) / Q_max (Eq. 9), codes of y * (Q_max / max|y|)
 // (Eq. 10, alpha cancels); equal to the literal order up to FP32 rounding.
+// Near zero (max|y| < 2^-100, where Q_max / max|y| can overflow) a warp codes
+// its rows again from 2^64 y, which keeps the roundings of the unscaled
+// formula.
 //
-// Ablations (Scheme): standard Hadamard + DS takes alpha = 1; DS only puts
-// the identity in place of H (y = G) with alpha = 1; ASH only stores s = 1
-// and converts Z = alpha y / sqrt(B) directly; E5M2 and INT8 codes use
-// Q_max = 57344 and 127.
+// Ablations (Scheme): standard Hadamard + DS takes alpha = 1; DS only (its
+// own instantiation, DS_ONLY) puts the identity in place of H (y = G) with
+// alpha = 1 and codes G / s correctly rounded, as Eq. (10) writes it; ASH
+// only stores s = 1 and converts Z = alpha y / sqrt(B) directly; E5M2 and
+// INT8 codes use Q_max = 57344 and 127.
 #include <cstring>
 #include <type_traits>
 

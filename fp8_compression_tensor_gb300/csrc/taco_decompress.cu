@@ -6,7 +6,9 @@
 // Y = A H^T (H symmetric) gives H q for every block at once: the codes are
 // the MMA's 8-bit operand (.kind::f8f6f4), H holds +-1 in E4M3, products are
 // exact and accumulate in FP32 in tensor memory.  G' = Y * (s / sqrt(B) / alpha)
-// per block is Eqs. (11)-(13) up to FP32 summation order.
+// per block is Eqs. (11)-(13) up to FP32 summation order.  Near zero the
+// factor would be subnormal: below 2^-100 it is formed 2^64 times larger and
+// the products are scaled back by 2^-64.
 //
 // Scheduling: one CTA per tile, one CTA per SM resident (shared memory); a
 // running CTA takes its own tile, then the tiles of CTAs it cancels before

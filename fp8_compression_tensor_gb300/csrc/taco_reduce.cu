@@ -9,8 +9,15 @@
 // mean(S^2) = |W|^2 / B, Z = alpha' R S = alpha' W, s' = alpha' max|W| / Q_max and
 // codes Cvt_FP8(Q_max W / max|W|).  The kernel computes exactly these, which
 // differ from decode-sum-encode with explicit rotations only by FP32 rounding.
+// Near zero (a block sum below 2^-80, where the factors s_p / alpha_p are
+// subnormal or zero in binary32) the block is summed again from global memory
+// with factors 2^64 s_p / alpha_p and its scales taken back by 2^-64.  DS only
+// has no rotation: W is the FP32 sum of the decoded shards itself, coded as
+// W / s' correctly rounded.
 //
-// Data movement.  A tile is T consecutive blocks (T = 4096 / B); its records
+// Data movement.  A tile is T consecutive blocks (T = 4096 / B for most shard
+// counts; 8/P times that for the 2- and 4-shard kernels, which take 8/P
+// passes per tile, and half of it for the 16-shard kernel); its records
 // are contiguous in every shard, T * (B + 8) bytes (a multiple of 16: T is
 // even).  The loader warp bulk-copies the tile's P record runs (lane p the
 // run of shard p) into one stage of a shared-memory ring (as many stages of
