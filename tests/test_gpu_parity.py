@@ -92,6 +92,23 @@ def test_reduce_parity(taco, block, P):
                     scales_exact=exact_reduce_scales(packed, block))
 
 
+@pytest.mark.parametrize("block", [32, 512])
+@pytest.mark.parametrize("P", [2, 4, 16])
+def test_reduce_parity_fixed_shard_counts(taco, block, P):
+    """The 2-, 4- and 16-shard kernels (tiles of 4x, 2x and 1/2x the usual
+    length) at the smallest and largest block, on a shape whose last tile is
+    partial and has an odd number of blocks."""
+    rows, hidden = 301, 3 * block          # 903 blocks
+    xs = [workloads.generate("student_t_channels", rows, hidden, seed=20 + p).reshape(-1) for p in range(P)]
+    packed = [oracle.compress(x, block) for x in xs]
+    ref = oracle.reduce_shards(packed, xs[0].size, block)
+    got = taco.reduce_shards([u8_dev(p) for p in packed], rows, hidden, block)
+    torch.cuda.synchronize()
+    compare_records(got.cpu().numpy(), ref, block, u_exact=reduce_exact_u(packed, block),
+                    scales_exact=exact_reduce_scales(packed, block))
+    assert taco.device_status() == 0
+
+
 def test_reduce_repeated_and_negated_shards(taco):
     block, rows, hidden = 128, 64, 512
     x = workloads.generate("laplace_outliers", rows, hidden, seed=3).reshape(-1)
