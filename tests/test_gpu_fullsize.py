@@ -177,3 +177,33 @@ def test_full_size_shard_reduce(taco):
     e_gpu = np.linalg.norm(yg - total) / nt
     e_ref = np.linalg.norm(yr - total) / nt
     assert abs(e_gpu - e_ref) <= RELL2_ATOL, (e_gpu, e_ref)
+
+
+SCHEMES = [(0, 1), (0, 2), (1, 0), (2, 0), (3, 0), (2, 1)]   # (variant, code): E5M2, INT8, plain Hadamard, DS only, ASH only
+
+
+@pytest.mark.parametrize("variant,code", SCHEMES)
+def test_full_size_ablation_schemes(taco, variant, code):
+    """The paper's ablations at the GPT-activation workload's full size
+    ([8192 x 4096], block 128): every record of the GPU's compress against the
+    oracle's, every element of the GPU's decode of the oracle's records, and
+    the round trip's RelL2."""
+    from test_gpu_variants import exact_u
+    w = workloads.WORKLOADS["gpt_activation_8192x4096"]
+    block = 128
+    x = w.tensor().reshape(-1)
+    xd = to_dev(x, w.rows, w.hidden)
+    got = taco.compress(xd, block, variant=variant, code=code).cpu().numpy()
+    ref = oracle_compress_parallel(x, block, variant, code)
+    compare_records(got, ref, block, code=code, u_exact=exact_u(x, block, variant, code),
+                    scales_exact=exact_compress_scales(x, block, variant, code))
+    y_ref = oracle_decompress_parallel(ref, x.size, block, variant, code)
+    y_dec = bits_of(taco.decompress(torch.from_numpy(ref).to(DEV), w.rows, w.hidden, block, variant=variant,
+                                    code=code))
+    compare_decoded(y_dec, y_ref, block)
+    y_gpu = bits_of(taco.decompress(torch.from_numpy(got).to(DEV), w.rows, w.hidden, block, variant=variant,
+                                    code=code))
+    assert abs(rel_l2_bf16(y_gpu, x) - rel_l2_bf16(y_ref, x)) <= RELL2_ATOL
+    assert taco.device_status() == 0
+    del xd
+    torch.cuda.empty_cache()
