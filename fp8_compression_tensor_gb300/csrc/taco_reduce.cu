@@ -53,8 +53,8 @@ namespace {
 #ifndef TACO_REDUCE_RING_KB
 #define TACO_REDUCE_RING_KB 192
 #endif
-#ifndef TACO_REDUCE_FIXED_P8
-#define TACO_REDUCE_FIXED_P8 1
+#ifndef TACO_REDUCE_FIXED_SHARDS
+#define TACO_REDUCE_FIXED_SHARDS 1
 #endif
 #ifndef TACO_REDUCE_GROUPS
 #define TACO_REDUCE_GROUPS 3
@@ -476,14 +476,14 @@ KernelInfo reduce_kernel_info(int block, int code, int num_shards)
     // Tensor-parallel degrees 2, 4 and 16 (the owner reduces that many
     // segments) have kernels with the shard loop unrolled, 2 and 4 with longer
     // tiles, for the method's E4M3 codes.
-    if (TACO_REDUCE_FIXED_P8 && code == 0 && (num_shards == 2 || num_shards == 4))
+    if (TACO_REDUCE_FIXED_SHARDS && code == 0 && (num_shards == 2 || num_shards == 4))
         return num_shards == 2 ? info_for_block<0, 2>(block) : info_for_block<0, 4>(block);
     // 16 shards: the same with tiles half as long (two stages would fit otherwise).
-    if (TACO_REDUCE_FIXED_P8 && code == 0 && num_shards == 16)
+    if (TACO_REDUCE_FIXED_SHARDS && code == 0 && num_shards == 16)
         return info_for_block<0, 16>(block);
     // The 8-shard case has kernels with the shard loop unrolled, for every
     // code format and block size.
-    if (TACO_REDUCE_FIXED_P8 && num_shards == 8) {
+    if (TACO_REDUCE_FIXED_SHARDS && num_shards == 8) {
         switch (code) {
         case 0: return info_for_block<0, 8>(block);
         case 1: return info_for_block<1, 8>(block);

@@ -158,6 +158,19 @@ def reduce_exact_u(shard_packed, block: int, variant: int = 0, code: int = 0) ->
     return np.where(m > 0, qmax * W / np.where(m > 0, m, 1.0), 0.0)
 
 
+def exact_compress_u(x_bf16: np.ndarray, block: int, variant: int = 0, code: int = 0) -> np.ndarray:
+    """float64 values before quantisation of every element, in real
+    arithmetic: Q_max y / max|y| with y = H G (G itself for DS only; alpha
+    cancels), or Z = alpha y / sqrt(B) for ASH only."""
+    from helpers import hadamard
+    G = bf16_to_f64(x_bf16).reshape(-1, block)
+    y = G if variant == 2 else G @ hadamard(block).T
+    if variant == 3:
+        return y / np.sqrt((G * G).sum(axis=1, keepdims=True) + float(np.float32(1e-30)) * block)
+    m = np.abs(y).max(axis=1, keepdims=True)
+    return np.where(m > 0, CODE_QMAX[code] * y / np.where(m > 0, m, 1.0), 0.0)
+
+
 def exact_compress_scales(x_bf16: np.ndarray, block: int, variant: int = 0, code: int = 0):
     """alpha and s of every block in real arithmetic (float64) from the bf16
     input: Eqs. (6)-(7) and (9), alpha cancelling out of the codes."""

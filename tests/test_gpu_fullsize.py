@@ -22,7 +22,7 @@ import oracle
 import workloads
 from parity import (RELL2_ATOL, compare_decoded, compare_records, oracle_compress_parallel,
                     oracle_decompress_parallel, oracle_reduce_parallel, reduce_exact_u, rel_l2_bf16,
-                    exact_compress_scales, exact_reduce_scales)
+                    exact_compress_scales, exact_compress_u, exact_reduce_scales)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -188,14 +188,13 @@ def test_full_size_ablation_schemes(taco, variant, code):
     ([8192 x 4096], block 128): every record of the GPU's compress against the
     oracle's, every element of the GPU's decode of the oracle's records, and
     the round trip's RelL2."""
-    from test_gpu_variants import exact_u
     w = workloads.WORKLOADS["gpt_activation_8192x4096"]
     block = 128
     x = w.tensor().reshape(-1)
     xd = to_dev(x, w.rows, w.hidden)
     got = taco.compress(xd, block, variant=variant, code=code).cpu().numpy()
     ref = oracle_compress_parallel(x, block, variant, code)
-    compare_records(got, ref, block, code=code, u_exact=exact_u(x, block, variant, code),
+    compare_records(got, ref, block, code=code, u_exact=exact_compress_u(x, block, variant, code),
                     scales_exact=exact_compress_scales(x, block, variant, code))
     y_ref = oracle_decompress_parallel(ref, x.size, block, variant, code)
     y_dec = bits_of(taco.decompress(torch.from_numpy(ref).to(DEV), w.rows, w.hidden, block, variant=variant,

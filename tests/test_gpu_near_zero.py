@@ -19,9 +19,9 @@ import torch
 
 import oracle
 import workloads
-from helpers import bf16_to_f64, exact_compress_quantities, records
+from helpers import bf16_to_f64, records
 from near_zero import CODE_QMAX, near_zero_blocks
-from parity import compare_decoded, compare_records, exact_reduce_scales, reduce_exact_u
+from parity import compare_decoded, compare_records, exact_compress_u, exact_reduce_scales, reduce_exact_u
 
 pytestmark = pytest.mark.gpu
 
@@ -45,12 +45,6 @@ def from_dev(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
 
 
-def exact_u(bits, B, code):
-    """float64 values before quantisation: Q_max H G / max|H G| (alpha cancels)."""
-    _, _, u, _ = exact_compress_quantities(bf16_to_f64(bits), B)
-    return u * (CODE_QMAX[code] / 448.0)
-
-
 def no_nan_codes(codes, code):
     c7 = np.asarray(codes) & 0x7F
     return not np.any(c7 == 0x7F) if code == 0 else not np.any(c7 > 0x7B)
@@ -65,7 +59,7 @@ def test_near_zero_compress(taco, B, code):
     got = taco.compress(to_dev(X), B, code=code).cpu().numpy()
     cg, ag, sg = records(got, B)
     assert no_nan_codes(cg, code)
-    stats = compare_records(got, ref, B, code=code, u_exact=exact_u(X, B, code))
+    stats = compare_records(got, ref, B, code=code, u_exact=exact_compress_u(X, B, 0, code))
     assert stats["code_mismatches"] == 0, stats
     # Every block is nonzero: its largest code is +-Q_max (Eqs. 9-10).
     top = 0x7E if code == 0 else 0x7B

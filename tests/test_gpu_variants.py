@@ -17,7 +17,8 @@ import torch
 import oracle
 import workloads
 from helpers import bf16_to_f64, records
-from parity import (RELL2_ATOL, compare_decoded, compare_records, exact_reduce_scales, oracle_compress_parallel,
+from parity import (RELL2_ATOL, compare_decoded, compare_records, exact_compress_u, exact_reduce_scales,
+                    oracle_compress_parallel,
                     oracle_decompress_parallel, reduce_exact_u, rel_l2_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -42,18 +43,6 @@ def from_dev(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
 
 
-def exact_u(bits, B, variant, code):
-    """float64 pre-quantisation values of the compression (for tie marking)."""
-    G = bf16_to_f64(bits).reshape(-1, B)
-    from helpers import hadamard
-    y = G if variant == 2 else G @ hadamard(B).T
-    if variant == 3:
-        return y / np.sqrt((G * G).sum(axis=1, keepdims=True) + 1e-30 * B)
-    qmax = {0: 448.0, 1: 57344.0, 2: 127.0}[code]
-    m = np.abs(y).max(axis=1, keepdims=True)
-    return np.where(m > 0, qmax * y / np.where(m > 0, m, 1.0), 0.0)
-
-
 BLOCKS = [32, 64, 128, 256, 512]
 
 
@@ -65,7 +54,7 @@ def test_compress_decompress(taco, B, variant, code):
     n = bits.size
     ref = oracle_compress_parallel(bits, B, variant, code)
     got = taco.compress(to_dev(bits).view(ROWS, HIDDEN), B, variant=variant, code=code).cpu().numpy()
-    u = exact_u(bits, B, variant, code)
+    u = exact_compress_u(bits, B, variant, code)
     compare_records(got, ref, B, u_exact=u, code=code)
     # Decompress the oracle's records on the GPU.
     y = from_dev(taco.decompress(torch.from_numpy(ref).cuda(), ROWS, HIDDEN, B, variant=variant, code=code))

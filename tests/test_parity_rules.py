@@ -201,3 +201,21 @@ def test_scale_closer_to_exact_passes_and_otherwise_fails(case):
     rec[3, B:B + 4] = np.float32(ae[3] * (1 - 3e-6)).reshape(1).view(np.uint8)
     with pytest.raises(AssertionError):
         compare_records(got, bad_ref.reshape(-1), B, scales_exact=(ae, se))
+
+
+def test_exact_compress_u_matches_the_float64_restatement():
+    """exact_compress_u against helpers.exact_compress_quantities (ASH + DS)
+    for each code format's Q_max, and the DS-only and ASH-only forms against
+    their definitions."""
+    from helpers import exact_compress_quantities
+    from parity import exact_compress_u
+    bits = workloads.generate("laplace_outliers", 16, 1024, 9).reshape(-1)
+    G = bf16_to_f64(bits).reshape(-1, B)
+    _, _, u, _ = exact_compress_quantities(G, B)
+    for code, qmax in ((0, 448.0), (1, 57344.0), (2, 127.0)):
+        assert np.allclose(exact_compress_u(bits, B, 0, code), u * qmax / 448.0, rtol=1e-12, atol=0)
+    ds = exact_compress_u(bits, B, 2, 0)
+    assert np.allclose(ds, 448.0 * G / np.abs(G).max(axis=1, keepdims=True), rtol=1e-12, atol=0)
+    ash = exact_compress_u(bits, B, 3, 0)
+    alpha = 1.0 / np.sqrt((G * G).mean(axis=1, keepdims=True) + float(np.float32(1e-30)))
+    assert np.allclose(ash, alpha * (G @ hadamard(B).T) / np.sqrt(B), rtol=1e-12, atol=0)
