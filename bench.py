@@ -11,15 +11,18 @@ configuration.  One step is one pass of the whole path over one tensor:
                         AllReduce, -> one reduced segment          (Section 4.4.2)
   3. taco_decompress    packed records      -> y (bf16)           (Eqs. 11-13)
 
-Steady state.  The step runs as a CUDA graph of the three launches, replayed
-K times back to back.  Inputs rotate over R buffer sets (R x the bytes of one
-set >= 3 x L2) and the three kernels of step k work on different sets: compress
-on set k, the reduce on the packed records of set k-2 and decompress on those
-of set k-3 (k mod R), so every kernel reads data last written at least two
-kernels and some hundreds of MB of traffic earlier, from HBM, and the deferred
-write-back of every kernel's output is paid inside the timed region.  Each
-kernel's own average launch duration is timed the same way: graphs of R
-back-to-back launches of that kernel alone, replayed, over the rotating sets.
+Steady state.  The K steps run as CUDA graphs of C consecutive steps (C a
+multiple of R with at least LAUNCHES_PER_GRAPH launches, and one graph for the
+K mod C steps left), replayed back to back: each replay boundary leaves the GPU
+idle for a few microseconds, which a graph of C steps pays once.  Inputs rotate
+over R buffer sets (R x the bytes of one set >= 3 x L2) and the three kernels
+of step k work on different sets: compress on set k, the reduce on the packed
+records of set k-2 and decompress on those of set k-3 (k mod R), so every
+kernel reads data last written at least two kernels and some hundreds of MB of
+traffic earlier, from HBM, and the deferred write-back of every kernel's output
+is paid inside the timed region.  Each kernel's own average launch duration is
+timed the same way: graphs of at least LAUNCHES_PER_GRAPH back-to-back launches
+of that kernel alone over the rotating sets, replayed.
 
 Metric (`value`): compress/decompress GB/s of bf16 input = 2 x 2N bytes (the
 bf16 tensor compressed plus the bf16 tensor decompressed) over the sum of the
@@ -68,6 +71,9 @@ KERNEL_SOURCES = {
     "reduce": "fp8_compression_tensor_gb300/csrc/taco_reduce.cu",
 }
 FALLBACK_HBM_GBS = 6800.0
+# Launches per captured graph (at least): a replay boundary idles the GPU for
+# about 4 us, which would otherwise be charged to the launches of one replay.
+LAUNCHES_PER_GRAPH = 32
 
 
 def parse_args():
@@ -421,16 +427,16 @@ def run_taco(args, rank, world):
     def op_decompress(r, st=None):
         taco.decompress(packs[r], rows, hidden, block, out=ys[r], stream=st or stream, **scheme)
 
-    # The cycle of R steps as a graph with one branch per kernel kind and an
+    # A cycle of steps as a graph with one branch per kernel kind and an
     # edge only where data flows (compress -> reduce / decompress of the same
     # set, and a set's next compress after the reads of its records): the
     # three kernels of a step work on different buffer sets (micro-batches),
     # so one kernel's tail overlaps the next kernel's start.
     branch = {"C": torch.cuda.Stream(dev), "R": torch.cuda.Stream(dev), "D": torch.cuda.Stream(dev)}
 
-    def cycle_with_data_edges():
+    def cycle_with_data_edges(steps):
         ops = []
-        for k in range(R):
+        for k in range(steps):
             ops += [("C", k % R), ("R", (k - 2) % R), ("D", (k - 3) % R)]
         for st in branch.values():
             st.wait_stream(stream)
@@ -467,6 +473,15 @@ def run_taco(args, rank, world):
             fn()
         return g
 
+    # Graphs of L = M x R launches (M passes over the rotating sets).
+    M = -(-LAUNCHES_PER_GRAPH // R)
+    L = M * R
+    K = args.steps
+    C = min(L, max(R, K // R * R))
+
+    def capture_solo(fn):
+        return capture(lambda: [fn(r) for _ in range(M) for r in range(R)])
+
     def barrier():
         if world > 1:
             dist.barrier()
@@ -479,8 +494,9 @@ def run_taco(args, rank, world):
             step(k)
         stream.synchronize()
         step_graphs = [capture(lambda k=k: step(k)) for k in range(R)]
-        cycle_graph = capture(cycle_with_data_edges)   # R steps, sets 0..R-1 once each
-        solo_graphs = {name: capture(lambda fn=fn: [fn(r) for r in range(R)])
+        cycle_graph = capture(lambda: cycle_with_data_edges(C))   # C steps, the R sets C / R times each
+        tail_graph = capture(lambda: cycle_with_data_edges(K % C)) if K % C else None
+        solo_graphs = {name: capture_solo(fn)
                        for name, fn in (("compress", op_compress), ("reduce", op_reduce),
                                         ("decompress", op_decompress))}
 
@@ -493,7 +509,6 @@ def run_taco(args, rank, world):
     if not args.no_clocks:
         sampler.start()
 
-    K = args.steps
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
             step_graphs[k % R].replay()
@@ -505,10 +520,10 @@ def run_taco(args, rank, world):
     t_wall0 = time.time()
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(K // R):
+        for _ in range(K // C):
             cycle_graph.replay()
-        for k in range(K - K % R, K):
-            step_graphs[k % R].replay()
+        if tail_graph is not None:
+            tail_graph.replay()
         ev1.record(stream)
     barrier()
     t_wall1 = time.time()
@@ -516,7 +531,7 @@ def run_taco(args, rank, world):
     ms_step = max_over_ranks([ev0.elapsed_time(ev1) / K], device=dev)[0]
 
     names = ("compress", "reduce", "decompress")
-    solo = time_solo(solo_graphs, stream, R, K, dev)
+    solo = time_solo(solo_graphs, stream, L, K, dev)
     solo_ms = {k: solo[k]["ms"] for k in names}
     t_wall2 = time.time()            # the clock record covers the steps and the per-kernel timings
 
@@ -559,8 +574,8 @@ def run_taco(args, rank, world):
             with torch.cuda.stream(stream):
                 for r in range(R):
                     fns["compress"](r)
-                graphs = {name: capture(lambda fn=fns[name]: [fn(r) for r in range(R)]) for name in names}
-            tb = time_solo(graphs, stream, R, K, dev)
+                graphs = {name: capture_solo(fns[name]) for name in names}
+            tb = time_solo(graphs, stream, L, K, dev)
             alg_b = {"compress": 2 * n + nb, "reduce": (P + 1) * sb, "decompress": nb + 2 * n}
             entry = {op: op_line(op, tb[op], alg_b[op], n) for op in names}
             entry["value"] = whole_job_gbs(world, 4.0 * n, tb["compress"]["ms"] + tb["decompress"]["ms"])
@@ -582,9 +597,9 @@ def run_taco(args, rank, world):
             with torch.cuda.stream(stream):
                 for r in range(R):
                     op_compress(r)
-                g2 = {"reduce": capture(lambda: [taco.reduce_shards(segs2[r], sr2, hidden, block, out=outs2[r],
-                                                                    stream=stream, **scheme) for r in range(R)])}
-            t2 = time_solo(g2, stream, R, K, dev)["reduce"]
+                g2 = {"reduce": capture_solo(lambda r: taco.reduce_shards(segs2[r], sr2, hidden, block,
+                                                                          out=outs2[r], stream=stream, **scheme))}
+            t2 = time_solo(g2, stream, L, K, dev)["reduce"]
             shard_counts[str(P2)] = op_line("reduce", t2, (P2 + 1) * sb2, n)
             del outs2, segs2, g2
         torch.cuda.empty_cache()
@@ -702,8 +717,8 @@ def run_taco(args, rank, world):
                 "traffic_write": tr["dram_write_per_launch"] if tr else None,
                 "traffic_how": tr["how"] if tr else "no capture of the current kernel code",
                 "algorithmic_bytes_per_launch": alg[dom],
-                "duration": (f"mean of {solo[dom]['launches']} back-to-back launches of the kernel alone (graph "
-                             f"replays over the {R} rotating sets), CUDA events on its stream")}
+                "duration": (f"mean of {solo[dom]['launches']} back-to-back launches of the kernel alone (graphs "
+                             f"of {L} launches over the {R} rotating sets, replayed), CUDA events on its stream")}
 
     line = {
         "metric": METRIC,
@@ -725,10 +740,10 @@ def run_taco(args, rank, world):
                    "step": "compress + reduce_shards(P row-slices of the packed tensor) + decompress",
                    "l2": (f"no flush; inputs larger than L2: {R} rotating buffer sets of {set_bytes / 1e6:.1f} MB "
                           f"(L2 {l2 / 1e6:.0f} MB); step k compresses set k, reduces set k-2, decompresses "
-                          f"set k-3; graph replays (one graph per R steps, a branch per kernel kind with edges "
-                          f"only for data dependencies, so kernels of different sets overlap at their "
-                          f"boundaries), one CUDA-event pair around the K steps"),
-                   "buffer_sets": R,
+                          f"set k-3; graph replays (one graph per {C} steps and one for the K mod {C} left, a "
+                          f"branch per kernel kind with edges only for data dependencies, so kernels of "
+                          f"different sets overlap at their boundaries), one CUDA-event pair around the K steps"),
+                   "buffer_sets": R, "steps_per_graph": C, "launches_per_graph": L,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "step": {"ms": ms_step, "gbs_6n": whole_job_gbs(world, 6.0 * n, ms_step),
                  "what": "the K timed steps: 6N bytes per step (2N compressed + 2N logical bf16 of the reduced "
@@ -752,13 +767,14 @@ def run_taco(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def time_solo(graphs: dict, stream, R: int, K: int, dev) -> dict:
-    """Each kernel alone: its graph of R back-to-back launches over the
-    rotating sets, replayed; events split the replays into G groups.  Per
-    kernel: the mean over all launches (ms), the median and minimum of the
-    groups' per-launch means, MAX over ranks."""
+def time_solo(graphs: dict, stream, L: int, K: int, dev) -> dict:
+    """Each kernel alone: its graph of L back-to-back launches over the
+    rotating sets, replayed (about min(1000, 2K) launches in all); events
+    split the replays into G groups.  Per kernel: the mean over all launches
+    (ms), the median and minimum of the groups' per-launch means, MAX over
+    ranks."""
     import torch
-    reps = max(4, min(250, (20 * K) // (R * 10)))
+    reps = max(4, min(1000, 2 * K) // L)
     G = min(10, reps)
     reps = reps // G * G
     out = {}
@@ -773,17 +789,19 @@ def time_solo(graphs: dict, stream, R: int, K: int, dev) -> dict:
                     g.replay()
                 evs[j + 1].record(stream)
             stream.synchronize()
-            per = [evs[j].elapsed_time(evs[j + 1]) / (reps // G * R) for j in range(G)]
-            t = max_over_ranks([evs[0].elapsed_time(evs[G]) / (reps * R), statistics.median(per), min(per)],
+            per = [evs[j].elapsed_time(evs[j + 1]) / (reps // G * L) for j in range(G)]
+            t = max_over_ranks([evs[0].elapsed_time(evs[G]) / (reps * L), statistics.median(per), min(per)],
                                device=dev)
-            out[name] = {"ms": t[0], "median": t[1], "min": t[2], "launches": reps * R, "groups": G}
+            out[name] = {"ms": t[0], "median": t[1], "min": t[2], "launches": reps * L, "groups": G,
+                         "launches_per_graph": L}
     return out
 
 
 def time_full_shard_reduce(taco, wf, block, scheme, stream, dev, capture, peak):
     """The reduce of P full-size packed shards (the P-seed workload: each shard
-    its own seeded tensor, compressed on the GPU), back-to-back graph
-    replays."""
+    its own seeded tensor, compressed on the GPU): a graph of
+    LAUNCHES_PER_GRAPH back-to-back launches on the same shards (401 MB of
+    traffic a launch, three times L2), replayed."""
     import torch
     Pf = len(wf.seeds)
     rows, hidden = wf.rows, wf.hidden
@@ -797,24 +815,25 @@ def time_full_shard_reduce(taco, wf, block, scheme, stream, dev, capture, peak):
             taco.compress(xf, block, out=full[p_], stream=stream, **scheme)
             stream.synchronize()
             del xf
-        g_full = capture(lambda: taco.reduce_shards(full, rows, hidden, block, out=full_out, stream=stream,
-                                                    **scheme))
-        for _ in range(3):
-            g_full.replay()
+        Lf = LAUNCHES_PER_GRAPH
+        g_full = capture(lambda: [taco.reduce_shards(full, rows, hidden, block, out=full_out, stream=stream,
+                                                     **scheme) for _ in range(Lf)])
+        g_full.replay()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps_f = 50
+        reps_f = 8
         a.record(stream)
         for _ in range(reps_f):
             g_full.replay()
         b.record(stream)
         stream.synchronize()
-    ms_f = max_over_ranks([a.elapsed_time(b) / reps_f], device=dev)[0]
+    ms_f = max_over_ranks([a.elapsed_time(b) / (reps_f * Lf)], device=dev)[0]
     alg_f = (Pf + 1) * nbytes
     return {"workload": wf.name, "ms": ms_f, "shards": Pf, "block": block, "algorithmic_bytes": alg_f,
             "hbm_gbs": alg_f / ms_f / 1e6, "frac_of_measured_hbm": alg_f / ms_f / 1e6 / peak,
             "frac_of_nominal_8tbs": alg_f / ms_f / 1e6 / 8000.0, "logical_bf16_gbs": Pf * 2 * n / ms_f / 1e6,
+            "launches": reps_f * Lf, "launches_per_graph": Lf,
             "what": f"reduce of {Pf} full-size packed [{rows} x {hidden}] shards (seeds {list(wf.seeds)}), "
-                    f"back-to-back graph replays, the same input every replay"}
+                    f"graphs of {Lf} back-to-back launches on the same input, replayed"}
 
 
 def parity_against_oracle(taco, run, x_bits, block, P, scheme, stream, dev) -> dict:
