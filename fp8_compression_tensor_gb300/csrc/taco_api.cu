@@ -80,15 +80,19 @@ void init_device(DeviceState &st)
     const int blocks[5] = {32, 64, 128, 256, 512};
     for (int i = 0; i < 5 && e == cudaSuccess; i++) {
         if (tensor_core_block(blocks[i])) {
-            e = init_kernel(compress_kernel_info(blocks[i], 0), &st.ctas_per_sm);
+            e = init_kernel(compress_kernel_info(blocks[i], 0, 0), &st.ctas_per_sm);
             if (e == cudaSuccess)
-                e = init_kernel(compress_kernel_info(blocks[i], 2), &st.ctas_per_sm);
+                e = init_kernel(compress_kernel_info(blocks[i], 2, 0), &st.ctas_per_sm);
+            if (e == cudaSuccess)
+                e = init_kernel(compress_kernel_info(blocks[i], 0, 2), &st.ctas_per_sm);
             for (int code = 0; code < 3 && e == cudaSuccess; code += 2)   // E5M2 shares the E4M3 kernel
                 e = init_kernel(decompress_kernel_info(blocks[i], code), &st.ctas_per_sm);
         } else {
-            e = init_kernel(warp_codec_info(blocks[i], true), &st.ctas_per_sm);
+            e = init_kernel(warp_codec_info(blocks[i], true, 0), &st.ctas_per_sm);
             if (e == cudaSuccess)
-                e = init_kernel(warp_codec_info(blocks[i], false), &st.ctas_per_sm);
+                e = init_kernel(warp_codec_info(blocks[i], true, 2), &st.ctas_per_sm);
+            if (e == cudaSuccess)
+                e = init_kernel(warp_codec_info(blocks[i], false, 0), &st.ctas_per_sm);
         }
         for (int code = 0; code < 3 && e == cudaSuccess; code++)
             e = init_kernel(reduce_kernel_info(blocks[i], code, 1), &st.ctas_per_sm);
@@ -218,7 +222,7 @@ taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, in
         return st;
     const int64_t nblocks = n / block;
     if (!tensor_core_block(block)) {
-        const KernelInfo wk = warp_codec_info(block, true);
+        const KernelInfo wk = warp_codec_info(block, true, scheme.code);
         const int64_t want = (nblocks + wk.tile_blocks - 1) / wk.tile_blocks;
         const int64_t cap = static_cast<int64_t>(dev->sm_count) * 16;
         const cudaError_t e = launch_warp_compress(block, scheme, x_bf16, packed_out, nblocks,
@@ -228,7 +232,7 @@ taco_status_t compress_impl(const void *x_bf16, int64_t rows, int64_t hidden, in
     }
     // Tensor-core kernel over tiles of 128 blocks: one CTA per tile, of which
     // one per SM runs and takes the tiles of CTAs it cancels before they start.
-    const KernelInfo ki = compress_kernel_info(block, scheme.variant);
+    const KernelInfo ki = compress_kernel_info(block, scheme.variant, scheme.code);
     const int64_t ntiles = (nblocks + ki.tile_blocks - 1) / ki.tile_blocks;
     if (ntiles > INT32_MAX)
         return TACO_ERR_BAD_SHAPE;
@@ -263,7 +267,7 @@ taco_status_t decompress_impl(const void *packed_in, int64_t rows, int64_t hidde
         return st;
     const int64_t nblocks = n / block;
     if (!tensor_core_block(block)) {
-        const KernelInfo wk = warp_codec_info(block, false);
+        const KernelInfo wk = warp_codec_info(block, false, scheme.code);
         const int64_t want = (nblocks + wk.tile_blocks - 1) / wk.tile_blocks;
         const int64_t cap = static_cast<int64_t>(dev->sm_count) * 16;
         const cudaError_t e = launch_warp_decompress(block, scheme, packed_in, y_bf16_out, nblocks,

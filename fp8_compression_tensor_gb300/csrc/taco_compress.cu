@@ -43,10 +43,13 @@
 // formula.
 //
 // Ablations (Scheme): standard Hadamard + DS takes alpha = 1; DS only (its
-// own instantiation, DS_ONLY) puts the identity in place of H (y = G) with
+// own instantiation, MODE 1) puts the identity in place of H (y = G) with
 // alpha = 1 and codes G / s correctly rounded, as Eq. (10) writes it; ASH
 // only stores s = 1 and converts Z = alpha y / sqrt(B) directly; E5M2 and
-// INT8 codes use Q_max = 57344 and 127.
+// INT8 codes use Q_max = 57344 and 127.  The rotating schemes with INT8 codes
+// are their own instantiation too (MODE 2, scalar products before the integer
+// rounding, see encode4_scaled), so the FP8 kernel carries no format branch
+// around its packed products.
 #include <cstring>
 #include <type_traits>
 
@@ -144,7 +147,9 @@ __device__ void write_hadamard_sw128(uint8_t *h, bool rotate)
     }
 }
 
-template <int B, int STAGES, int EPG, int NBG, bool DS_ONLY>
+// MODE: 0 rotation, FP8 codes (E4M3 or E5M2); 1 DS only, any code format;
+// 2 rotation, INT8 codes.
+template <int B, int STAGES, int EPG, int NBG, int MODE>
 __global__ void __launch_bounds__(tc_threads(EPG), 1)
     taco_compress_kernel(const __grid_constant__ CUtensorMap tmap_x, uint8_t *__restrict__ packed,
                             int64_t nblocks, uint32_t *__restrict__ fault, const Scheme scheme)
@@ -217,6 +222,7 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
     if (warp == 1)
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
     // DS only (no rotation) is its own instantiation; the others rotate.
+    constexpr bool DS_ONLY = MODE == 1;
     constexpr bool rotate = !DS_ONLY;
     const bool adaptive = scheme.variant == 0 || scheme.variant == 3;  // alpha from Eqs. (6)-(7)
     const bool dual_scale = scheme.variant != 3;                    // s from Eq. (9)
@@ -405,7 +411,6 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
             // Pass 2: codes (Eq. 10) two per cvt, 32 per chunk.  `scaled`:
             // every value is first multiplied by `pre` (exact).
             auto code_pass = [&](float kk, auto scaled, float pre) {
-                const float2 k2 = make_float2(kk, kk);
                 // The rare scaled pass and DS only stay compact (one chunk at
                 // a time).
 #pragma unroll((decltype(scaled)::value || DS_ONLY) ? 1 : Lay::kAccCols / 32)
@@ -419,7 +424,14 @@ __global__ void __launch_bounds__(tc_threads(EPG), 1)
                             r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), pre));
                     }
                     uint32_t cw[8];
-                    if constexpr (!DS_ONLY) {
+                    if constexpr (MODE == 2) {
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+                            cw[j] = encode4_scaled(
+                                2, make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])),
+                                make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), kk);
+                    } else if constexpr (MODE == 0) {
+                        const float2 k2 = make_float2(kk, kk);
 #pragma unroll
                         for (int j = 0; j < 8; j++) {
                             const float2 u0 =
@@ -529,14 +541,15 @@ template <int B, int STAGES, int EPG, int NBG>
 struct TcCompressConfig {
     using Lay = TcCompressLayout<B, STAGES, EPG, NBG>;
     static_assert(Lay::kSmem <= 227 * 1024, "shared memory budget");
-    static void *fn(bool ds_only)
+    static void *fn(int mode)
     {
-        return ds_only ? reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG, true>)
-                       : reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG, false>);
+        return mode == 1   ? reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG, 1>)
+               : mode == 2 ? reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG, 2>)
+                           : reinterpret_cast<void *>(&taco_compress_kernel<B, STAGES, EPG, NBG, 0>);
     }
-    static KernelInfo info(bool ds_only)
+    static KernelInfo info(int mode)
     {
-        return KernelInfo{fn(ds_only), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), Lay::kTileBlocks, 0};
+        return KernelInfo{fn(mode), static_cast<size_t>(Lay::kSmem), tc_threads(EPG), Lay::kTileBlocks, 0};
     }
 };
 
@@ -560,14 +573,14 @@ using CompressTc512 = TcCompressConfig<512, TACO_TC512_CFG / 100, TACO_TC512_CFG
 
 }  // namespace
 
-KernelInfo compress_kernel_info(int block, int variant)
+KernelInfo compress_kernel_info(int block, int variant, int code)
 {
-    const bool ds_only = variant == 2;
+    const int mode = variant == 2 ? 1 : code == 2 ? 2 : 0;
     switch (block) {
-    case 64: return CompressTc64::info(ds_only);
-    case 128: return CompressTc128::info(ds_only);
-    case 256: return CompressTc256::info(ds_only);
-    case 512: return CompressTc512::info(ds_only);
+    case 64: return CompressTc64::info(mode);
+    case 128: return CompressTc128::info(mode);
+    case 256: return CompressTc256::info(mode);
+    case 512: return CompressTc512::info(mode);
     default: return KernelInfo{};
     }
 }
@@ -575,7 +588,7 @@ KernelInfo compress_kernel_info(int block, int variant)
 cudaError_t launch_compress(int block, Scheme scheme, const void *tmap, void *packed, int64_t nblocks, uint32_t *fault,
                             int grid, cudaStream_t stream)
 {
-    const KernelInfo ki = compress_kernel_info(block, scheme.variant);
+    const KernelInfo ki = compress_kernel_info(block, scheme.variant, scheme.code);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     CUtensorMap map;

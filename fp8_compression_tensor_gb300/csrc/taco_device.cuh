@@ -335,6 +335,21 @@ __device__ __forceinline__ uint32_t encode4(int code, float a, float b, float c,
     return int8x4_from_float(a, b, c, d);
 }
 
+// Codes of the four products ab.x k, ab.y k, cd.x k, cd.y k (first in the low
+// byte), each product rounded to binary32 before the conversion.  INT8 takes
+// scalar products: a packed multiply followed by the packed rounding add of
+// int8x4_from_float came out fused into one fused multiply-add, which rounds
+// the exact product to an integer (63.4999993 -> 63 where the binary32
+// product is 63.5 -> 64).  The FP8 conversions read the packed products.
+__device__ __forceinline__ uint32_t encode4_scaled(int code, float2 ab, float2 cd, float k)
+{
+    if (code == 2)
+        return int8x4_from_float(__fmul_rn(ab.x, k), __fmul_rn(ab.y, k), __fmul_rn(cd.x, k), __fmul_rn(cd.y, k));
+    const float2 k2 = make_float2(k, k);
+    const float2 u0 = mul2(ab, k2), u1 = mul2(cd, k2);
+    return encode4(code, u0.x, u0.y, u1.x, u1.y);
+}
+
 // Cvt_FP32 (Eq. 11) of the two E4M3 codes in the low 16 bits of `pair`
 // (exact): low byte -> .x, high byte -> .y.
 // The two f16 values of a word as floats (exact), low half first.

@@ -47,7 +47,7 @@ struct Scheme {
     int code;
 };
 
-KernelInfo compress_kernel_info(int block, int variant);   // variant 2 (DS only) has its own kernel
+KernelInfo compress_kernel_info(int block, int variant, int code);   // DS only, and INT8 codes, have their own kernels
 KernelInfo decompress_kernel_info(int block, int code);   // code 2 (INT8) has its own kernel
 KernelInfo reduce_kernel_info(int block, int code, int num_shards);
 
@@ -62,7 +62,7 @@ cudaError_t launch_decompress(int block, Scheme scheme, const void *tmap_y, cons
 
 // CUDA-core codec for block 32 (a lane per block); fn == nullptr otherwise.
 // tile_blocks = blocks per CTA.
-KernelInfo warp_codec_info(int block, bool compress);
+KernelInfo warp_codec_info(int block, bool compress, int code);   // INT8 compress has its own kernel
 cudaError_t launch_warp_compress(int block, Scheme scheme, const void *x, void *packed, int64_t nblocks, int grid,
                                  cudaStream_t stream);
 cudaError_t launch_warp_decompress(int block, Scheme scheme, const void *packed, void *y, int64_t nblocks, int grid,

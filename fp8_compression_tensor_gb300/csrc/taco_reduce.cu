@@ -410,13 +410,10 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
             for (int j = 0; j < LW; j++)
                 o[j] = 0u;
             if (wmax > 0.f && !ds_only) {
-                const float2 k2 = make_float2(kq, kq);
 #pragma unroll
-                for (int j = 0; j < LW; j++) {
-                    const float2 u0 = mul2(make_float2(w[4 * j], w[4 * j + 1]), k2);
-                    const float2 u1 = mul2(make_float2(w[4 * j + 2], w[4 * j + 3]), k2);
-                    o[j] = encode4(CODE, u0.x, u0.y, u1.x, u1.y);
-                }
+                for (int j = 0; j < LW; j++)
+                    o[j] = encode4_scaled(CODE, make_float2(w[4 * j], w[4 * j + 1]),
+                                          make_float2(w[4 * j + 2], w[4 * j + 3]), kq);
             } else if (ds_only && sc >= kDivFastMin) {
                 // DS only: W is the sum of the decoded shards itself (no
                 // rotation, alpha = 1); its codes are W / s' correctly rounded.

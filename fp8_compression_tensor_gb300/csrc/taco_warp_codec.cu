@@ -138,6 +138,10 @@ __device__ __forceinline__ void stage_records_async(uint4 *buf, const uint8_t *p
 // copies in flight (two buffers: 78.9 us, three: 76.9 us on 16384 x 8192).
 constexpr int kInBufs = TACO_LANE_IN_BUFS;
 
+// INT8: the rotating schemes with INT8 codes (scalar products before the
+// integer rounding, see encode4_scaled) are their own instantiation, so the
+// FP8 kernel carries no format branch around its packed products.
+template <bool INT8>
 __global__ void __launch_bounds__(kWarpThreads) taco_lane_compress_kernel(const uint16_t *__restrict__ x,
                                                                           uint8_t *__restrict__ packed,
                                                                           int64_t nblocks, const Scheme scheme)
@@ -236,7 +240,14 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_compress_kernel(const 
         }
         uint32_t cw[B / 4];
         const float2 k2 = make_float2(kq, kq);
-        if (rotate || !dual_scale) {
+        if ((rotate || !dual_scale) && INT8) {
+            // INT8: scalar products before the integer rounding (encode4_scaled).
+#pragma unroll
+            for (int j = 0; j < B / 4; j++)
+                cw[j] = ymax > 0.f ? encode4_scaled(2, make_float2(v[4 * j], v[4 * j + 1]),
+                                                    make_float2(v[4 * j + 2], v[4 * j + 3]), kq)
+                                   : 0u;
+        } else if (rotate || !dual_scale) {
 #pragma unroll
             for (int j = 0; j < B / 4; j++) {
                 const float2 u0 = mul2(make_float2(v[4 * j], v[4 * j + 1]), k2);
@@ -394,24 +405,25 @@ __global__ void __launch_bounds__(kWarpThreads) taco_lane_decompress_kernel(cons
     cp_async_wait<0>();   // no copy may land in shared memory after the CTA is gone
 }
 
-KernelInfo lane_info(bool compress)
+KernelInfo lane_info(bool compress, int code)
 {
-    void *fn = compress ? reinterpret_cast<void *>(&taco_lane_compress_kernel)
-                        : reinterpret_cast<void *>(&taco_lane_decompress_kernel);
+    void *fn = !compress ? reinterpret_cast<void *>(&taco_lane_decompress_kernel)
+               : code == 2 ? reinterpret_cast<void *>(&taco_lane_compress_kernel<true>)
+                           : reinterpret_cast<void *>(&taco_lane_compress_kernel<false>);
     return KernelInfo{fn, 0, kWarpThreads, kWarpThreads, kWarpThreads / 32};
 }
 
 }  // namespace
 
-KernelInfo warp_codec_info(int block, bool compress)
+KernelInfo warp_codec_info(int block, bool compress, int code)
 {
-    return block == 32 ? lane_info(compress) : KernelInfo{};
+    return block == 32 ? lane_info(compress, code) : KernelInfo{};
 }
 
 cudaError_t launch_warp_compress(int block, Scheme scheme, const void *x, void *packed, int64_t nblocks, int grid,
                                  cudaStream_t stream)
 {
-    const KernelInfo ki = warp_codec_info(block, true);
+    const KernelInfo ki = warp_codec_info(block, true, scheme.code);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     const uint16_t *xp = static_cast<const uint16_t *>(x);
@@ -423,7 +435,7 @@ cudaError_t launch_warp_compress(int block, Scheme scheme, const void *x, void *
 cudaError_t launch_warp_decompress(int block, Scheme scheme, const void *packed, void *y, int64_t nblocks, int grid,
                                    cudaStream_t stream)
 {
-    const KernelInfo ki = warp_codec_info(block, false);
+    const KernelInfo ki = warp_codec_info(block, false, scheme.code);
     if (!ki.fn)
         return cudaErrorInvalidValue;
     const uint8_t *pp = static_cast<const uint8_t *>(packed);
