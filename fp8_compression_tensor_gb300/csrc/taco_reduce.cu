@@ -145,7 +145,10 @@ __device__ __forceinline__ void decode4(uint32_t x, float2 &q0, float2 &q1)
 
 // w[k] += q[k] * f for the thread's codes in `words`, each product rounded on
 // its own before the add (so that a shard and its negation cancel exactly, as
-// in an FP32 sum of decoded shards).
+// in an FP32 sum of decoded shards).  The products stay scalar: packed ones
+// (__fmul2_rn, mul.rn.f32x2, or fma.rn.f32x2 with a -0 addend) before the
+// packed add came out fused into FFMA2, which tests/test_gpu_reduce_exact_sum.py
+// detects.
 template <int CODE, int LW>
 __device__ __forceinline__ void accumulate_shard(float (&w)[4 * LW], const uint32_t (&words)[LW], float f)
 {
