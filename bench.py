@@ -474,10 +474,8 @@ def run_taco(args, rank, world):
         return g
 
     # Graphs of L = M x R launches (M passes over the rotating sets).
-    M = -(-LAUNCHES_PER_GRAPH // R)
-    L = M * R
     K = args.steps
-    C = min(L, max(R, K // R * R))
+    M, L, C = graph_plan(K, R)
 
     def capture_solo(fn):
         return capture(lambda: [fn(r) for _ in range(M) for r in range(R)])
@@ -765,6 +763,20 @@ def run_taco(args, rank, world):
         "gpu": props.name,
     }
     print(json.dumps(line), flush=True)
+
+
+def graph_plan(K: int, R: int, min_launches: int = LAUNCHES_PER_GRAPH):
+    """How the timed work is cut into graphs, over R rotating buffer sets:
+    M passes over the sets per per-kernel graph (L = M x R >= min_launches
+    launches), and C steps per step graph (a multiple of R, at most L); the K
+    steps run as K // C replays of the C-step graph and one graph of the
+    K mod C steps left."""
+    if K < 1 or R < 1:
+        raise ValueError("need K >= 1 steps and R >= 1 buffer sets")
+    M = -(-min_launches // R)
+    L = M * R
+    C = min(L, max(R, K // R * R))
+    return M, L, C
 
 
 def time_solo(graphs: dict, stream, L: int, K: int, dev) -> dict:

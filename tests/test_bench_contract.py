@@ -48,3 +48,25 @@ def test_reference_arm_prints_one_contract_line():
 @pytest.mark.parametrize("rank", ["1", "3"])
 def test_reference_arm_other_ranks_exit_without_work(rank):
     assert run({"RANK": rank, "WORLD_SIZE": "4", "LOCAL_RANK": rank}) == []
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 5, 31, 32, 33, 40, 100, 10000])
+@pytest.mark.parametrize("R", [1, 4, 5, 19, 40])
+def test_graph_plan_times_exactly_k_steps(K, R):
+    """The step graphs cover exactly K steps (K // C replays of C steps plus
+    one graph of K mod C), every set-rotating graph is a whole number of
+    passes over the R sets, and the per-kernel graphs hold at least the
+    minimum number of launches."""
+    import bench
+    M, L, C = bench.graph_plan(K, R)
+    assert L == M * R and L >= bench.LAUNCHES_PER_GRAPH and L - R < bench.LAUNCHES_PER_GRAPH
+    assert C % R == 0 and R <= C <= L
+    assert (K // C) * C + K % C == K
+    if K >= L:
+        assert C == L                     # the full graph length once there are enough steps
+
+
+def test_graph_plan_rejects_empty_runs():
+    import bench
+    with pytest.raises(ValueError):
+        bench.graph_plan(0, 4)
