@@ -17,11 +17,12 @@
 //
 // Data movement.  A tile is T consecutive blocks (T = 4096 / B for most shard
 // counts; 8/P times that for the 2- and 4-shard kernels, which take 8/P
-// passes per tile, and half of it for the 16-shard kernel); its records
-// are contiguous in every shard, T * (B + 8) bytes (a multiple of 16: T is
-// even).  The loader warp bulk-copies the tile's P record runs (lane p the
-// run of shard p) into one stage of a shared-memory ring (as many stages of
-// P runs as fit in kRingBytes) and a group of 8 consumer warps decodes them
+// passes per tile, and half of it for the 16-shard kernel at B = 32); its
+// records are contiguous in every shard, T * (B + 8) bytes (a multiple of 16:
+// T is even).  The loader warp bulk-copies the tile's P record runs (lane p
+// the run of shard p) into one stage of a shared-memory ring (as many stages
+// of P runs as fit in its 192 KB; the 16-shard kernel's ring holds exactly
+// three stages) and a group of 8 consumer warps decodes them
 // from shared memory (three groups take turns, so three tiles are decoded at
 // once): B/16 consecutive threads of a group share a block, each owns 16
 // elements (TACO_REDUCE_LANE_CODES = 8 halves that where a block still fits a
@@ -85,10 +86,13 @@ static_assert(kTileRing >= kMaxStages + kGroups, "published-tile slot reused too
 // (2 or 4) takes tiles of MUL = 8 / P times as many blocks, so that a stage
 // still holds about 35 KB of records in long runs (the copies of 2 shards at
 // the 8-shard tile size moved 42% of the bandwidth).
-// LCODES: codes per thread per shard (0: kLaneCodes).  The 16-shard kernel
-// takes 8, which halves its tiles so that five stages of 16 record runs fit
-// the ring instead of two.
-template <int B, int MUL = 1, int LCODES = 0>
+// LCODES: codes per thread per shard (0: kLaneCodes).
+// RING: bytes of the stage ring.  The 16-shard kernel for B >= 64 sizes it
+// for exactly three stages of 16 runs of full tiles (195-216 KB): two
+// stages, or tiles halved to 8 codes per thread (2.2 KB copies, five stages),
+// kept DRAM under-fed (16384 x 8192: 31.4 -> 24.8 us).  B = 32 would fit only
+// two such stages and keeps halved tiles.
+template <int B, int MUL = 1, int LCODES = 0, int RING = kRingBytes>
 struct ReduceLayout {
     // Codes per thread: LCODES or kLaneCodes, or 16 where a block would span
     // more than a warp (its energy and maximum are reduced with shuffles inside
@@ -104,7 +108,7 @@ struct ReduceLayout {
     static constexpr int pass_blocks()
     {
         int t = kConsumers * kLC / B;
-        while (t > 2 && 2 * kMaxP * MUL * t * (B + 8) > kRingBytes)
+        while (t > 2 && 2 * kMaxP * MUL * t * (B + 8) > RING)
             t /= 2;
         return t;
     }
@@ -115,16 +119,29 @@ struct ReduceLayout {
     static constexpr int kRec = B + 8;
     static constexpr int kRunBytes = kT * kRec;             // one shard's records of a tile
     static_assert(kT % 2 == 0 && kRunBytes % 16 == 0, "bulk copies need 16-byte multiples");
-    static_assert(kRingBytes >= 2 * kMaxP * kRunBytes, "at least two stages at the largest shard count");
+    static constexpr int kRing = RING;
+    static_assert(kRing >= 2 * kMaxP * kRunBytes, "at least two stages at the largest shard count");
     // Offsets from the 128-byte aligned base.
     static constexpr int kOffRing = 0;
-    static constexpr int kOffSched = kOffRing + kRingBytes;           // 16-byte aligned
+    static constexpr int kOffSched = kOffRing + kRing;                // 16-byte aligned
     static constexpr int kOffPtrs = kOffSched + kSchedBytes;
     static constexpr int kOffBar = kOffPtrs + 8 * kMaxShards;
     static constexpr int kNumBars = 2 * kMaxStages;
     static constexpr int kBytes = kOffBar + 8 * kNumBars;
     static constexpr int kSmem = kBytes + 128;                        // slack for alignment
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
+
+// The layout of the reduce kernel for block B, code format CODE and shard
+// count PFIX (0: any count).
+__host__ __device__ constexpr int reduce_mul(int pfix) { return pfix == 2 ? 4 : pfix == 4 ? 2 : 1; }
+__host__ __device__ constexpr int reduce_lcodes(int B, int pfix) { return pfix == 16 && B < 64 ? 8 : 0; }
+__host__ __device__ constexpr int reduce_ring(int B, int pfix)
+{
+    return pfix == 16 && B >= 64 ? 3 * 16 * (kConsumers * 16 / B) * (B + 8) : kRingBytes;
+}
+template <int B, int PFIX>
+using ReduceLayoutFor = ReduceLayout<B, reduce_mul(PFIX), reduce_lcodes(B, PFIX), reduce_ring(B, PFIX)>;
 
 // Values of the four codes in `x`, first code in .x of the first pair.
 template <int CODE>
@@ -177,8 +194,8 @@ __device__ __forceinline__ uint2 ldg_u2(const uint8_t *p)
 template <int B, int CODE, int PFIX>
 __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const ReduceArgs args, uint32_t *fault)
 {
-    constexpr int MUL = PFIX == 2 ? 4 : PFIX == 4 ? 2 : 1;
-    using Lay = ReduceLayout<B, MUL, PFIX == 16 ? 8 : 0>;
+    constexpr int MUL = reduce_mul(PFIX);
+    using Lay = ReduceLayoutFor<B, PFIX>;
     constexpr int T = Lay::kT;
     constexpr int kRec = Lay::kRec;
     constexpr int LC = Lay::kLC, LW = Lay::kLW;
@@ -202,7 +219,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
     const bool ds_only = args.variant == 2;                         // no rotation: W is the decoded sum
     // Stages of P record runs in the ring.
     const int stage_bytes = P * Lay::kRunBytes;
-    int nst = kRingBytes / stage_bytes;
+    int nst = Lay::kRing / stage_bytes;
     nst = nst > kMaxStages ? kMaxStages : nst;
 
     auto tile_valid = [&](int64_t t) {
@@ -451,7 +468,7 @@ __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const R
 template <int B, int CODE, int PFIX = 0>
 KernelInfo info()
 {
-    using Lay = ReduceLayout<B, PFIX == 2 ? 4 : PFIX == 4 ? 2 : 1, PFIX == 16 ? 8 : 0>;
+    using Lay = ReduceLayoutFor<B, PFIX>;
     return KernelInfo{reinterpret_cast<void *>(&taco_shard_reduce_kernel<B, CODE, PFIX>), Lay::kSmem, kRThreads,
                       Lay::kT, kRThreads / 32};
 }
