@@ -16,19 +16,20 @@
 // W / s' correctly rounded.
 //
 // Data movement.  A tile is T consecutive blocks (T = 4096 / B for most shard
-// counts; 8/P times that for the 2- and 4-shard kernels, which take 8/P
-// passes per tile, and half of it for the 16-shard kernel at B = 32); its
-// records are contiguous in every shard, T * (B + 8) bytes (a multiple of 16:
-// T is even).  The loader warp bulk-copies the tile's P record runs (lane p
-// the run of shard p) into one stage of a shared-memory ring (as many stages
-// of P runs as fit in its 192 KB; the 16-shard kernel's ring holds exactly
-// three stages) and a group of 8 consumer warps decodes them
-// from shared memory (three groups take turns, so three tiles are decoded at
-// once): B/16 consecutive threads of a group share a block, each owns 16
-// elements (TACO_REDUCE_LANE_CODES = 8 halves that where a block still fits a
-// warp; measured slower).  Energy and maximum are reduced across
-// the block's threads with xor-shuffles (every thread ends with the same bits),
-// and every thread stores its 16 codes directly (8-byte stores).
+// counts; twice that for the 4-shard kernel, four times for the 2-shard
+// kernel, which takes two passes per tile, and half of it for the 16-shard
+// kernel at B = 32); its records are contiguous in every shard, T * (B + 8)
+// bytes (a multiple of 16: T is even).  The loader warp bulk-copies the
+// tile's P record runs (lane p the run of shard p) into one stage of a
+// shared-memory ring (as many stages of P runs as fit in its 192 KB; the
+// 16-shard kernel's ring holds exactly three stages) and a group of 8
+// consumer warps decodes them from shared memory (three groups take turns, so
+// three tiles are decoded at once): each thread owns LC consecutive elements
+// of a block (16; 32 in the 2- and 4-shard kernels; TACO_REDUCE_LANE_CODES = 8
+// halves the 16 where a block still fits a warp, measured slower), so B / LC
+// consecutive threads share a block.  Energy and maximum are reduced across
+// the block's threads with xor-shuffles (every thread ends with the same
+// bits), and every thread stores its codes directly (8-byte stores).
 //
 // Ablations: the decode of every code format is exact (E4M3 and E5M2 through
 // f16, INT8 as integers), W is the same for every variant, and the output
@@ -82,17 +83,22 @@ constexpr int kRSchedAhead = TACO_REDUCE_SCHED_AHEAD;   // cancel requests in fl
 // (and the end marks of kGroups items) is reused only after its readers are done.
 static_assert(kTileRing >= kMaxStages + kGroups, "published-tile slot reused too early");
 
-// MUL: passes of the consumer group over a tile.  A kernel for few shards
-// (2 or 4) takes tiles of MUL = 8 / P times as many blocks, so that a stage
-// still holds about 35 KB of records in long runs (the copies of 2 shards at
-// the 8-shard tile size moved 42% of the bandwidth).
-// LCODES: codes per thread per shard (0: kLaneCodes).
+// MUL: passes of the consumer group over a tile.  The 2-shard kernel takes
+// tiles of two passes, so that a stage still holds about 35 KB of records in
+// long runs (the copies of 2 shards at the 8-shard tile size moved 42% of the
+// bandwidth).
+// LCODES: codes per thread per shard (0: kLaneCodes).  The 2- and 4-shard
+// kernels give each thread 32: with few shards a thread's work is mostly the
+// per-block epilogue (energy, maximum, scales, conversion, stores), which it
+// then does once for twice the codes (16384 x 8192: 2 shards 42.1 -> 34.5 us,
+// 4 shards 30.4 -> 27.4 us; 32 codes at 8 shards were slower, 25.6 -> 26.7 us).
+// MAXP: the shard count the layout is sized for (0: from MUL).
 // RING: bytes of the stage ring.  The 16-shard kernel for B >= 64 sizes it
 // for exactly three stages of 16 runs of full tiles (195-216 KB): two
 // stages, or tiles halved to 8 codes per thread (2.2 KB copies, five stages),
 // kept DRAM under-fed (16384 x 8192: 31.4 -> 24.8 us).  B = 32 would fit only
 // two such stages and keeps halved tiles.
-template <int B, int MUL = 1, int LCODES = 0, int RING = kRingBytes>
+template <int B, int MUL = 1, int LCODES = 0, int RING = kRingBytes, int MAXP = 0>
 struct ReduceLayout {
     // Codes per thread: LCODES or kLaneCodes, or 16 where a block would span
     // more than a warp (its energy and maximum are reduced with shuffles inside
@@ -101,7 +107,7 @@ struct ReduceLayout {
     static constexpr int kLC = B / kLC0 > 32 ? 16 : kLC0;
     static constexpr int kLW = kLC / 4;                      // 32-bit words of a thread's codes
     // Shards a kernel of this layout takes at most.
-    static constexpr int kMaxP = MUL > 1 ? 8 / MUL : kMaxShards;
+    static constexpr int kMaxP = MAXP > 0 ? MAXP : MUL > 1 ? 8 / MUL : kMaxShards;
     // Blocks per consumer pass: one per kLpb consumer threads, halved until two
     // stages of kMaxP record runs of a tile fit the ring (the threads beyond it
     // stay idle).
@@ -134,14 +140,17 @@ struct ReduceLayout {
 
 // The layout of the reduce kernel for block B, code format CODE and shard
 // count PFIX (0: any count).
-__host__ __device__ constexpr int reduce_mul(int pfix) { return pfix == 2 ? 4 : pfix == 4 ? 2 : 1; }
-__host__ __device__ constexpr int reduce_lcodes(int B, int pfix) { return pfix == 16 && B < 64 ? 8 : 0; }
+__host__ __device__ constexpr int reduce_mul(int pfix) { return pfix == 2 ? 2 : 1; }
+__host__ __device__ constexpr int reduce_lcodes(int B, int pfix)
+{
+    return pfix == 2 || pfix == 4 ? 32 : pfix == 16 && B < 64 ? 8 : 0;
+}
 __host__ __device__ constexpr int reduce_ring(int B, int pfix)
 {
     return pfix == 16 && B >= 64 ? 3 * 16 * (kConsumers * 16 / B) * (B + 8) : kRingBytes;
 }
 template <int B, int PFIX>
-using ReduceLayoutFor = ReduceLayout<B, reduce_mul(PFIX), reduce_lcodes(B, PFIX), reduce_ring(B, PFIX)>;
+using ReduceLayoutFor = ReduceLayout<B, reduce_mul(PFIX), reduce_lcodes(B, PFIX), reduce_ring(B, PFIX), PFIX>;
 
 // Values of the four codes in `x`, first code in .x of the first pair.
 template <int CODE>
