@@ -44,3 +44,27 @@ def test_reduce_exact_inputs_separate_rounded_from_fused_sum(B, P):
         fused = (fused + table[c] * s[:, None]).astype(np.float32).astype(np.float64)   # one rounding per add
     changed = np.abs(W).max(axis=1) != np.abs(fused).max(axis=1).astype(np.float32)
     assert changed.sum() >= 50
+
+
+@pytest.mark.parametrize("code", [0, 1])
+@pytest.mark.parametrize("B", [128, 512])
+def test_decompress_exact_inputs_see_the_rescaling(B, code):
+    """tests/test_gpu_decompress_exact.py: without the 2^64 rescaling, the
+    blocks whose factor is subnormal in binary32 (a few bits left) decode to
+    other bf16 values than the expected ones.  (The order in which an
+    ordinary factor is formed is not resolved there: two orders differ by a
+    binary32 ulp, which moves a bf16 output only near a bf16 rounding
+    boundary.  With INT8 codes, or E4M3 codes at B = 32, the products of such
+    factors are mostly below the bf16 range.)"""
+    import oracle
+    import test_gpu_decompress_exact as decompress_exact
+    _, codes, alpha, s = decompress_exact.crafted_records(B, code, seed=100 * B + 10 * code)
+    want = decompress_exact.expected_bits(codes, alpha, s, B, code, rotate=True)
+    rB = np.float32(1.0 / np.sqrt(B))
+    y = (decode_table(code)[codes] @ hadamard(B).T).astype(np.float32)
+    with np.errstate(under="ignore"):
+        f = ((s * rB).astype(np.float32) / alpha).astype(np.float32)
+        plain = oracle.bf16_round((y * f[:, None]).astype(np.float32).reshape(-1)).reshape(want.shape)
+    subnormal = (f > 0) & (f < np.float32(2.0 ** -126))
+    assert subnormal.sum() >= 20
+    assert np.sum(plain[subnormal] != want[subnormal]) >= 20
