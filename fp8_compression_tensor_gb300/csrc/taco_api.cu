@@ -97,9 +97,8 @@ void init_device(DeviceState &st)
         for (int code = 0; code < 3 && e == cudaSuccess; code++)
             e = init_kernel(reduce_kernel_info(blocks[i], code, 1), &st.ctas_per_sm);
         for (int code = 0; code < 3 && e == cudaSuccess; code++)
-            e = init_kernel(reduce_kernel_info(blocks[i], code, 8), &st.ctas_per_sm);
-        for (int shards = 2; shards <= 16 && e == cudaSuccess; shards *= 2)
-            e = init_kernel(reduce_kernel_info(blocks[i], 0, shards), &st.ctas_per_sm);
+            for (int shards = 2; shards <= 16 && e == cudaSuccess; shards *= 2)
+                e = init_kernel(reduce_kernel_info(blocks[i], code, shards), &st.ctas_per_sm);
     }
     st.init_error = e;
 }

@@ -93,11 +93,12 @@ static_assert(kTileRing >= kMaxStages + kGroups, "published-tile slot reused too
 // then does once for twice the codes (16384 x 8192: 2 shards 42.1 -> 34.5 us,
 // 4 shards 30.4 -> 27.4 us; 32 codes at 8 shards were slower, 25.6 -> 26.7 us).
 // MAXP: the shard count the layout is sized for (0: from MUL).
-// RING: bytes of the stage ring.  The 16-shard kernel for B >= 64 sizes it
-// for exactly three stages of 16 runs of full tiles (195-216 KB): two
-// stages, or tiles halved to 8 codes per thread (2.2 KB copies, five stages),
-// kept DRAM under-fed (16384 x 8192: 31.4 -> 24.8 us).  B = 32 would fit only
-// two such stages and keeps halved tiles.
+// RING: bytes of the stage ring.  The 16-shard and the generic kernels for
+// B >= 64 size it for exactly three stages of 16 runs of full tiles
+// (195-216 KB): two stages, or tiles halved to 8 codes per thread (2.2 KB
+// copies, five stages), kept DRAM under-fed (16384 x 8192, 16 shards:
+// 31.4 -> 24.8 us).  B = 32 would fit only two such stages: its 16-shard
+// kernel keeps halved tiles, its generic kernel the 192 KB ring.
 template <int B, int MUL = 1, int LCODES = 0, int RING = kRingBytes, int MAXP = 0>
 struct ReduceLayout {
     // Codes per thread: LCODES or kLaneCodes, or 16 where a block would span
@@ -147,7 +148,7 @@ __host__ __device__ constexpr int reduce_lcodes(int B, int pfix)
 }
 __host__ __device__ constexpr int reduce_ring(int B, int pfix)
 {
-    return pfix == 16 && B >= 64 ? 3 * 16 * (kConsumers * 16 / B) * (B + 8) : kRingBytes;
+    return (pfix == 16 || pfix == 0) && B >= 64 ? 3 * 16 * (kConsumers * 16 / B) * (B + 8) : kRingBytes;
 }
 template <int B, int PFIX>
 using ReduceLayoutFor = ReduceLayout<B, reduce_mul(PFIX), reduce_lcodes(B, PFIX), reduce_ring(B, PFIX), PFIX>;
@@ -495,34 +496,35 @@ KernelInfo info_for_block(int block)
     }
 }
 
+template <int PFIX>
+KernelInfo info_for_code(int block, int code)
+{
+    switch (code) {
+    case 0: return info_for_block<0, PFIX>(block);
+    case 1: return info_for_block<1, PFIX>(block);
+    case 2: return info_for_block<2, PFIX>(block);
+    default: return KernelInfo{};
+    }
+}
+
 }  // namespace
 
 KernelInfo reduce_kernel_info(int block, int code, int num_shards)
 {
-    // Tensor-parallel degrees 2, 4 and 16 (the owner reduces that many
-    // segments) have kernels with the shard loop unrolled, 2 and 4 with longer
-    // tiles, for the method's E4M3 codes.
-    if (TACO_REDUCE_FIXED_SHARDS && code == 0 && (num_shards == 2 || num_shards == 4))
-        return num_shards == 2 ? info_for_block<0, 2>(block) : info_for_block<0, 4>(block);
-    // 16 shards: the same with tiles half as long (two stages would fit otherwise).
-    if (TACO_REDUCE_FIXED_SHARDS && code == 0 && num_shards == 16)
-        return info_for_block<0, 16>(block);
-    // The 8-shard case has kernels with the shard loop unrolled, for every
-    // code format and block size.
-    if (TACO_REDUCE_FIXED_SHARDS && num_shards == 8) {
-        switch (code) {
-        case 0: return info_for_block<0, 8>(block);
-        case 1: return info_for_block<1, 8>(block);
-        case 2: return info_for_block<2, 8>(block);
-        default: return KernelInfo{};
+    // The tensor-parallel degrees 2, 4, 8 and 16 (the owner reduces that many
+    // segments) have kernels with the shard loop unrolled, for every code
+    // format and block size: 2 and 4 with 32 codes per thread, 16 with a ring
+    // of exactly three stages.  Other counts take the generic kernel.
+    if (TACO_REDUCE_FIXED_SHARDS) {
+        switch (num_shards) {
+        case 2: return info_for_code<2>(block, code);
+        case 4: return info_for_code<4>(block, code);
+        case 8: return info_for_code<8>(block, code);
+        case 16: return info_for_code<16>(block, code);
+        default: break;
         }
     }
-    switch (code) {
-    case 0: return info_for_block<0>(block);
-    case 1: return info_for_block<1>(block);
-    case 2: return info_for_block<2>(block);
-    default: return KernelInfo{};
-    }
+    return info_for_code<0>(block, code);
 }
 
 cudaError_t launch_reduce(int block, int code, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream)
