@@ -94,11 +94,10 @@ void init_device(DeviceState &st)
             if (e == cudaSuccess)
                 e = init_kernel(warp_codec_info(blocks[i], false, 0), &st.ctas_per_sm);
         }
+        const int reduce_shards[6] = {1, 2, 4, 5, 8, 16};   // every reduce kernel: generic up to 4, 2, 4, generic, 8, 16
         for (int code = 0; code < 3 && e == cudaSuccess; code++)
-            e = init_kernel(reduce_kernel_info(blocks[i], code, 1), &st.ctas_per_sm);
-        for (int code = 0; code < 3 && e == cudaSuccess; code++)
-            for (int shards = 2; shards <= 16 && e == cudaSuccess; shards *= 2)
-                e = init_kernel(reduce_kernel_info(blocks[i], code, shards), &st.ctas_per_sm);
+            for (int k = 0; k < 6 && e == cudaSuccess; k++)
+                e = init_kernel(reduce_kernel_info(blocks[i], code, reduce_shards[k]), &st.ctas_per_sm);
     }
     st.init_error = e;
 }

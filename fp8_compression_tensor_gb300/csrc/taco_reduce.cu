@@ -140,18 +140,21 @@ struct ReduceLayout {
 };
 
 // The layout of the reduce kernel for block B, code format CODE and shard
-// count PFIX (0: any count).
+// count PFIX (0: any count; -4: any count up to 4, which takes the 2- and
+// 4-shard kernels' 32 codes per thread).
 __host__ __device__ constexpr int reduce_mul(int pfix) { return pfix == 2 ? 2 : 1; }
 __host__ __device__ constexpr int reduce_lcodes(int B, int pfix)
 {
-    return pfix == 2 || pfix == 4 ? 32 : pfix == 16 && B < 64 ? 8 : 0;
+    return pfix == 2 || pfix == 4 || pfix == -4 ? 32 : pfix == 16 && B < 64 ? 8 : 0;
 }
+__host__ __device__ constexpr int reduce_maxp(int pfix) { return pfix < 0 ? -pfix : pfix; }
 __host__ __device__ constexpr int reduce_ring(int B, int pfix)
 {
     return (pfix == 16 || pfix == 0) && B >= 64 ? 3 * 16 * (kConsumers * 16 / B) * (B + 8) : kRingBytes;
 }
 template <int B, int PFIX>
-using ReduceLayoutFor = ReduceLayout<B, reduce_mul(PFIX), reduce_lcodes(B, PFIX), reduce_ring(B, PFIX), PFIX>;
+using ReduceLayoutFor =
+    ReduceLayout<B, reduce_mul(PFIX), reduce_lcodes(B, PFIX), reduce_ring(B, PFIX), reduce_maxp(PFIX)>;
 
 // Values of the four codes in `x`, first code in .x of the first pair.
 template <int CODE>
@@ -200,7 +203,8 @@ __device__ __forceinline__ uint2 ldg_u2(const uint8_t *p)
     return *reinterpret_cast<const uint2 *>(p);
 }
 
-// PFIX > 0: the shard count is fixed at compile time (the shard loop unrolls).
+// PFIX > 0: the shard count is fixed at compile time (the shard loop unrolls);
+// 0 or -4: the count is the call's (any, or at most 4).
 template <int B, int CODE, int PFIX>
 __global__ void __launch_bounds__(kRThreads, 1) taco_shard_reduce_kernel(const ReduceArgs args, uint32_t *fault)
 {
@@ -514,7 +518,9 @@ KernelInfo reduce_kernel_info(int block, int code, int num_shards)
     // The tensor-parallel degrees 2, 4, 8 and 16 (the owner reduces that many
     // segments) have kernels with the shard loop unrolled, for every code
     // format and block size: 2 and 4 with 32 codes per thread, 16 with a ring
-    // of exactly three stages.  Other counts take the generic kernel.
+    // of exactly three stages.  Other counts take a generic kernel: 1 and 3
+    // the one with 32 codes per thread (16384 x 8192, 3 shards: 54.3 -> 33.2 us),
+    // 5 to 15 the one with 16.
     if (TACO_REDUCE_FIXED_SHARDS) {
         switch (num_shards) {
         case 2: return info_for_code<2>(block, code);
@@ -524,7 +530,7 @@ KernelInfo reduce_kernel_info(int block, int code, int num_shards)
         default: break;
         }
     }
-    return info_for_code<0>(block, code);
+    return num_shards <= 4 ? info_for_code<-4>(block, code) : info_for_code<0>(block, code);
 }
 
 cudaError_t launch_reduce(int block, int code, const ReduceArgs &args, uint32_t *fault, int grid, cudaStream_t stream)
