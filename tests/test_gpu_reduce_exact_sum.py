@@ -14,6 +14,9 @@ follow from the rotated-domain reading of the reduce (compressing
   s'    = fl(fl(alpha' * max|W|) / Q_max)     exactly, alpha' read back
   alpha' = tau / sqrt(|W|^2 / B + eps)        within 1e-6 (FP32 energy order)
 
+and for the ablations the same W with their own last step (the test's
+docstring below).
+
 A fused multiply-add in place of the separately rounded product changes W by
 an ulp here and there, and so max|W| and s' in a fifth of the blocks: this
 test sees it where the oracle-tolerance comparisons cannot.  Every fifth
@@ -92,30 +95,52 @@ def float32_sum(shards, B, code):
     return W
 
 
+VARIANTS = {0: "ash_ds", 1: "hadamard_ds", 2: "ds_only", 3: "ash_only"}
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 @pytest.mark.parametrize("code", [0, 1, 2])
 @pytest.mark.parametrize("P", [2, 3, 4, 8, 16])
 @pytest.mark.parametrize("B", [32, 64, 128, 256, 512])
-def test_reduce_is_the_float32_sum_of_rounded_products(taco, B, P, code):
+def test_reduce_is_the_float32_sum_of_rounded_products(taco, B, P, code, variant):
+    """The method (variant 0) and the ablations, whose outputs differ only in
+    the last step: standard Hadamard + DS takes alpha' = 1; DS only codes
+    W / s' correctly rounded with s' = fl(max|W| / Q_max) and alpha' = 1; ASH
+    only stores s' = 1 and codes Cvt(fl(W * alpha'))."""
     shards, tiny = crafted_shards(P, B, code, seed=1000 * B + 10 * P + code)
-    got = taco.reduce_shards([torch.from_numpy(s).to(DEV) for s in shards], NBLK, B, B, code=code).cpu().numpy()
+    got = taco.reduce_shards([torch.from_numpy(s).to(DEV) for s in shards], NBLK, B, B,
+                             variant=VARIANTS[variant], code=code).cpu().numpy()
     cg, ag, sg = records(got, B)
     W = float32_sum(shards, B, code)
     wmax = np.max(np.abs(W), axis=1)
     zero = wmax == 0
     assert np.all(zero[:10]) and not np.any(zero[10:])
-    # W = 0: the all-zero record.
-    assert np.all(cg[zero] == 0) and np.all(sg[zero] == 0)
+    # W = 0: all codes zero; s' = 0 (1 for ASH only, which stores no scale).
+    assert np.all(cg[zero] == 0) and np.all(sg[zero] == (1.0 if variant == 3 else 0.0))
     nz = ~zero
-    qmax = np.float32(QMAX[code])
-    kq = (qmax / wmax[nz]).astype(np.float32)
-    u = (W[nz] * kq[:, None]).astype(np.float32)
+    f32 = np.float32
+    qmax = f32(QMAX[code])
+    ag32 = ag[nz].astype(np.float32)
+    if variant == 3:
+        u = (W[nz] * ag32[:, None]).astype(np.float32)
+        s_want = np.ones(int(nz.sum()), np.float32)
+    elif variant == 2:
+        s_want = (wmax[nz] / qmax).astype(np.float32)
+        u = (W[nz] / s_want[:, None]).astype(np.float32)
+    else:
+        alpha = ag32 if variant == 0 else np.ones_like(ag32)
+        kq = (qmax / wmax[nz]).astype(np.float32)
+        u = (W[nz] * kq[:, None]).astype(np.float32)
+        s_want = ((alpha * wmax[nz]).astype(np.float32) / qmax).astype(np.float32)
     want = oracle.code_encode(code, u).reshape(u.shape)
     bad = np.argwhere(cg[nz] != want)
     assert bad.size == 0, f"{len(bad)} codes differ, first (block, element) {bad[:4].tolist()}"
-    s_want = ((ag[nz] * wmax[nz]).astype(np.float32) / qmax).astype(np.float32)
     bad = np.nonzero(sg[nz] != s_want)[0]
     assert bad.size == 0, f"{bad.size} of {nz.sum()} scales differ (tiny blocks among them: {int(tiny[nz][bad].sum())})"
-    Wd = W.astype(np.float64)
-    a_exact = TAU / np.sqrt((Wd * Wd).sum(axis=1) / B + EPS)
-    assert np.max(np.abs(ag[nz] / a_exact[nz] - 1.0)) <= 1e-6
+    if variant in (0, 3):
+        Wd = W.astype(np.float64)
+        a_exact = TAU / np.sqrt((Wd * Wd).sum(axis=1) / B + EPS)
+        assert np.max(np.abs(ag[nz] / a_exact[nz] - 1.0)) <= 1e-6
+    else:
+        assert np.all(ag == 1.0)
     assert taco.device_status() == 0
